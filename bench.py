@@ -1,0 +1,418 @@
+"""Benchmark of the per-token adapter routing hot path on one GB300 (or N, one rank per GPU).
+
+Workload: the 4-modality kernel benchmark of "MoLoRA: Composable Specialization via
+Per-Token Adapter Routing" (Table 3: K = 4 modalities, 2048 tokens, d = 4096), with rank 16,
+bf16 x / A / B, fp32 y updated in place, tokens in runs of geometric length (mean 64) with one
+uniformly drawn modality (vocabulary range) per run; synthetic, seeded.
+
+One step = the whole path over one batch: vocabulary routing -> dispatch (histogram, scan,
+permutation) -> grouped LoRA apply, as two CUDA graphs (route+dispatch, apply) with CUDA
+events around each.  Between timed steps a 256 MiB buffer (about twice the 129 MB L2) is
+written so every step starts with cold caches.  ``value`` = tokens / mean step time;
+``apply_only`` gives the same for the apply kernel alone, and ``roofline`` relates that
+kernel's algorithmic bytes per launch (x read once, y read and written once, the adapters
+it touches read once) to its measured duration.  ``e2e`` runs the same path through the
+public calls with the step's inputs copied from pinned host memory and y copied back
+inside the timed region.  ``cpu_baseline`` times the CPU oracle (single thread) on the same
+inputs.
+
+Multi-GPU: tokens are independent, so each rank runs its own batch (weak scaling, no
+collective on the data path); the step time is the max over ranks.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "per-token LoRA apply tokens/s (2048 tok, d=4096, K=4); % of HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "modality4"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--path", choices=["auto", "grouped", "scalar"], default="grouped")
+    p.add_argument("--soak-s", type=float, default=1.0, help="untimed seconds of steps while clocks settle")
+    p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, world: int, step_seconds_max: float, steps: int) -> dict:
+    """Whole-job throughput: every rank processes its own batch each step; the job's step
+    time is the slowest rank's."""
+    ms = step_seconds_max / steps * 1e3
+    return {"value": tokens_per_rank * world * steps / step_seconds_max, "ms_per_step": ms}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu_index}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- the GPU arm
+
+def algorithmic_bytes(wl, n_active_adapters: int) -> int:
+    """Bytes the apply must move at least once: x read, y read + written, the active
+    adapters' A and B read, ids + permutation read."""
+    x = wl.N * wl.d_in * wl.x.element_size()
+    y = 2 * wl.N * wl.d_out * 4
+    ab = n_active_adapters * (wl.d_in * wl.r + wl.r * wl.d_out) * wl.A.element_size()
+    idx = 2 * wl.N * wl.k * 4 + (wl.K + 1) * 4
+    return x + y + ab + idx
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def run_ours(args, rank, world, local):
+    import token_adapter_routing_gb300 as m
+    from token_adapter_routing_gb300 import build as lib_build
+
+    lib_build.build()
+    m.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+
+    wl = workloads.make(WORKLOAD, seed=1234 + 1 + rank * 1000)
+    tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+    x, A, B = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev)
+    y = wl.y0.to(dev)
+    adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+    counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+    offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    g_rd, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        # eager run first (loads the module, sets kernel attributes), then capture
+        m.molora_route_vocab(tok, starts, adapter=adapter, err_word=err)
+        m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm, err_word=err)
+        m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
+                            err_word=err, path=args.path)
+        stream.synchronize()
+        with torch.cuda.graph(g_rd, stream=stream):
+            m.molora_route_vocab(tok, starts, adapter=adapter, err_word=err)
+            m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm, err_word=err)
+        with torch.cuda.graph(g_apply, stream=stream):
+            m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
+                                err_word=err, path=args.path)
+    n_active = int((torch.bincount(adapter.cpu().long(), minlength=wl.K) > 0).sum().item())
+    launches_per_step = 3  # route_vocab, dispatch, apply
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        g_rd.replay()
+        if evs is not None:
+            evs[1].record(stream)
+        g_apply.replay()
+        if evs is not None:
+            evs[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            step()
+        stream.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        t_end = time.time() + args.soak_s
+        while time.time() < t_end:
+            for _ in range(50):
+                flush.zero_()
+                step()
+            stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()  # outside the events: each step starts with a cold L2
+            step(evs[i])
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    apply_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    apply_s = max_over_ranks(sum(apply_ms) / 1e3, world, dev)
+    agg = aggregate(wl.N, world, total_s, args.steps)
+
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x}"
+
+    peaks, peak_kind = measured_peaks()
+    algo = algorithmic_bytes(wl, n_active)
+    apply_mean_s = apply_s / args.steps
+    achieved_gbs = algo / apply_mean_s / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "traffic": None, "peak_kind": peak_kind,
+            "kernel": "lora_grouped_kernel" if args.path != "scalar" else "lora_scalar_kernel",
+            "algorithmic_bytes_per_launch": algo, "launch_us_mean": round(apply_mean_s * 1e6, 3),
+            "launch_us_p50": round(statistics.median(apply_ms) * 1e3, 3),
+            "launch_us_p99": round(sorted(apply_ms)[min(len(apply_ms) - 1, int(0.99 * len(apply_ms)))] * 1e3, 3),
+            "frac_of_8TBs": round(achieved_gbs / 8000.0, 4)}
+    traffic = load_profiled_traffic(args.path)
+    if traffic is not None:
+        roof["traffic"] = traffic
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(m, wl, dev, args, world)
+
+    result = {
+        "metric": METRIC, "value": round(agg["value"], 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "4-modality kernel benchmark: N=2048 tokens, d_in=d_out=4096, K=4, r=16, "
+                               "bf16 x/A/B, fp32 y, vocabulary routing, geometric runs (mean 64)",
+                   "global_batch": wl.N * world, "tokens_per_rank": wl.N, "path": args.path,
+                   "step": "route_vocab -> dispatch -> lora_apply (2 CUDA graphs)",
+                   "l2": "256 MiB buffer written between timed steps (outside the timed events)",
+                   "parallelism": f"dp{world}" if world > 1 else "single-gpu"},
+        "apply_only": {"value": round(wl.N * world / apply_mean_s, 1), "unit": UNIT,
+                       "us_per_launch": round(apply_mean_s * 1e6, 3)},
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    return result
+
+
+def run_e2e(m, wl, dev, args, world):
+    """Public calls with host buffers: H2D of the step's inputs, the path, D2H of y."""
+    tok_h = wl.tok.pin_memory()
+    x_h = wl.x.pin_memory()
+    y0_h = wl.y0.pin_memory()
+    y_h = torch.empty_like(y0_h).pin_memory()
+    starts = wl.starts.to(dev)
+    A, B = wl.A.to(dev), wl.B.to(dev)  # the hot set stays resident
+    tok = torch.empty_like(wl.tok, device=dev)
+    x = torch.empty_like(wl.x, device=dev)
+    y = torch.empty_like(wl.y0, device=dev)
+    adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+    counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+    offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one():
+        tok.copy_(tok_h, non_blocking=True)
+        x.copy_(x_h, non_blocking=True)
+        y.copy_(y0_h, non_blocking=True)
+        m.molora_route_vocab(tok, starts, adapter=adapter)
+        m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm)
+        m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
+                            path=args.path)
+        y_h.copy_(y, non_blocking=True)
+
+    steps = max(5, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        stream.synchronize()
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    h2d = tok_h.numel() * 4 + x_h.numel() * x_h.element_size() + y0_h.numel() * 4
+    d2h = y_h.numel() * 4
+    return {"value": round(wl.N * world * steps / sec, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(sec / steps * 1e3, 4)}
+
+
+def load_profiled_traffic(path):
+    """DRAM bytes per apply launch from the committed ncu summary, if it matches this kernel."""
+    fn = os.path.join(ROOT, "profiles", "lora_grouped_kernel_modality4.json")
+    if path == "scalar" or not os.path.exists(fn):
+        return None
+    try:
+        with open(fn) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_step(wl):
+    import oracle
+    adapter, _ = oracle.route_vocab(wl.tok, wl.starts)
+    counts, offsets, perm, _ = oracle.dispatch(adapter, wl.K)
+    y, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter, wl.y0, wl.scale)
+    return y
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle as it stands, single-threaded, on the full batch, repeated for ~budget_s."""
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(wl)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": round(wl.N * reps / el, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full batch ({wl.N} tokens: route_vocab + dispatch + lora_apply in double) x {reps} reps, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, as it stands, on this arm's workload and metric."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = workloads.make(WORKLOAD, seed=1234 + 1)
+    for _ in range(max(0, args.warmup)):
+        oracle_step(wl)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(wl)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = wl.N * args.steps / total
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "4-modality kernel benchmark: N=2048 tokens, d_in=d_out=4096, K=4, r=16, "
+                                   "bf16 x/A/B, fp32 y, vocabulary routing, geometric runs (mean 64)",
+                       "global_batch": wl.N, "implementation": "CPU oracle (plain C, double, one thread)"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"full batch of {wl.N} tokens per step, {args.steps} steps"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,209 @@
+/*
+ * molora.h -- C ABI of the GB300 (sm_103a) per-token adapter routing library.
+ *
+ * The method is "MoLoRA: Composable Specialization via Per-Token Adapter Routing"
+ * (Shah & Wagle).  Its pages define the path this library runs:
+ *   - Table 1: two routing decisions, vocabulary ranges R_vocab(v) (O(1) per token) and a
+ *     learned router TopK(g(x)) (O(64d + 64K) per token), followed by infrastructure both
+ *     share: histogram computation, pointer arrays, grouped GEMM dispatch.
+ *   - Figure 2: the top-k selected adapters are combined by a weighted sum; in execution,
+ *     tokens are grouped by their selected adapter and the groups run as grouped GEMMs.
+ *   - Table 10: adapter weight shapes A: (K, d, r) and B: (K, r, d).
+ *   - Figure 4: adapters live in a GPU-resident hot set at fixed addresses, so the whole
+ *     sequence can be captured in one CUDA graph.
+ *   - Tables 3 and 7: the per-sequence alternative runs K masked passes (K*N token-work
+ *     against N for per-token routing).
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers owned by the caller (for example torch tensors).
+ *     The library never allocates, frees or synchronises inside a call: each call only
+ *     enqueues kernels on `stream`, so a sequence of calls can be captured in a CUDA graph.
+ *     Pointers must stay valid until the enqueued work completes.
+ *   - All arrays are dense and row-major; slot s = t*k + j is token t's j-th choice.
+ *   - Sizes are validated on the host before anything is launched; a bad argument returns
+ *     MOLORA_ERR_INVALID_ARG (or MOLORA_ERR_UNSUPPORTED for a valid but unimplemented
+ *     shape) and launches nothing.  MOLORA_ERR_CUDA means a launch failed; call
+ *     cudaGetLastError() for the detail.
+ *   - Conditions only the device can see (an id outside [0, K), a token outside every
+ *     vocabulary range, ranges that do not increase, an inconsistent permutation, a wait
+ *     that ran out of time) are OR-ed into *err_word (a device int32 the caller zeroes; may
+ *     be NULL to ignore them) with the MOLORA_DEV_* bits below.  The offending slot or
+ *     token is skipped; no kernel traps or aborts.
+ *   - Empty inputs (N == 0) are valid and launch nothing (apart from writing the empty
+ *     histogram in molora_dispatch).
+ */
+#ifndef MOLORA_H_
+#define MOLORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOLORA_API __attribute__((visibility("default")))
+#else
+#define MOLORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOLORA_OK = 0,
+  MOLORA_ERR_INVALID_ARG = 1,
+  MOLORA_ERR_UNSUPPORTED = 2,
+  MOLORA_ERR_CUDA = 3
+} molora_status;
+
+typedef enum { MOLORA_F32 = 0, MOLORA_BF16 = 1 } molora_dtype;
+
+/* Which kernel family molora_lora_apply_ex uses.  AUTO picks by the measured crossover
+ * between the two (Figures 5 and 9 put it near batch 160 on the paper's hardware; this
+ * library measures its own and stores the result in its dispatch table). */
+typedef enum {
+  MOLORA_PATH_AUTO = 0,
+  MOLORA_PATH_SCALAR = 1,  /* CUDA-core, token-major, one CTA per token (the memory-bound regime) */
+  MOLORA_PATH_GROUPED = 2  /* grouped tcgen05 shrink + expand over the dispatch permutation */
+} molora_path;
+
+/* Device-side error bits OR-ed into *err_word. */
+#define MOLORA_DEV_TOKEN_OUTSIDE_RANGES 0x1 /* route_vocab: token in no range; adapter = -1 */
+#define MOLORA_DEV_BAD_RANGES 0x2           /* route_vocab: starts not strictly increasing */
+#define MOLORA_DEV_BAD_ADAPTER_ID 0x4       /* dispatch / apply: id outside [0, K); slot skipped */
+#define MOLORA_DEV_BAD_PERMUTATION 0x8      /* apply: offsets or perm inconsistent; entry skipped */
+#define MOLORA_DEV_WAIT_TIMEOUT 0x10        /* a bounded on-chip wait ran out; work abandoned */
+
+#define MOLORA_MAX_ADAPTERS 64   /* K: hot-set size limit (the decode sweep goes to 64) */
+#define MOLORA_ROUTER_HIDDEN 64  /* hidden width of the learned router (Table 1 cost term 64d) */
+
+/*
+ * molora_route_vocab -- vocabulary routing R_vocab(v) (Table 1; Table 12 "disjoint vocab").
+ *
+ *   adapter[t] = a   where starts[a] <= tok[t] < starts[a+1]
+ *   adapter[t] = -1  if tok[t] lies in no range (sets MOLORA_DEV_TOKEN_OUTSIDE_RANGES)
+ *
+ * tok     int32 [N]     token ids
+ * starts  int32 [K+1]   strictly increasing range starts; adapter a owns [starts[a], starts[a+1])
+ * K       1..MOLORA_MAX_ADAPTERS
+ * adapter int32 [N]     output
+ */
+MOLORA_API molora_status molora_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                 int32_t* adapter, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * molora_router_topk -- learned router TopK(g(x)) (Table 1; Figure 2 with k = 2;
+ * Table 10's softmax(Wx + b) gating), hidden width 64:
+ *
+ *   hidden = ReLU(x W1 + b1)                       [N x 64], fp32 accumulation
+ *   logits = hidden W2 + b2                        [N x K], fp32
+ *   ids[t] = the k adapters with the largest logits, ordered by logit descending;
+ *            equal logits order by the lower index first
+ *   w[t,j] = exp(logits[t,ids[t,j]] - m) / sum over the k selected of exp(logit - m),
+ *            m = the largest selected logit (the softmax renormalised over the top k)
+ *
+ * x       [N x d_in]  dtype (MOLORA_BF16 or MOLORA_F32), row-major
+ * W1      [d_in x 64] same dtype;   b1 fp32 [64] or NULL (zero)
+ * W2      [64 x K]    same dtype;   b2 fp32 [K]  or NULL (zero)
+ * K       1..MOLORA_MAX_ADAPTERS;   k  1..K
+ * logits  fp32 [N x K] output, or NULL to skip storing it
+ * ids     int32 [N x k] output;  w  fp32 [N x k] output
+ * bf16 x with d_in a multiple of 64 runs on the tcgen05 tensor cores; other shapes and fp32
+ * run on CUDA cores.
+ */
+MOLORA_API molora_status molora_router_topk(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                 const void* W1, const float* b1, const void* W2, const float* b2,
+                                 int32_t K, int32_t k, float* logits, int32_t* ids, float* w,
+                                 cudaStream_t stream);
+
+/*
+ * molora_dispatch -- histogram, pointer arrays and grouping (Table 1 rows "Histogram
+ * computation" and "Pointer arrays"; Figure 2 right "tokens are grouped by their selected
+ * adapter").  Over the S = N*k slots:
+ *
+ *   counts[a]   = number of slots s with ids[s] == a
+ *   offsets[0]  = 0,  offsets[a+1] = offsets[a] + counts[a]
+ *   perm[offsets[a] + q] = the q-th slot, in ascending s, whose id is a   (stable)
+ *   perm[offsets[K] .. S-1] = -1
+ *
+ * Slots with an id outside [0, K) are left out and set MOLORA_DEV_BAD_ADAPTER_ID.
+ * Deterministic and bit-exact: one CTA, no atomics whose order matters.
+ * ids int32 [N x k];  counts int32 [K];  offsets int32 [K+1];  perm int32 [N*k]
+ */
+MOLORA_API molora_status molora_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts,
+                              int32_t* offsets, int32_t* perm, int32_t* err_word,
+                              cudaStream_t stream);
+
+/*
+ * molora_lora_apply -- batched per-token LoRA apply over the hot set (Figure 2; Table 10
+ * shapes; Figure 4 hot set):
+ *
+ *   y[t,:] += scale * sum_j w[t,j] * (x[t,:] A_{ids[t,j]}) B_{ids[t,j]}
+ *
+ * x       [N x d_in]      dtype, row-major
+ * A       [K x d_in x r]  dtype, the hot set's down-projections, contiguous, fixed address
+ * B       [K x r x d_out] dtype, the hot set's up-projections, contiguous, fixed address
+ * r       8, 16, 32 or 64
+ * ids     int32 [N x k]   adapter per slot (from molora_route_vocab with k = 1, or
+ *                         molora_router_topk)
+ * w       fp32 [N x k]    slot weights, or NULL for all ones
+ * counts, offsets, perm   molora_dispatch's outputs for these ids (read by the grouped
+ *                         path; the scalar path reads ids directly and ignores them)
+ * y       fp32 [N x d_out], updated in place (read-modify-write)
+ *
+ * Accumulation is fp32 (tensor cores or FMA); x, A, B are read as given.  The grouped path
+ * needs bf16 and r >= 16; anything else runs on the scalar path.  With k > 1 the grouped
+ * path adds each slot's contribution to y with an fp32 reduction in L2, so the order of the
+ * k additions (and therefore the last bits of y) may vary from run to run; with k = 1 and
+ * on the scalar path every element of y is written exactly once and results are
+ * reproducible bit for bit.
+ */
+MOLORA_API molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                int32_t d_out, const void* A, const void* B, int32_t K, int32_t r,
+                                const int32_t* ids, const float* w, int32_t k,
+                                const int32_t* counts, const int32_t* offsets,
+                                const int32_t* perm, float scale, float* y, int32_t* err_word,
+                                cudaStream_t stream);
+
+/* molora_lora_apply with an explicit kernel family (used to measure the crossover).
+ * MOLORA_PATH_GROUPED on an unsupported shape returns MOLORA_ERR_UNSUPPORTED. */
+MOLORA_API molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                   int32_t d_out, const void* A, const void* B, int32_t K,
+                                   int32_t r, const int32_t* ids, const float* w, int32_t k,
+                                   const int32_t* counts, const int32_t* offsets,
+                                   const int32_t* perm, float scale, float* y, int32_t* err_word,
+                                   molora_path path, cudaStream_t stream);
+
+/*
+ * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:
+ * per-sequence routing needs K passes for a K-modality batch).  Adapter `a` is evaluated
+ * for EVERY token; the result is multiplied by the 0/1 mask [adapter_of[t] == a]:
+ *
+ *   y[t,:] += [adapter_of[t] == a] * scale * (x[t,:] A_a) B_a
+ *
+ * Running it for a = 0..K-1 reproduces molora_lora_apply with k = 1 at K times the work.
+ * It exists only as the comparison baseline.  adapter_of int32 [N]; 0 <= a < K.
+ */
+MOLORA_API molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, int64_t N,
+                                            int32_t d_in, int32_t d_out, const void* A,
+                                            const void* B, int32_t K, int32_t r,
+                                            const int32_t* adapter_of, int32_t a, float scale,
+                                            float* y, int32_t* err_word, molora_path path,
+                                            cudaStream_t stream);
+
+/* The kernel family molora_lora_apply would choose for this shape (never AUTO). */
+MOLORA_API molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                               int32_t K, int32_t r, int32_t k);
+
+/* Short text for a status code (static storage). */
+MOLORA_API const char* molora_status_string(molora_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+MOLORA_API int32_t molora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOLORA_H_ */

@@ -1,0 +1,349 @@
+"""GPU parity: every step of the path, called through the C ABI, against the CPU oracle.
+
+Bars (from the method's definition and the arithmetic):
+  * routing ids, histograms, offsets and permutations: bit-exact;
+  * learned top-k: ids exact on tokens whose k-th vs (k+1)-th oracle logit gap exceeds 1e-3,
+    weights within 1e-5 relative, logits within 1e-4 absolute + 1e-4 relative (fp32
+    accumulation of bf16 products against the oracle's double);
+  * LoRA apply (bf16 in, fp32 accumulate): max|dy| <= 1e-2 * rms(oracle y).  Each case also
+    checks a tight bound of 2e-4 * rms(oracle y): fp32 accumulation over d_in <= 4096 terms
+    (and the grouped path's two-bf16 split of the shrink output, relative error 2^-17) stays
+    far below it, while a dropped term, a wrong weight or a wrong adapter does not;
+  * small-integer inputs (every partial sum exact in fp32): bit-exact on both paths.
+"""
+
+import math
+
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_CONTRACT = 1e-2
+TOL_TIGHT = 2e-4
+
+
+@pytest.fixture(scope="module")
+def m():
+    from token_adapter_routing_gb300 import build
+    build.build()
+    import token_adapter_routing_gb300 as mod
+    mod.load_library()
+    return mod
+
+
+def dev(t):
+    return None if t is None else t.cuda().contiguous()
+
+
+def err_word():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def assert_apply_close(y_gpu, y_ref, tight=True):
+    y_gpu = y_gpu.cpu().double()
+    y_ref = y_ref.double()
+    rms = y_ref.pow(2).mean().sqrt().item()
+    err = (y_gpu - y_ref).abs().max().item()
+    assert err <= TOL_CONTRACT * rms, f"max|dy| {err:.3e} > 1e-2 rms ({rms:.3e})"
+    if tight:
+        assert err <= TOL_TIGHT * rms, f"max|dy| {err:.3e} > 2e-4 rms ({rms:.3e})"
+
+
+def grouped_available(m, wl, k):
+    return m.molora_select_path(wl.dtype, 4096, wl.d_in, wl.d_out, wl.K, wl.r, k) == "grouped"
+
+
+PATHS = ["scalar", "grouped"]
+
+
+def run_vocab_path(m, wl, path):
+    """route -> dispatch -> apply on the GPU; returns (adapter, counts, offsets, perm, y, err)."""
+    e = err_word()
+    tok, starts = dev(wl.tok), dev(wl.starts)
+    adapter = m.molora_route_vocab(tok, starts, err_word=e)
+    counts, offsets, perm = m.molora_dispatch(adapter, wl.K, err_word=e)
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), adapter, y, wl.scale, counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    return adapter, counts, offsets, perm, y, int(e.item())
+
+
+# ------------------------------------------------------------------------- routing / dispatch
+
+@pytest.mark.parametrize("name,kw", [("tiny_vocab", {}), ("modality4", {}), ("decode_sweep", {"N": 512, "K": 64}),
+                                     ("decode_sweep", {"N": 300, "K": 7, "dist": "zipf"})])
+def test_route_vocab_bitexact(m, name, kw):
+    wl = workloads.make(name, **kw)
+    e = err_word()
+    got = m.molora_route_vocab(dev(wl.tok), dev(wl.starts), err_word=e).cpu()
+    ref, n_out = oracle.route_vocab(wl.tok, wl.starts)
+    assert torch.equal(got, ref)
+    assert int(e.item()) == 0 and n_out == 0
+
+
+def test_route_vocab_outside_and_bad_ranges(m):
+    starts = torch.tensor([10, 20, 35, 50], dtype=torch.int32)
+    tok = torch.tensor([10, 19, 20, 34, 35, 49, 50, 9, -5, 1 << 30], dtype=torch.int32)
+    e = err_word()
+    got = m.molora_route_vocab(dev(tok), dev(starts), err_word=e).cpu()
+    ref, n_out = oracle.route_vocab(tok, starts)
+    assert torch.equal(got, ref) and n_out == 4
+    assert int(e.item()) == m.DEV_TOKEN_OUTSIDE_RANGES
+    e2 = err_word()
+    m.molora_route_vocab(dev(tok), dev(torch.tensor([0, 30, 20, 40], dtype=torch.int32)), err_word=e2)
+    torch.cuda.synchronize()
+    assert int(e2.item()) & m.DEV_BAD_RANGES
+
+
+@pytest.mark.parametrize("N,k,K,invalid", [(0, 1, 4, False), (1, 1, 1, False), (2048, 1, 4, False),
+                                           (4096, 2, 4, False), (8192, 4, 8, False), (3001, 3, 64, False),
+                                           (777, 2, 5, True), (100000, 1, 64, False)])
+def test_dispatch_bitexact(m, N, k, K, invalid):
+    g = torch.Generator().manual_seed(N * 7 + k * 3 + K)
+    lo = -1 if invalid else 0
+    hi = K + 1 if invalid else K
+    ids = torch.randint(lo, hi, (N, k), generator=g, dtype=torch.int32)
+    e = err_word()
+    counts, offsets, perm = m.molora_dispatch(dev(ids), K, err_word=e)
+    rc, ro, rp, n_inv = oracle.dispatch(ids, K)
+    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+    assert (int(e.item()) == m.DEV_BAD_ADAPTER_ID) == (n_inv > 0)
+
+
+def test_dispatch_all_on_one_adapter(m):
+    ids = torch.full((5000, 1), 3, dtype=torch.int32)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), 8)
+    rc, ro, rp, _ = oracle.dispatch(ids, 8)
+    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+
+
+# ------------------------------------------------------------------------- apply
+
+def small_int_case(N, d_in, d_out, K, r, k, seed, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(-3, 4, (N, d_in), generator=g).to(dtype)
+    A = torch.randint(-2, 3, (K, d_in, r), generator=g).to(dtype)
+    B = torch.randint(-2, 3, (K, r, d_out), generator=g).to(dtype)
+    y0 = torch.randint(-8, 9, (N, d_out), generator=g).to(torch.float32)
+    ids = torch.stack([torch.randperm(K, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = (2.0 ** torch.randint(-3, 1, (N, k), generator=g)).to(torch.float32)
+    return x, A, B, y0, ids, w
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("N,d_in,d_out,K,r,k", [(200, 128, 256, 4, 16, 1), (130, 256, 128, 3, 32, 2),
+                                                (64, 64, 64, 8, 64, 4), (301, 192, 320, 5, 16, 1)])
+def test_apply_small_integers_bitexact(m, path, N, d_in, d_out, K, r, k):
+    x, A, B, y0, ids, w = small_int_case(N, d_in, d_out, K, r, k, N + d_in + r)
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 0.5, w)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), K)
+    y = dev(y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 0.5, w=dev(w), counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(y.cpu(), y_ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name,kw", [
+    ("modality4", {}),                                     # the 4-modality benchmark at full size
+    ("modality4", {"N": 1000, "d_in": 1024, "d_out": 3072}),
+    ("decode_sweep", {"N": 160, "K": 16}),
+    ("decode_sweep", {"N": 257, "K": 64, "dist": "zipf"}),
+    ("decode_sweep", {"N": 1, "K": 4}),
+    ("modality4", {"N": 333, "d_in": 2048, "d_out": 1024, "r": 32}),
+    ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048, "r": 64, "K": 8}),
+])
+def test_apply_vocab_routed_vs_oracle(m, path, name, kw):
+    wl = workloads.make(name, **kw)
+    adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, path)
+    assert e == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    assert_apply_close(y, y_ref)
+
+
+def test_apply_tiny_vocab_fp32(m):
+    wl = workloads.make("tiny_vocab")
+    adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, "scalar")
+    assert e == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    assert_apply_close(y, y_ref)
+    # auto must pick the scalar path for fp32 and still match
+    _, _, _, _, y2, _ = run_vocab_path(m, wl, "auto")
+    assert torch.equal(y2.cpu(), y.cpu())
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_apply_topk_weighted_vs_oracle(m, path, k):
+    # top-k slots with router-like weights, rank 64, K = 8, a ragged N
+    wl = workloads.make("topk_scaling", N=700, d_in=1024, d_out=1536, k=k)
+    g = torch.Generator().manual_seed(99 + k)
+    ids = torch.stack([torch.randperm(wl.K, generator=g)[:k] for _ in range(wl.N)]).to(torch.int32)
+    w = torch.softmax(torch.randn(wl.N, k, generator=g), dim=1)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K)
+    y = dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(ids), y, wl.scale, w=dev(w), counts=counts,
+                        offsets=offsets, perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    y_ref, rows = oracle.lora_apply(wl.x, wl.A, wl.B, ids, wl.y0, wl.scale, w)
+    assert rows == wl.N * k
+    assert_apply_close(y, y_ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_apply_degenerate_cases(m, path):
+    wl = workloads.make("modality4", N=300, d_in=512, d_out=512)
+    g = torch.Generator().manual_seed(5)
+    ids = torch.randint(0, wl.K, (wl.N, 2), generator=g, dtype=torch.int32)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K)
+    # B = 0 leaves y at y0 exactly
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(torch.zeros_like(wl.B)), dev(ids), y, wl.scale, counts=counts,
+                        offsets=offsets, perm=perm, path=path)
+    assert torch.equal(y.cpu(), wl.y0)
+    # w = 0 leaves y at y0 exactly
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(ids), y, wl.scale, w=torch.zeros(wl.N, 2, device="cuda"),
+                        counts=counts, offsets=offsets, perm=perm, path=path)
+    assert torch.equal(y.cpu(), wl.y0)
+    # k = K with uniform weights equals the dense sum of all adapters (oracle closed form)
+    idsK = torch.stack([torch.randperm(wl.K, generator=g) for _ in range(wl.N)]).to(torch.int32)
+    wK = torch.full((wl.N, wl.K), 1.0 / wl.K)
+    cK, oK, pK = m.molora_dispatch(dev(idsK), wl.K)
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(idsK), y, wl.scale, w=dev(wK), counts=cK, offsets=oK,
+                        perm=pK, path=path)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, idsK, wl.y0, wl.scale, wK)
+    assert_apply_close(y, y_ref)
+
+
+def test_apply_invalid_ids_are_skipped_and_reported(m):
+    wl = workloads.make("modality4", N=256, d_in=512, d_out=512)
+    g = torch.Generator().manual_seed(6)
+    ids = torch.randint(-1, wl.K + 1, (wl.N, 1), generator=g, dtype=torch.int32)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, wl.y0, wl.scale)
+    for path in PATHS:
+        e = err_word()
+        counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K, err_word=e)
+        y = dev(wl.y0).clone()
+        m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(ids), y, wl.scale, counts=counts, offsets=offsets,
+                            perm=perm, err_word=e, path=path)
+        torch.cuda.synchronize()
+        assert int(e.item()) & m.DEV_BAD_ADAPTER_ID
+        assert_apply_close(y, y_ref)
+
+
+def test_apply_empty_batch(m):
+    wl = workloads.make("modality4", N=4, d_in=256, d_out=256)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, 1, dtype=torch.int32, device="cuda")
+    y = torch.empty(0, 256, dtype=torch.float32, device="cuda")
+    counts, offsets, perm = m.molora_dispatch(ids, wl.K)
+    assert counts.cpu().tolist() == [0] * wl.K and offsets.cpu().tolist() == [0] * (wl.K + 1)
+    for path in ("auto",) + tuple(PATHS):
+        m.molora_lora_apply(x, dev(wl.A), dev(wl.B), ids, y, 2.0, counts=counts, offsets=offsets, perm=perm, path=path)
+
+
+# ------------------------------------------------------------------------- per-sequence baseline
+
+@pytest.mark.parametrize("path", PATHS)
+def test_masked_passes_equal_per_token(m, path):
+    wl = workloads.make("modality4", N=640, d_in=1024, d_out=1024)
+    adapter, counts, offsets, perm, y_tok, e = run_vocab_path(m, wl, path)
+    y_seq = dev(wl.y0).clone()
+    for a in range(wl.K):
+        m.molora_lora_apply_masked_pass(dev(wl.x), dev(wl.A), dev(wl.B), adapter, a, y_seq, wl.scale, path=path)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.per_sequence_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    assert_apply_close(y_seq, y_ref)
+    assert_apply_close(y_tok, y_ref)
+
+
+# ------------------------------------------------------------------------- router
+
+def check_router(wl, k, logits, ids, w):
+    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x, wl.W1, wl.W2, k)
+    assert torch.allclose(logits.cpu(), ref_logits, rtol=1e-4, atol=1e-4)
+    srt = torch.sort(ref_logits.double(), dim=1, descending=True).values
+    if k < wl.K:
+        clear = (srt[:, k - 1] - srt[:, k]) > 1e-3
+    else:
+        clear = torch.ones(wl.N, dtype=torch.bool)
+    assert clear.float().mean() > 0.5
+    assert torch.equal(ids.cpu()[clear], ref_ids[clear])
+    rel = ((w.cpu()[clear].double() - ref_w[clear].double()).abs() / ref_w[clear].double().abs().clamp_min(1e-30))
+    assert rel.max().item() <= 1e-5
+    return clear
+
+
+@pytest.mark.parametrize("name,kw,k", [("topk_mlp", {"N": 1000}, 2), ("topk_scaling", {"N": 777}, 1),
+                                       ("topk_scaling", {"N": 513}, 3), ("topk_scaling", {"N": 300}, 4),
+                                       ("topk_mlp", {"N": 129, "d_in": 192}, 2)])
+def test_router_topk_vs_oracle(m, name, kw, k):
+    wl = workloads.make(name, k=k, **kw)
+    logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(wl.W2), k)
+    torch.cuda.synchronize()
+    check_router(wl, k, logits, ids, w)
+
+
+def test_router_fp32_and_biases(m):
+    wl = workloads.make("topk_mlp", N=200, d_in=96, dtype=torch.float32, k=2)
+    g = torch.Generator().manual_seed(3)
+    b1 = torch.randn(64, generator=g) * 0.1
+    b2 = torch.randn(wl.K, generator=g) * 0.1
+    logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(wl.W2), 2, b1=dev(b1), b2=dev(b2))
+    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x, wl.W1, wl.W2, 2, b1, b2)
+    assert torch.allclose(logits.cpu(), ref_logits, rtol=1e-4, atol=1e-4)
+    srt = torch.sort(ref_logits.double(), dim=1, descending=True).values
+    clear = (srt[:, 1] - srt[:, 2]) > 1e-3
+    assert torch.equal(ids.cpu()[clear], ref_ids[clear])
+
+
+def test_router_ties_lower_index_first(m):
+    wl = workloads.make("topk_mlp", N=256, k=2)
+    W2 = wl.W2.clone()
+    W2[:, 3] = W2[:, 0]  # adapters 0 and 3 tie exactly
+    logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(W2), 4)
+    ids = ids.cpu()
+    pos0 = (ids == 0).int().argmax(1)
+    pos3 = (ids == 3).int().argmax(1)
+    assert torch.all(pos0 < pos3)
+
+
+# ------------------------------------------------------------------------- whole path in a CUDA graph
+
+@pytest.mark.parametrize("path", PATHS)
+def test_graph_captured_learned_path(m, path):
+    wl = workloads.make("topk_mlp", N=1024, d_in=1024, d_out=2048, k=2)
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    y = dev(wl.y0).clone()
+    logits = torch.empty(wl.N, wl.K, device="cuda")
+    ids = torch.empty(wl.N, 2, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.N, 2, device="cuda")
+    counts = torch.empty(wl.K, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(wl.K + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(wl.N * 2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            m.molora_router_topk(x, W1, W2, 2, logits=logits, ids=ids, w=w)
+            m.molora_dispatch(ids, wl.K, counts=counts, offsets=offsets, perm=perm)
+            m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm, path=path)
+    for rep in range(3):
+        y.copy_(dev(wl.y0))
+        graph.replay()
+    torch.cuda.synchronize()
+    check_router(wl, 2, logits, ids, w)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids.cpu(), wl.y0, wl.scale, w.cpu())
+    assert_apply_close(y, y_ref)

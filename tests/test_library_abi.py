@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every entry point include/molora.h declares;
+host-side validation rejects bad arguments before any launch (no GPU needed: every call
+here returns before touching the CUDA runtime)."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "molora.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOLORA_API\s+[\w\s\*]+?\b(molora_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from token_adapter_routing_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_four_calls():
+    syms = declared_symbols()
+    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply"):
+        assert name in syms
+
+
+@needs_nvcc
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    import token_adapter_routing_gb300 as m
+    assert set(m.EXPORTED) == set(declared_symbols())
+
+
+@needs_nvcc
+def test_only_the_c_abi_is_exported(lib):
+    import subprocess
+    from token_adapter_routing_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    text_syms = [ln.split()[-1] for ln in out.splitlines() if " T " in ln]
+    assert sorted(text_syms) == declared_symbols()
+
+
+@needs_nvcc
+def test_host_validation_rejects_bad_arguments_without_launching(lib):
+    P, I64, I32, F, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_int
+    lib.molora_route_vocab.argtypes = [P, I64, P, I32, P, P, P]
+    lib.molora_dispatch.argtypes = [P, I64, I32, I32, P, P, P, P, P]
+    lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
+    lib.molora_router_topk.argtypes = [P, S, I64, I32, P, P, P, P, I32, I32, P, P, P, P]
+    lib.molora_status_string.restype = ctypes.c_char_p
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x10004)   # not 16-byte aligned
+    INVALID, UNSUPPORTED = 1, 2
+    # route_vocab: K out of range, null pointers; N == 0 is a valid no-op
+    assert lib.molora_route_vocab(fake, 10, fake, 0, fake, None, None) == INVALID
+    assert lib.molora_route_vocab(fake, 10, fake, 65, fake, None, None) == INVALID
+    assert lib.molora_route_vocab(None, 10, fake, 4, fake, None, None) == INVALID
+    assert lib.molora_route_vocab(None, 0, None, 4, None, None, None) == 0
+    # dispatch: k > K, k < 1, K > 64, null outputs
+    assert lib.molora_dispatch(fake, 8, 5, 4, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_dispatch(fake, 8, 0, 4, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_dispatch(fake, 8, 1, 65, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_dispatch(fake, 8, 1, 4, None, fake, fake, None, None) == INVALID
+
+    def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0):
+        return lib.molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, None, k, fake, fake, fake,
+                                        2.0, y, None, path, None)
+
+    assert apply(r=12) == INVALID
+    assert apply(K=0) == INVALID and apply(K=65) == INVALID
+    assert apply(k=5) == INVALID and apply(k=0) == INVALID
+    assert apply(dtype=7) == INVALID
+    assert apply(x=None) == INVALID and apply(y=None) == INVALID and apply(ids=None) == INVALID
+    assert apply(x=odd) == INVALID and apply(A=odd) == INVALID and apply(B=odd) == INVALID and apply(y=odd) == INVALID
+    assert apply(N=-1) == INVALID and apply(d_in=0) == INVALID
+    assert apply(path=9) == INVALID
+    # the grouped tensor-core path needs bf16 and r >= 16
+    assert apply(dtype=0, path=2) == UNSUPPORTED
+    assert apply(r=8, path=2) == UNSUPPORTED
+    assert apply(N=0) == 0
+    # router: k > K, K > 64, null outputs
+    assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 5, None, fake, fake, None) == INVALID
+    assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 65, 1, None, fake, fake, None) == INVALID
+    assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 1, None, None, fake, None) == INVALID
+    assert lib.molora_status_string(1) == b"invalid argument"

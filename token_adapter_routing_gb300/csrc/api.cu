@@ -1,0 +1,149 @@
+// api.cu -- the C ABI declared in include/molora.h: host-side argument validation, then
+// kernel selection and launch.  Nothing here allocates, frees or synchronises.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace molora {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool valid_dtype(molora_dtype d) { return d == MOLORA_F32 || d == MOLORA_BF16; }
+static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_OK : MOLORA_ERR_CUDA; }
+
+// Token count at which the grouped tensor-core apply overtakes the scalar apply, measured on
+// GB300 with the decode sweep (d = 4096, r = 16, top-1, K = 4..64 hot-set adapters).
+static int64_t crossover_tokens(int32_t K) {
+  (void)K;
+  return 64;
+}
+
+static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                      const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                                      int32_t k, const float* y) {
+  if (!valid_dtype(dtype) || N < 0 || d_in < 1 || d_out < 1 || K < 1 || K > kMaxAdapters || k < 1 || k > K)
+    return MOLORA_ERR_INVALID_ARG;
+  if (!(r == 8 || r == 16 || r == 32 || r == 64)) return MOLORA_ERR_INVALID_ARG;
+  if (N > INT32_MAX || N * (int64_t)k > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0) return MOLORA_OK;
+  if (!x || !A || !B || !ids || !y) return MOLORA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y)) return MOLORA_ERR_INVALID_ARG;
+  return MOLORA_OK;
+}
+
+}  // namespace molora
+
+using namespace molora;
+
+extern "C" {
+
+molora_status molora_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K, int32_t* adapter,
+                                 int32_t* err_word, cudaStream_t stream) {
+  if (N < 0 || K < 1 || K > kMaxAdapters) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0) return MOLORA_OK;
+  if (!tok || !starts || !adapter) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_route_vocab(tok, N, starts, K, adapter, err_word, stream));
+}
+
+molora_status molora_router_topk(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
+                                 const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,
+                                 float* logits, int32_t* ids, float* w, cudaStream_t stream) {
+  if (!valid_dtype(dtype) || N < 0 || d_in < 1 || K < 1 || K > kMaxAdapters || k < 1 || k > K)
+    return MOLORA_ERR_INVALID_ARG;
+  if (N > INT32_MAX || N * (int64_t)K > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0) return MOLORA_OK;
+  if (!x || !W1 || !W2 || !ids || !w) return MOLORA_ERR_INVALID_ARG;
+  if (router_tc_supported(dtype, N, d_in, K, k)) {
+    if (!aligned16(x) || !aligned16(W1)) return MOLORA_ERR_INVALID_ARG;
+    return launched(launch_router_tc(x, N, d_in, W1, b1, W2, b2, K, k, logits, ids, w, stream));
+  }
+  return launched(launch_router_scalar(x, dtype, N, d_in, W1, b1, W2, b2, K, k, logits, ids, w, stream));
+}
+
+molora_status molora_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts, int32_t* offsets,
+                              int32_t* perm, int32_t* err_word, cudaStream_t stream) {
+  if (N < 0 || k < 1 || K < 1 || K > kMaxAdapters || k > K) return MOLORA_ERR_INVALID_ARG;
+  if (N * (int64_t)k > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (!counts || !offsets || (N > 0 && (!ids || !perm))) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_dispatch(ids, N, k, K, counts, offsets, perm, err_word, stream));
+}
+
+molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
+                               int32_t k) {
+  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
+  return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
+}
+
+molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                   const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                                   const float* w, int32_t k, const int32_t* counts, const int32_t* offsets,
+                                   const int32_t* perm, float scale, float* y, int32_t* err_word, molora_path path,
+                                   cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+  if (st != MOLORA_OK || N == 0) return st;
+  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+  if (path == MOLORA_PATH_SCALAR)
+    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, -1, err_word,
+                                       stream));
+  if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
+  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !perm) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, -1,
+                                      err_word, stream));
+}
+
+molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
+                                int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                                float scale, float* y, int32_t* err_word, cudaStream_t stream) {
+  return molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y,
+                              err_word, MOLORA_PATH_AUTO, stream);
+}
+
+molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                            int32_t d_out, const void* A, const void* B, int32_t K, int32_t r,
+                                            const int32_t* adapter_of, int32_t a, float scale, float* y,
+                                            int32_t* err_word, molora_path path, cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, adapter_of, 1, y);
+  if (st != MOLORA_OK) return st;
+  if (a < 0 || a >= K) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0) return MOLORA_OK;
+  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, 1);
+  if (path == MOLORA_PATH_SCALAR)
+    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, scale, y, a,
+                                       err_word, stream));
+  if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
+  if (!grouped_supported(dtype, N, d_in, d_out, K, r, 1)) return MOLORA_ERR_UNSUPPORTED;
+  return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, nullptr, nullptr,
+                                      nullptr, scale, y, a, err_word, stream));
+}
+
+const char* molora_status_string(molora_status status) {
+  switch (status) {
+    case MOLORA_OK:
+      return "ok";
+    case MOLORA_ERR_INVALID_ARG:
+      return "invalid argument";
+    case MOLORA_ERR_UNSUPPORTED:
+      return "unsupported shape for this path";
+    case MOLORA_ERR_CUDA:
+      return "CUDA launch error";
+  }
+  return "unknown status";
+}
+
+int32_t molora_version(void) { return 100; }
+
+}  // extern "C"

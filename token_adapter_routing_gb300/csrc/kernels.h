@@ -1,0 +1,51 @@
+// kernels.h -- host-side launchers of the library's kernels (internal; the public surface
+// is include/molora.h).  Each launcher assumes its arguments were validated by api.cu and
+// returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "molora.h"
+
+namespace molora {
+
+cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                               int32_t* adapter, int32_t* err_word, cudaStream_t stream);
+
+cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* err_word, cudaStream_t stream);
+
+// Token-major CUDA-core apply.  mask_adapter >= 0 turns it into one masked per-sequence pass:
+// adapter mask_adapter for every token, weight [ids[t] == mask_adapter] (k must be 1).
+cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                               const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                               const float* w, int32_t k, float scale, float* y, int32_t mask_adapter,
+                               int32_t* err_word, cudaStream_t stream);
+
+// CUDA-core learned router (any dtype / shape).
+cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
+                                 const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,
+                                 float* logits, int32_t* ids, float* w, cudaStream_t stream);
+
+// Grouped tcgen05 apply: true if this shape is supported.
+bool grouped_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
+                       int32_t k);
+// Grouped tcgen05 apply.  With mask_adapter >= 0 the tiles cover tokens 0..N-1 in order with
+// adapter mask_adapter and weight [ids[t] == mask_adapter] (one masked per-sequence pass);
+// counts/offsets/perm are then unused.
+cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
+                                const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
+                                int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                                float scale, float* y, int32_t mask_adapter, int32_t* err_word,
+                                cudaStream_t stream);
+
+// tcgen05 learned router: true if this shape is supported.
+bool router_tc_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t K, int32_t k);
+cudaError_t launch_router_tc(const void* x, int64_t N, int32_t d_in, const void* W1, const float* b1,
+                             const void* W2, const float* b2, int32_t K, int32_t k, float* logits,
+                             int32_t* ids, float* w, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace molora

@@ -1,0 +1,302 @@
+// lora_scalar.cu -- the CUDA-core paths of "MoLoRA: Composable Specialization via Per-Token
+// Adapter Routing":
+//   * the token-major LoRA apply for the memory-bound small-batch regime (Figures 5 and 9:
+//     below the crossover a scalar per-token kernel beats the tensor-core kernel), which
+//     also serves fp32 inputs, rank 8 and shapes the grouped tcgen05 path does not take;
+//   * a CUDA-core learned router TopK(g(x)) (Table 1) for fp32 or odd shapes.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace molora {
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// 16 bytes of T unpacked to floats.
+template <typename T>
+struct Chunk16;
+template <>
+struct Chunk16<float> {
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static void load(const float* p, float (&v)[4]) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+  }
+};
+template <>
+struct Chunk16<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  }
+};
+
+// Four consecutive elements of T as floats (8 bytes of bf16 or 16 bytes of fp32).
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+  v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+  v[0] = __uint_as_float(q.x << 16), v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(q.y << 16), v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+}
+
+constexpr int kScalarThreads = 256;
+
+// One CTA per (token, column split).  Phase 1: for each of the token's k slots the CTA
+// reduces h = x[t] A_a over d_in (each thread streams 16-byte chunks of A_a, which is
+// row-major [d_in x R], so a warp reads 512 contiguous bytes per step) and stores
+// g_j = scale * w_j * h.  Phase 2: each thread owns 4 output columns and accumulates
+// sum_j sum_q g_j[q] B_a[q, c..c+3] in registers, then updates y once.  Every y element is
+// read and written exactly once whatever k is, so the result is deterministic.
+template <typename T, int R>
+__global__ void __launch_bounds__(kScalarThreads)
+    lora_scalar_kernel(const T* __restrict__ x, int32_t d_in, int32_t d_out, const T* __restrict__ A,
+                       const T* __restrict__ B, int32_t K, const int32_t* __restrict__ ids,
+                       const float* __restrict__ w, int32_t k, float scale, float* __restrict__ y,
+                       int32_t cols_per_split, int32_t mask_adapter, int32_t* err_word) {
+  using C16 = Chunk16<T>;
+  constexpr int VEC = C16::kVec;
+  constexpr int CPR = R / VEC;  // 16-byte chunks per row of A_a
+  static_assert(R % VEC == 0 && (kScalarThreads % CPR) == 0, "chunking");
+  extern __shared__ float smem[];
+  float* g = smem;                 // [k][R]
+  float* red = smem + k * R;       // [8 warps][R]
+  int32_t* s_adapter = reinterpret_cast<int32_t*>(red + (kScalarThreads / 32) * R);  // [k]
+
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const T* xr = x + t * (int64_t)d_in;
+
+  for (int j = 0; j < k; ++j) {
+    int32_t a;
+    float wj;
+    if (mask_adapter >= 0) {
+      a = mask_adapter;
+      wj = (ids[t] == mask_adapter) ? 1.f : 0.f;
+    } else {
+      a = ids[t * k + j];
+      wj = w ? w[t * k + j] : 1.f;
+      if (a < 0 || a >= K) {
+        if (tid == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
+        a = -1;
+      }
+    }
+    if (a < 0) {  // uniform over the CTA
+      if (tid == 0) s_adapter[j] = -1;
+      continue;
+    }
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    const T* Aa = A + (int64_t)a * d_in * R;
+    const int64_t nchunks = (int64_t)d_in * CPR;
+#pragma unroll 4
+    for (int64_t c = tid; c < nchunks; c += kScalarThreads) {
+      const float xv = to_f(xr[c / CPR]);
+      float av[VEC];
+      C16::load(Aa + c * VEC, av);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[v] = fmaf(xv, av[v], acc[v]);
+    }
+    // lanes with equal (lane % CPR) hold the same columns q0..q0+VEC-1
+#pragma unroll
+    for (int off = 16; off >= CPR; off >>= 1)
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], off);
+    if (lane < CPR)
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) red[warp * R + lane * VEC + v] = acc[v];
+    __syncthreads();
+    if (tid < R) {
+      float h = 0.f;
+#pragma unroll
+      for (int q = 0; q < kScalarThreads / 32; ++q) h += red[q * R + tid];
+      g[j * R + tid] = scale * wj * h;
+    }
+    if (tid == 0) s_adapter[j] = a;
+    __syncthreads();
+  }
+  __syncthreads();
+
+  const int32_t c_begin = blockIdx.y * cols_per_split;
+  const int32_t c_end = min(d_out, c_begin + cols_per_split);
+  float* yr = y + t * (int64_t)d_out;
+  if ((d_out & 3) == 0) {
+    for (int32_t c = c_begin + 4 * tid; c < c_end; c += 4 * kScalarThreads) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        const int32_t a = s_adapter[j];
+        if (a < 0) continue;
+        const T* Bq = B + (int64_t)a * R * d_out + c;
+        const float* gj = g + j * R;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          float b[4];
+          load4(Bq + (int64_t)q * d_out, b);
+          const float gq = gj[q];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[v] = fmaf(gq, b[v], acc[v]);
+        }
+      }
+      float4 yv = *reinterpret_cast<float4*>(yr + c);
+      yv.x += acc[0], yv.y += acc[1], yv.z += acc[2], yv.w += acc[3];
+      *reinterpret_cast<float4*>(yr + c) = yv;
+    }
+  } else {
+    for (int32_t c = c_begin + tid; c < c_end; c += kScalarThreads) {
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int32_t a = s_adapter[j];
+        if (a < 0) continue;
+        const T* Bq = B + (int64_t)a * R * d_out + c;
+        for (int q = 0; q < R; ++q) acc = fmaf(g[j * R + q], to_f(Bq[(int64_t)q * d_out]), acc);
+      }
+      yr[c] += acc;
+    }
+  }
+}
+
+template <typename T>
+static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
+                                   const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
+                                   int32_t k, float scale, float* y, int32_t mask_adapter, int32_t* err_word,
+                                   cudaStream_t stream) {
+  // Enough CTAs to cover the GPU twice: small batches split the output columns (each split
+  // recomputes the token's cheap shrink).
+  const int64_t want = 2 * (int64_t)num_sms();
+  int64_t splits = N >= want ? 1 : (want + N - 1) / N;
+  const int64_t max_splits = d_out >= 512 ? d_out / 512 : 1;
+  if (splits > max_splits) splits = max_splits;
+  int32_t cols = (int32_t)((d_out + splits - 1) / splits);
+  cols = (cols + 3) & ~3;
+  splits = (d_out + cols - 1) / cols;
+  const size_t smem = sizeof(float) * ((size_t)k * r + (kScalarThreads / 32) * r) + sizeof(int32_t) * k;
+  dim3 grid((unsigned)N, (unsigned)splits);
+  const T* xp = static_cast<const T*>(x);
+  const T* Ap = static_cast<const T*>(A);
+  const T* Bp = static_cast<const T*>(B);
+  switch (r) {
+    case 8:
+      lora_scalar_kernel<T, 8><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k, scale,
+                                                                       y, cols, mask_adapter, err_word);
+      break;
+    case 16:
+      lora_scalar_kernel<T, 16><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                                                        scale, y, cols, mask_adapter, err_word);
+      break;
+    case 32:
+      lora_scalar_kernel<T, 32><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                                                        scale, y, cols, mask_adapter, err_word);
+      break;
+    case 64:
+      lora_scalar_kernel<T, 64><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                                                        scale, y, cols, mask_adapter, err_word);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                               const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                               const float* w, int32_t k, float scale, float* y, int32_t mask_adapter,
+                               int32_t* err_word, cudaStream_t stream) {
+  if (dtype == MOLORA_BF16)
+    return launch_scalar_t<__nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter,
+                                          err_word, stream);
+  return launch_scalar_t<float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter, err_word,
+                                stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// CUDA-core router: 8 tokens per CTA so each W1 element is read once per 8 tokens.  Four
+// thread groups split d_in; thread j of a group accumulates hidden unit j.  Then the 64 x K
+// second layer, and one thread per token selects the top k (strictly greater wins, so equal
+// logits keep the lower index) and renormalises the softmax over the selected k.
+constexpr int kRouterTok = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    router_scalar_kernel(const T* __restrict__ x, int64_t N, int32_t d_in, const T* __restrict__ W1,
+                         const float* __restrict__ b1, const T* __restrict__ W2, const float* __restrict__ b2,
+                         int32_t K, int32_t k, float* __restrict__ logits, int32_t* __restrict__ ids,
+                         float* __restrict__ w) {
+  __shared__ float part[4][kRouterTok][kRouterHidden];
+  __shared__ float hid[kRouterTok][kRouterHidden];
+  __shared__ float lg[kRouterTok][kMaxAdapters];
+  const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
+  const int j = threadIdx.x & 63, grp = threadIdx.x >> 6;
+  float acc[kRouterTok];
+#pragma unroll
+  for (int q = 0; q < kRouterTok; ++q) acc[q] = 0.f;
+  for (int32_t i = grp; i < d_in; i += 4) {
+    const float wv = to_f(W1[(int64_t)i * kRouterHidden + j]);
+#pragma unroll
+    for (int q = 0; q < kRouterTok; ++q)
+      if (t0 + q < N) acc[q] = fmaf(to_f(x[(t0 + q) * d_in + i]), wv, acc[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < kRouterTok; ++q) part[grp][q][j] = acc[q];
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kRouterTok * kRouterHidden; idx += blockDim.x) {
+    const int q = idx / kRouterHidden, jj = idx % kRouterHidden;
+    float h = part[0][q][jj] + part[1][q][jj] + part[2][q][jj] + part[3][q][jj];
+    if (b1) h += b1[jj];
+    hid[q][jj] = h > 0.f ? h : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kRouterTok * K; idx += blockDim.x) {
+    const int q = idx / K, a = idx % K;
+    float s = 0.f;
+    for (int jj = 0; jj < kRouterHidden; ++jj) s = fmaf(hid[q][jj], to_f(W2[jj * K + a]), s);
+    if (b2) s += b2[a];
+    lg[q][a] = s;
+    if (logits && t0 + q < N) logits[(t0 + q) * K + a] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < kRouterTok && t0 + threadIdx.x < N) {
+    const int q = threadIdx.x;
+    const int64_t t = t0 + q;
+    uint64_t used = 0;
+    float m = 0.f, denom = 0.f;
+    for (int js = 0; js < k; ++js) {
+      int best = -1;
+      for (int a = 0; a < K; ++a)
+        if (!((used >> a) & 1ull) && (best < 0 || lg[q][a] > lg[q][best])) best = a;
+      used |= 1ull << best;
+      ids[t * k + js] = best;
+      if (js == 0) m = lg[q][best];
+      const float e = expf(lg[q][best] - m);
+      w[t * k + js] = e;
+      denom += e;
+    }
+    const float inv = 1.f / denom;
+    for (int js = 0; js < k; ++js) w[t * k + js] *= inv;
+  }
+}
+
+cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
+                                 const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,
+                                 float* logits, int32_t* ids, float* w, cudaStream_t stream) {
+  const unsigned grid = (unsigned)((N + kRouterTok - 1) / kRouterTok);
+  if (dtype == MOLORA_BF16)
+    router_scalar_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), N, d_in, static_cast<const __nv_bfloat16*>(W1), b1,
+        static_cast<const __nv_bfloat16*>(W2), b2, K, k, logits, ids, w);
+  else
+    router_scalar_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), N, d_in,
+                                                          static_cast<const float*>(W1), b1,
+                                                          static_cast<const float*>(W2), b2, K, k, logits, ids, w);
+  return cudaGetLastError();
+}
+
+}  // namespace molora

@@ -1,0 +1,147 @@
+// route_dispatch.cu -- vocabulary routing and the dispatch step (histogram, exclusive scan,
+// stable permutation) of "MoLoRA: Composable Specialization via Per-Token Adapter Routing"
+// (Table 1: R_vocab(v), histogram computation, pointer arrays; Figure 2 right: tokens
+// grouped by their selected adapter).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace molora {
+
+// One thread per token; the K+1 range starts sit in shared memory and each token does a
+// binary search for the last start <= its id.
+__global__ void __launch_bounds__(256) route_vocab_kernel(const int32_t* __restrict__ tok, int64_t N,
+                                                          const int32_t* __restrict__ starts, int32_t K,
+                                                          int32_t* __restrict__ adapter, int32_t* err_word) {
+  __shared__ int32_t s_starts[kMaxAdapters + 1];
+  for (int i = threadIdx.x; i <= K; i += blockDim.x) s_starts[i] = starts[i];
+  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int a = 0; a < K; ++a)
+      if (s_starts[a] >= s_starts[a + 1]) {
+        report(err_word, MOLORA_DEV_BAD_RANGES);
+        break;
+      }
+  }
+  bool outside = false;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < N; t += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t v = tok[t];
+    int32_t a = -1;
+    if (v >= s_starts[0] && v < s_starts[K]) {
+      int lo = 0, hi = K;  // s_starts[lo] <= v < s_starts[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_starts[mid] <= v)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      a = lo;
+    } else {
+      outside = true;
+    }
+    adapter[t] = a;
+  }
+  if (__any_sync(0xffffffffu, outside) && (threadIdx.x & 31) == 0) report(err_word, MOLORA_DEV_TOKEN_OUTSIDE_RANGES);
+}
+
+cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K, int32_t* adapter,
+                               int32_t* err_word, cudaStream_t stream) {
+  const int64_t blocks = (N + 255) / 256;
+  const int grid = (int)(blocks < 8 * num_sms() ? blocks : 8 * num_sms());
+  route_vocab_kernel<<<grid, 256, 0, stream>>>(tok, N, starts, K, adapter, err_word);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// Dispatch: a single CTA of 32 warps.  Warp w owns a contiguous run of slots; it walks the
+// run 32 slots at a time, and __match_any_sync groups the lanes that carry the same adapter
+// id.  Pass 1 counts slots per (warp, adapter).  The counts, read adapter-major, give each
+// (adapter, warp) the first output position of its slots (the exclusive scan).  Pass 2
+// repeats the walk and writes each slot at base + its rank among equal lanes of lower index,
+// so the permutation is stable: within an adapter, slots appear in ascending order.  No
+// atomics whose order could change a result; no inter-CTA waiting.
+constexpr int kDispatchWarps = 32;
+
+__global__ void __launch_bounds__(kDispatchWarps * 32, 1)
+    dispatch_kernel(const int32_t* __restrict__ ids, int64_t S, int32_t K, int32_t* __restrict__ counts,
+                    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* err_word) {
+  __shared__ int32_t cnt[kDispatchWarps][kMaxAdapters];
+  __shared__ int32_t s_total[kMaxAdapters];
+  __shared__ int32_t s_off[kMaxAdapters + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+
+  const int64_t per_warp = ((S + kDispatchWarps * 32 - 1) / (kDispatchWarps * 32)) * 32;
+  const int64_t beg = min(S, (int64_t)warp * per_warp);
+  const int64_t end = min(S, beg + per_warp);
+  const unsigned lanes_below = (1u << lane) - 1u;
+
+  bool bad = false;
+  for (int64_t base = beg; base < end; base += 32) {
+    const int64_t s = base + lane;
+    int32_t a = -1;
+    if (s < end) {
+      a = ids[s];
+      if (a < 0 || a >= K) {
+        bad = true;
+        a = -1;
+      }
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, a);
+    if (a >= 0 && lane == __ffs(m) - 1) cnt[warp][a] += __popc(m);
+  }
+  __syncthreads();
+
+  if (threadIdx.x < K) {
+    int32_t sum = 0;
+    for (int w = 0; w < kDispatchWarps; ++w) sum += cnt[w][threadIdx.x];
+    s_total[threadIdx.x] = sum;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t run = 0;
+    for (int a = 0; a < K; ++a) {
+      s_off[a] = run;
+      run += s_total[a];
+    }
+    s_off[K] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x < K) {
+    const int a = threadIdx.x;
+    int32_t run = s_off[a];
+    for (int w = 0; w < kDispatchWarps; ++w) {
+      const int32_t c = cnt[w][a];
+      cnt[w][a] = run;  // first output position of warp w's slots of adapter a
+      run += c;
+    }
+    counts[a] = s_total[a];
+  }
+  if (threadIdx.x <= K) offsets[threadIdx.x] = s_off[threadIdx.x];
+  __syncthreads();
+
+  for (int64_t base = beg; base < end; base += 32) {
+    const int64_t s = base + lane;
+    int32_t a = -1;
+    if (s < end) {
+      a = ids[s];
+      if (a < 0 || a >= K) a = -1;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, a);
+    if (a >= 0) perm[cnt[warp][a] + __popc(m & lanes_below)] = (int32_t)s;
+    __syncwarp();
+    if (a >= 0 && lane == __ffs(m) - 1) cnt[warp][a] += __popc(m);
+    __syncwarp();
+  }
+  for (int64_t i = s_off[K] + threadIdx.x; i < S; i += blockDim.x) perm[i] = -1;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
+}
+
+cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts, int32_t* offsets,
+                            int32_t* perm, int32_t* err_word, cudaStream_t stream) {
+  dispatch_kernel<<<1, kDispatchWarps * 32, 0, stream>>>(ids, N * (int64_t)k, K, counts, offsets, perm, err_word);
+  return cudaGetLastError();
+}
+
+}  // namespace molora
