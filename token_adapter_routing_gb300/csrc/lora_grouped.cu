@@ -5,24 +5,35 @@
 //
 // One fused kernel per call.  A work tile is up to 128 consecutive slots of one adapter's
 // group (dispatch order), handled by a thread-block cluster of C CTAs:
+//   0. each CTA asks L2 to prefetch the y rows it will update, so the y reads overlap the
+//      x gather instead of following it;
 //   1. shrink, split over d_in: CTA c gathers its 128 token rows x[tok, c*KS:(c+1)*KS)
-//      with 16-byte cp.async (the gather fused as an index list: no permuted copy of x),
-//      TMA-loads A_a's matching K-slice, and accumulates h_c = x A_a (128 x r, fp32) in
-//      TMEM with tcgen05.mma;
+//      with 16-byte cp.async in rounds of XR columns (the gather is fused as an index
+//      list: no permuted copy of x), TMA-loads A_a's matching K-slice, and accumulates
+//      h_c = x A_a (128 x r, fp32) in TMEM with tcgen05.mma;
 //   2. the C partial h_c are summed through distributed shared memory in a fixed order
 //      (deterministic), scaled by scale * w(slot), and split into two bf16 terms
 //      g = g_hi + g_lo (relative error 2^-17) to feed the next MMA;
 //   3. expand, split over d_out: CTA c computes D = g B_a[:, c*NC:(c+1)*NC) into TMEM in
-//      passes of up to 256 columns (double-buffered), B_a's columns TMA-loaded;
-//   4. epilogue: D goes TMEM -> registers -> shared memory, and each row is added into
-//      y[tok, cols] by one cp.reduce.async.bulk .add.f32: the TMA unit performs the fp32
-//      read-modify-write in L2, which also un-permutes (scatter by token) and, for top-k
-//      with k > 1, combines the k slots of a token.
+//      double-buffered passes of PW columns, B_a's columns TMA-loaded;
+//   4. epilogue: D goes TMEM -> registers -> shared memory, then each warp adds its rows
+//      into y[tok, cols] with coalesced 16-byte accesses (this un-permutes: scatter by
+//      token).  With k = 1 every y row has one writer, so it is a plain read-modify-write;
+//      with k > 1 the k slots of a token live in different tiles and the additions are
+//      red.global.add.v4.f32 reductions in L2.
 // The same kernel runs one masked per-sequence pass when given a fixed adapter: tiles are
 // then 128 consecutive tokens and the slot weight is the 0/1 mask.
+//
+// Shapes small enough for two CTAs per SM (shared memory <= 113 KB, 256 TMEM columns) use
+// 128-column passes; larger ones run one CTA per SM with 512 TMEM columns.  Either way the
+// TMEM of all resident CTAs fits in the SM's 512 columns, so an allocation never waits on
+// a CTA that is itself waiting at a cluster barrier.
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#ifdef MOLORA_TUNING_ENV
+#include <cstdlib>
+#endif
 
 #include "common.cuh"
 #include "kernels.h"
@@ -31,53 +42,98 @@ namespace molora {
 
 namespace {
 
-constexpr int kTileM = 128;          // slots per tile = TMEM lanes = MMA M
-constexpr int kKBlock = 64;          // K elements per 128-byte swizzle row (bf16)
-constexpr int kPassN = 256;          // columns per expand pass (one MMA N, one TMEM buffer)
-constexpr int kPieceN = 128;         // columns per epilogue bulk reduction
+constexpr int kTileM = 128;   // slots per tile = TMEM lanes = MMA M
+constexpr int kKBlock = 64;   // K elements per 128-byte swizzle row (bf16)
 constexpr int kEpilogueThreads = 128;
 constexpr int kThreads = kEpilogueThreads + 32;  // + one producer/MMA warp
-constexpr uint32_t kTmemCols = 512;
-constexpr size_t kMinSmem = 116 * 1024;  // at most one CTA per SM, so a 512-column TMEM allocation never waits
+constexpr size_t kSmemPerSm = 228 * 1024;
+constexpr size_t kSmemReservedPerCta = 1024;
 constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kCtrlBytes = 2048;
+constexpr uint32_t kBarX = 1;  // named barrier: x round staged (warps 0-4)
+constexpr int kEpiBulk = 0, kEpiPlain = 1, kEpiRed = 2, kEpiMixed = 3;
 
-struct GroupedShape {
-  int C;          // cluster size (split of d_in and of d_out)
-  int KS;         // d_in / C
-  int NC;         // d_out / C
-  size_t off_a;   // phase 1: A slice after the x tile
-  size_t off_g;   // phase 2: g_hi (g_lo follows at +16 KB)
-  size_t off_b;   // phase 2: B column chunk
-  size_t off_s;   // phase 2: epilogue staging
-  size_t region;  // bytes of the reused region
-  size_t smem;    // dynamic shared memory requested
+struct GroupedPlan {
+  int TM;            // valid rows per tile (64 or 128; the MMA always has M = 128)
+  int C;             // cluster size: split of d_in and of d_out
+  int KS;            // d_in / C: K-slice per CTA
+  int NC;            // d_out / C: output columns per CTA
+  int XR;            // x columns gathered per round
+  int PW;            // expand pass width (TMEM columns per buffer)
+  int piece;         // columns per bulk reduction
+  uint32_t tmem_cols;
+  uint32_t off_a;    // phase 1: A slice after the x round buffer
+  uint32_t off_g;    // phase 2: g_hi (g_lo follows at +16 KB)
+  uint32_t off_b;    // phase 2: B column chunk
+  uint32_t off_s;    // phase 2: epilogue staging
+  uint32_t off_recv; // receive slots for partial h, [C sources][128/C rows][r] fp32
+  uint32_t region;   // bytes before the control block (1024-aligned)
+  int epi;           // epilogue: kEpiBulk, kEpiPlain (k == 1 only), kEpiRed or kEpiMixed
+  int prefetch_y;    // prefetch this CTA's y rows into L2 at the start
+  uint32_t smem;     // dynamic shared memory requested
 };
-
-__host__ __device__ constexpr uint32_t p_stride(int r) { return (uint32_t)r * 4u + 16u; }
-constexpr uint32_t kStageStride = kPieceN * 4 + 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool plan(int32_t d_in, int32_t d_out, int32_t r, int C, GroupedShape* s) {
+bool plan_one(int32_t d_in, int32_t d_out, int32_t r, int C, int TM, bool two_per_sm, GroupedPlan* s) {
   if (d_in % (C * kKBlock) || d_out % (C * 64)) return false;
+  s->TM = TM;
   s->C = C;
   s->KS = d_in / C;
   s->NC = d_out / C;
-  const size_t phase1 = (size_t)s->KS * (kTileM * 2 + 2 * r);
-  s->off_a = (size_t)s->KS * kTileM * 2;
-  s->off_g = align_up((size_t)kTileM * p_stride(r), 1024);
-  s->off_b = s->off_g + 2 * 16384;
-  s->off_s = align_up(s->off_b + (size_t)s->NC * r * 2, 1024);
-  const size_t phase2 = s->off_s + (size_t)kTileM * kStageStride;
-  s->region = phase1 > phase2 ? phase1 : phase2;
-  s->smem = align_up(s->region, 1024) + 1024 /* base alignment slack */ + 2048 /* control block */;
-  if (s->smem < kMinSmem) s->smem = kMinSmem;
-  return s->smem <= kMaxSmem;
+  s->PW = two_per_sm ? 128 : 256;
+  s->piece = two_per_sm ? 64 : 128;
+  s->tmem_cols = two_per_sm ? 256 : 512;
+  const size_t budget = two_per_sm ? kSmemPerSm / 2 - kSmemReservedPerCta : kMaxSmem;
+  // phase 2 (after this CTA's shrink): g tiles, B chunk, epilogue staging.  g arrives from
+  // the row owners only after every CTA of the cluster finished its shrink, so it may reuse
+  // phase-1 space.  The receive slots for partial h get their own region: other CTAs may
+  // push into them while this CTA's tensor core still reads its x tile.
+  const size_t stage = (size_t)kTileM * (s->piece * 4 + 16);
+  const size_t off_b = 2 * 16384;
+  const size_t off_s = align_up(off_b + (size_t)s->NC * r * 2, 1024);
+  const size_t phase2 = off_s + stage;
+  const size_t recv = align_up((size_t)kTileM * r * 4, 1024);
+  s->off_g = 0;
+  s->off_b = (uint32_t)off_b;
+  s->off_s = (uint32_t)off_s;
+  for (int XR = s->KS > 256 ? 256 : s->KS; XR >= kKBlock; XR -= kKBlock) {
+    if (s->KS % XR) continue;
+    const size_t phase1 = (size_t)XR * kTileM * 2 + (size_t)s->KS * r * 2;
+    const size_t shared_region = align_up(phase1 > phase2 ? phase1 : phase2, 1024);
+    size_t smem = shared_region + recv + 1024 /* base alignment slack */ + kCtrlBytes;
+    if (!two_per_sm && smem < kSmemPerSm / 2) smem = kSmemPerSm / 2;  // keep it at one CTA per SM
+    if (smem <= budget) {
+      s->XR = XR;
+      s->off_a = (uint32_t)((size_t)XR * kTileM * 2);
+      s->off_recv = (uint32_t)shared_region;
+      s->region = (uint32_t)(shared_region + recv);
+      s->smem = (uint32_t)smem;
+      return true;
+    }
+  }
+  return false;
 }
 
-bool choose(int32_t d_in, int32_t d_out, int32_t r, GroupedShape* s) {
-  for (int C : {8, 4, 2, 1})
-    if (plan(d_in, d_out, r, C, s)) return true;
+// Picks cluster size, tile rows and CTAs per SM.  Clusters of 8 with two CTAs per SM are
+// preferred (they fit a whole small batch in one wave); shapes that do not fit fall back to
+// one CTA per SM, then to smaller clusters.
+bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, GroupedPlan* s) {
+  (void)S, (void)K;
+  int only_c = 0, only_one = 0, only_tm = 0;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_CLUSTER")) only_c = atoi(e);
+  if (const char* e = getenv("MOLORA_ONE_PER_SM")) only_one = atoi(e);
+  if (const char* e = getenv("MOLORA_TILE_ROWS")) only_tm = atoi(e);
+#endif
+  struct Cand { int C, TM; bool two; };
+  static const Cand order[] = {{8, 128, true}, {8, 128, false}, {4, 128, true}, {4, 128, false},
+                               {2, 128, true}, {2, 128, false}, {1, 128, true}, {1, 128, false},
+                               {4, 64, false}, {8, 64, true}};
+  for (const Cand& c : order) {
+    if ((only_c && c.C != only_c) || (only_one && c.two) || (only_tm && c.TM != only_tm)) continue;
+    if (plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
+  }
   return false;
 }
 
@@ -91,62 +147,89 @@ struct TileInfo {
 struct __align__(8) Ctrl {
   uint64_t bar_a;         // TMA of the A slice
   uint64_t bar_b;         // TMA of the B chunk
-  uint64_t bar_shrink;    // shrink MMAs done
+  uint64_t bar_x;         // shrink MMAs of one x round done (one phase per round)
   uint64_t bar_full[2];   // expand pass done, per TMEM buffer
   uint64_t bar_empty[2];  // epilogue drained a TMEM buffer
+  uint64_t bar_recv;      // partial-h rows this CTA owns have arrived from every CTA
+  uint64_t bar_g;         // all 128 rows of g (hi and lo) have arrived from their owners
   uint32_t tmem_base;
   int32_t abort;
   TileInfo tile;
-  int32_t tok[kTileM];  // token of each tile row (-1: padding or skipped)
-  float wgt[kTileM];    // weight of each tile row (0 for padding)
+  int32_t tok[kTileM];    // token of each tile row, -1 for padding (drives the gather)
+  int32_t live[kTileM];   // row passed validation and gets a reduction
+  float wgt[kTileM];      // weight of each tile row (0 for padding or invalid)
 };
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
-__device__ __forceinline__ uint64_t sw_for_rank(int r) {
+__device__ __forceinline__ SmemLayout sw_for_rank(int r) {
   return r == 16 ? kSwizzle32B : (r == 32 ? kSwizzle64B : kSwizzle128B);
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+// At most 168 registers: two CTAs (10 warps) must fit the 16K registers of an SM partition.
+__global__ void __maxnreg__(168)
     lora_grouped_kernel(const __nv_bfloat16* __restrict__ x, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
                         int32_t r, int32_t k, const int32_t* __restrict__ ids, const float* __restrict__ w,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, float scale,
-                        float* __restrict__ y, int32_t mask_adapter, int32_t C, int32_t KS, int32_t NC,
-                        uint32_t off_a, uint32_t off_g, uint32_t off_b, uint32_t off_s, uint32_t region,
-                        int32_t* err_word, const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_b) {
+                        float* __restrict__ y, int32_t mask_adapter, const GroupedPlan P, int32_t* err_word,
+                        const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(sm + region);  // region is 1024-aligned by the host
-  int32_t* s_tok = ctrl->tok;
-  float* s_w = ctrl->wgt;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(sm + P.region);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = P.C, KS = P.KS, NC = P.NC, TM = P.TM;
   const int crank = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x / C;
   const int64_t S = N * (int64_t)k;
+
+  // ---- prologue that reads nothing the previous kernel writes: overlaps it under PDL
+  if (warp == 4) {
+    tmem_alloc(&ctrl->tmem_base, P.tmem_cols);
+    tmem_relinquish();
+    if (lane == 0) {
+      mbar_init(&ctrl->bar_a, 1);
+      mbar_init(&ctrl->bar_b, 1);
+      mbar_init(&ctrl->bar_x, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ctrl->bar_full[i], 1);
+        mbar_init(&ctrl->bar_empty[i], kEpilogueThreads);
+      }
+      mbar_init(&ctrl->bar_recv, 1);
+      mbar_init(&ctrl->bar_g, 1);
+      mbar_fence_init();
+      // both receive 128 rows x r values: fp32 partials, and g as two bf16 halves
+      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)kTileM * r * 4u);
+      mbar_arrive_expect_tx(&ctrl->bar_g, (uint32_t)kTileM * r * 4u);
+      tma_prefetch_desc(&map_a);
+      tma_prefetch_desc(&map_b);
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
 
   // ---- which tile this cluster owns (identical in every CTA of the cluster)
   if (tid == 0) {
     TileInfo ti{-1, 0, 0, 0};
     if (mask_adapter >= 0) {
-      const int64_t t0 = (int64_t)cluster_id * kTileM;
-      if (t0 < N) ti = TileInfo{mask_adapter, (int32_t)t0, (int32_t)(N - t0 < kTileM ? N - t0 : kTileM), 0};
+      const int64_t t0 = (int64_t)cluster_id * TM;
+      if (t0 < N) ti = TileInfo{mask_adapter, (int32_t)t0, (int32_t)(N - t0 < TM ? N - t0 : TM), 0};
     } else {
       int32_t cum = 0;
       int32_t prev = offsets[0];
       bool bad = prev != 0;
-      for (int a = 0; a < K && ti.adapter < 0; ++a) {
+      for (int a = 0; a < K && ti.adapter < 0 && !bad; ++a) {
         const int32_t nxt = offsets[a + 1];
         if (nxt < prev || nxt > S) {
           bad = true;
           break;
         }
         const int32_t n_a = nxt - prev;
-        const int32_t tiles = (n_a + kTileM - 1) / kTileM;
+        const int32_t tiles = (n_a + TM - 1) / TM;
         if (cluster_id < cum + tiles) {
-          const int32_t row0 = (cluster_id - cum) * kTileM;
-          ti = TileInfo{a, row0, min(kTileM, n_a - row0), prev};
+          const int32_t row0 = (cluster_id - cum) * TM;
+          ti = TileInfo{a, row0, min(TM, n_a - row0), prev};
         }
         cum += tiles;
         prev = nxt;
@@ -161,109 +244,134 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const TileInfo tile = ctrl->tile;
-  if (tile.adapter < 0) return;  // whole cluster idles (every CTA computed the same tile)
+  if (tile.adapter < 0) {  // the whole cluster idles: every CTA computed the same tile
+    if (warp == 4) {
+      tc_fence_after();
+      tmem_dealloc(ctrl->tmem_base, P.tmem_cols);
+    }
+    return;
+  }
   const int a = tile.adapter;
 
-  uint8_t* xs = sm;             // phase 1: x tile, KS/64 blocks of [128 rows x 128 B]
-  uint8_t* as = sm + off_a;     // phase 1: A slice [KS x r], MN-major, swizzled by TMA
-  uint8_t* ps = sm;             // phase 2: partial h, [128][r] fp32 (row stride r*4+16)
-  uint8_t* g_hi = sm + off_g;   // phase 2: g as two bf16 K-major tiles
+  uint8_t* xs = sm;              // phase 1: x round, XR/64 blocks of [128 rows x 128 B], 128B swizzle
+  uint8_t* as = sm + P.off_a;    // phase 1: A slice [KS x r], MN-major, swizzled by TMA
+  uint8_t* g_hi = sm + P.off_g;  // phase 2: g as two bf16 K-major tiles
   uint8_t* g_lo = g_hi + 16384;
-  uint8_t* bs = sm + off_b;     // phase 2: B chunk, NC/64 boxes of [r rows x 128 B]
-  float* stage = reinterpret_cast<float*>(sm + off_s);
+  uint8_t* bs = sm + P.off_b;    // phase 2: B chunk, NC/64 boxes of [r rows x 128 B]
+  uint8_t* stage = sm + P.off_s;
+  const uint32_t stage_stride = (uint32_t)P.piece * 4u + 16u;
 
-  if (warp == 4) {
-    tmem_alloc(&ctrl->tmem_base, kTmemCols);
-    tmem_relinquish();
-    if (lane == 0) {
-      mbar_init(&ctrl->bar_a, 1);
-      mbar_init(&ctrl->bar_b, 1);
-      mbar_init(&ctrl->bar_shrink, 1);
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&ctrl->bar_full[i], 1);
-        mbar_init(&ctrl->bar_empty[i], kEpilogueThreads);
-      }
-      mbar_fence_init();
-      tma_prefetch_desc(&map_a);
-      tma_prefetch_desc(&map_b);
-    }
-  } else {
-    // per-row metadata: token and weight (weight 0 for padding rows)
+  int32_t slot = -1;
+  if (warp < 4) {
     const int row = tid;
     int32_t tok = -1;
-    float wt = 0.f;
     if (row < tile.nvalid) {
       if (mask_adapter >= 0) {
         tok = tile.row0 + row;
-        wt = ids[tok] == mask_adapter ? 1.f : 0.f;
       } else {
-        const int32_t slot = perm[tile.group_off + tile.row0 + row];
-        if (slot >= 0 && slot < S && ids[slot] == a) {
-          tok = slot / k;
-          wt = w ? w[slot] : 1.f;
-        } else if (crank == 0) {
-          report(err_word, MOLORA_DEV_BAD_PERMUTATION);
-        }
+        slot = perm[tile.group_off + tile.row0 + row];
+        if (slot >= 0 && slot < S) tok = slot / k;
       }
     }
-    s_tok[row] = tok;
-    s_w[row] = wt;
+    ctrl->tok[row] = tok;
+    if (tok >= 0 && P.prefetch_y) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  __syncwarp();
+  cluster_arrive();  // barriers of every CTA initialised and armed (waited on before the first remote store)
 
-  if (warp == 4) {
-    if (lane == 0) {
-      // A slice rows a*d_in + crank*KS + [0, KS), in boxes of 64 rows
-      mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
-      for (int kb = 0; kb < KS / kKBlock; ++kb)
-        tma_load_2d(smem_u32(as + (size_t)kb * kKBlock * r * 2), &map_a, 0, a * d_in + crank * KS + kb * kKBlock,
-                    &ctrl->bar_a);
-    }
-  } else {
-    // gather: lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
-    const int sub = lane >> 3, chunk = lane & 7;
-    const int nkb = KS / kKBlock;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const uint32_t blk = smem_u32(xs + (size_t)kb * kTileM * 128);
-#pragma unroll 4
-      for (int it = 0; it < kTileM / 16; ++it) {
-        const int row = it * 16 + warp * 4 + sub;
-        const int32_t tok = s_tok[row];
-        const __nv_bfloat16* src =
-            tok >= 0 ? x + (int64_t)tok * d_in + crank * KS + kb * kKBlock + chunk * 8 : x;
-        cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
-      }
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-  }
-  __syncthreads();  // x tile in shared memory
-
+  // ---- shrink: rounds of XR columns, each gathered, then consumed by XR/16 MMAs
+  const int rounds = KS / P.XR;
   const uint32_t idesc_shrink = idesc_bf16_f32(kTileM, r, false, true);
   if (warp == 4 && lane == 0) {
-    bool ok = mbar_wait(&ctrl->bar_a, 0);
-    tc_fence_after();
-    if (ok) {
-      const uint32_t atom = 8u * r * 2u;
-      const SmemLayout swz = (SmemLayout)sw_for_rank(r);
-      for (int kb = 0; kb < KS / kKBlock; ++kb)
-        for (int ks = 0; ks < kKBlock / 16; ++ks) {
-          const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
-          const uint64_t db = smem_desc(smem_u32(as + (size_t)(kb * kKBlock + ks * 16) * r * 2), atom, atom, swz);
-          umma_f16(tmem, da, db, idesc_shrink, (kb | ks) != 0);
-        }
-      umma_commit(&ctrl->bar_shrink);
-    } else {
-      ctrl->abort = 1;
-      report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-      mbar_arrive(&ctrl->bar_shrink);
+    mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
+    for (int kb = 0; kb < KS / kKBlock; ++kb)
+      tma_load_2d(smem_u32(as + (size_t)kb * kKBlock * r * 2), &map_a, 0, a * d_in + crank * KS + kb * kKBlock,
+                  &ctrl->bar_a);
+  }
+  if (TM < kTileM && warp < 4) {
+    // MMA rows the tile does not use stay zero in every round
+    for (int i = tid; i < (kTileM - TM) * (P.XR / 8); i += kEpilogueThreads) {
+      const int row = TM + i % (kTileM - TM), cidx = i / (kTileM - TM);
+      *reinterpret_cast<uint4*>(xs + (size_t)(cidx / 8) * kTileM * 128 + sw128_offset(row, cidx % 8)) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
-    // B chunk lands in the (now dead) phase-1 region once the shrink has read it
-    ok = mbar_wait(&ctrl->bar_shrink, 0);
-    if (ok) {
+  }
+  for (int rd = 0; rd < rounds; ++rd) {
+    if (warp < 4) {
+      if (rd > 0 && !mbar_wait(&ctrl->bar_x, (rd - 1) & 1)) {  // previous round consumed
+        ctrl->abort = 1;
+        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+      }
+      // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
+      const int sub = lane >> 3, chunk = lane & 7;
+      for (int kb = 0; kb < P.XR / kKBlock; ++kb) {
+        const uint32_t blk = smem_u32(xs + (size_t)kb * kTileM * 128);
+        const int col = crank * KS + rd * P.XR + kb * kKBlock + chunk * 8;
+#pragma unroll 4
+        for (int it = 0; it < TM / 16; ++it) {
+          const int row = it * 16 + warp * 4 + sub;
+          const int32_t tok = ctrl->tok[row];
+          const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
+          cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (rd == 0) {
+        // validate this row's slot while the gather is in flight
+        const int row = tid;
+        int32_t live = 0;
+        float wt = 0.f;
+        const int32_t tok = ctrl->tok[row];
+        if (tok >= 0) {
+          if (mask_adapter >= 0) {
+            live = 1;
+            wt = ids[tok] == mask_adapter ? 1.f : 0.f;
+          } else if (ids[slot] == a) {
+            live = 1;
+            wt = w ? w[slot] : 1.f;
+          } else if (crank == 0) {
+            report(err_word, MOLORA_DEV_BAD_PERMUTATION);
+          }
+        } else if (row < tile.nvalid && crank == 0) {
+          report(err_word, MOLORA_DEV_BAD_PERMUTATION);
+        }
+        ctrl->live[row] = live;
+        ctrl->wgt[row] = wt;
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    named_barrier(kBarX, kThreads);  // round rd is in shared memory
+    if (warp == 4 && lane == 0) {
+      bool ok = !ctrl->abort;
+      if (ok && rd == 0) ok = mbar_wait(&ctrl->bar_a, 0);
+      tc_fence_after();
+      if (ok) {
+        const uint32_t atom = 8u * r * 2u;
+        const SmemLayout swz = sw_for_rank(r);
+        for (int kb = 0; kb < P.XR / kKBlock; ++kb)
+          for (int ks = 0; ks < kKBlock / 16; ++ks) {
+            const int krow = rd * P.XR + kb * kKBlock + ks * 16;
+            const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
+            const uint64_t db = smem_desc(smem_u32(as + (size_t)krow * r * 2), atom, atom, swz);
+            umma_f16(tmem, da, db, idesc_shrink, (rd | kb | ks) != 0);
+          }
+        umma_commit(&ctrl->bar_x);
+      } else {
+        ctrl->abort = 1;
+        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+        mbar_arrive(&ctrl->bar_x);
+      }
+    }
+  }
+  const uint32_t last_parity = (uint32_t)(rounds - 1) & 1u;
+  if (warp == 4 && lane == 0) {
+    // B chunk lands in the phase-1 region once the last shrink MMAs have read it
+    if (mbar_wait(&ctrl->bar_x, last_parity)) {
       mbar_arrive_expect_tx(&ctrl->bar_b, (uint32_t)NC * r * 2);
       for (int q = 0; q < NC / 64; ++q)
         tma_load_2d(smem_u32(bs + (size_t)q * r * 128), &map_b, crank * NC + q * 64, a * r, &ctrl->bar_b);
@@ -273,42 +381,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&ctrl->bar_b);
     }
   }
+  // ---- cluster reduction of h, pushed rather than pulled: CTA c owns tile rows
+  // [c*RPC, (c+1)*RPC).  Every CTA sends each row's partial h to the row's owner
+  // (st.async into the owner's receive slots, counted by its bar_recv); the owner sums the
+  // C partials in rank order (deterministic), forms g = scale * w * h, splits it into bf16
+  // hi + lo, and sends both rows to every CTA's g tiles (counted by their bar_g).
+  const int RPC = kTileM / C;
+  float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [C sources][RPC rows][r]
+  bool have_h = true;
   if (warp < 4) {
-    // partial h of this CTA: TMEM -> registers -> shared memory (for the cluster reduction)
-    const bool ok = mbar_wait(&ctrl->bar_shrink, 0);
+    have_h = mbar_wait(&ctrl->bar_x, last_parity);
     tc_fence_after();
-    const int row = tid;
-    if (ok) {
-      float v[16];
-      for (int c0 = 0; c0 < r; c0 += 16) {
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-        float4* dst = reinterpret_cast<float4*>(ps + row * p_stride(r) + c0 * 4);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      }
-    } else {
+    if (!have_h) {
       ctrl->abort = 1;
       report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
     }
-    tc_fence_before();
   }
   __syncwarp();
-  cluster_sync();  // every CTA's partial h is in its shared memory
-
+  cluster_wait();  // every CTA's barriers are armed
   if (warp < 4) {
     const int row = tid;
-    const float coef = scale * s_w[row];
-    const uint32_t mine = smem_u32(ps + row * p_stride(r));
-    for (int c0 = 0; c0 < r; c0 += 8) {
-      float h[8];
+    const uint32_t owner = (uint32_t)(row / RPC);
+    const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * r), owner);
+    const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
+    float v[16];
+    for (int c0 = 0; c0 < r; c0 += 16) {
+      if (have_h)
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      else
 #pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = 0.f;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        st_async_v4(dst + (c0 + 4 * i) * 4,
+                    make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                               __float_as_uint(v[4 * i + 3])),
+                    dst_bar);
+    }
+    tc_fence_before();
+    // owner: reduce its rows once every source has delivered them
+    const bool got = mbar_wait(&ctrl->bar_recv, 0);
+    if (!got) {
+      ctrl->abort = 1;
+      report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+    }
+    const int groups = r / 8;
+    for (int item = tid; item < RPC * groups; item += kEpilogueThreads) {
+      const int rl = item / groups, c0 = (item % groups) * 8;
+      const int trow = crank * RPC + rl;
+      float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int cc = 0; cc < C; ++cc) {
-        const uint32_t src = dsmem_addr(mine, (uint32_t)cc) + c0 * 4;
-        const float4 p0 = dsmem_ld_f4(src), p1 = dsmem_ld_f4(src + 16);
+        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * RPC + rl) * r + c0);
+        const float4 p0 = src[0], p1 = src[1];
         h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
         h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
       }
+      const float coef = scale * ctrl->wgt[trow];
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -319,24 +447,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
         lo[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
       }
-      const uint32_t off = sw128_offset(row, c0 / 8);
-      *reinterpret_cast<uint4*>(g_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(g_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      const uint32_t off = sw128_offset(trow, c0 / 8);
+      const uint4 vh = make_uint4(hi[0], hi[1], hi[2], hi[3]), vl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      for (int d = 0; d < C; ++d) {
+        const uint32_t bar_d = dsmem_addr(smem_u32(&ctrl->bar_g), (uint32_t)d);
+        st_async_v4(dsmem_addr(smem_u32(g_hi + off), (uint32_t)d), vh, bar_d);
+        st_async_v4(dsmem_addr(smem_u32(g_lo + off), (uint32_t)d), vl, bar_d);
+      }
     }
-    fence_proxy_async_smem();
   }
   __syncwarp();
-  cluster_arrive();  // done reading the other CTAs' partials (waited on before exit)
-  __syncthreads();   // g ready for the tensor core
 
-  const int npass = (NC + kPassN - 1) / kPassN;
+  const int npass = (NC + P.PW - 1) / P.PW;
   if (warp == 4) {
     if (lane == 0) {
-      bool ok = !ctrl->abort && mbar_wait(&ctrl->bar_b, 0);
+      bool ok = !ctrl->abort && mbar_wait(&ctrl->bar_b, 0) && mbar_wait(&ctrl->bar_g, 0);
+      fence_proxy_async_smem();
       tc_fence_after();
       for (int p = 0; p < npass; ++p) {
         const int buf = p & 1;
-        const int width = min(kPassN, NC - p * kPassN);
+        const int width = min(P.PW, NC - p * P.PW);
         if (p >= 2 && ok) ok = mbar_wait(&ctrl->bar_empty[buf], ((p >> 1) - 1) & 1);
         if (!ok) {
           ctrl->abort = 1;
@@ -346,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(kTileM, width, false, true);
-        const uint32_t d = tmem + buf * kPassN;
+        const uint32_t d = tmem + buf * P.PW;
         for (int ks = 0; ks < r / 16; ++ks) {
-          const uint64_t db = smem_desc(smem_u32(bs + (size_t)(p * (kPassN / 64)) * r * 128 + ks * 2048), r * 128,
+          const uint64_t db = smem_desc(smem_u32(bs + (size_t)(p * (P.PW / 64)) * r * 128 + ks * 2048), r * 128,
                                         1024, kSwizzle128B);
           umma_f16(d, smem_desc(smem_u32(g_hi + ks * 32), 16, 1024, kSwizzle128B), db, idesc, ks != 0);
           umma_f16(d, smem_desc(smem_u32(g_lo + ks * 32), 16, 1024, kSwizzle128B), db, idesc, 1);
@@ -358,42 +488,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
+    // Each thread drains its own TMEM lane (tile row) into the staging rows; then the warp
+    // walks its 32 rows and adds each row segment into y with coalesced 16-byte L2
+    // reductions (lanes cover consecutive columns of one row).
     const int row = tid;
-    const int32_t tok = s_tok[row];
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float* srow = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(stage) + row * kStageStride);
+    float* srow = reinterpret_cast<float*>(stage + row * stage_stride);
+    const int lanes_per_row = P.piece / 4;           // 16 or 32
+    const int rows_per_step = 32 / lanes_per_row;    // 2 or 1
+    const int sub_row = lane / lanes_per_row, col4 = (lane % lanes_per_row) * 4;
+    const int32_t my_tok = ctrl->live[row] ? ctrl->tok[row] : -1;
     for (int p = 0; p < npass; ++p) {
       const int buf = p & 1;
-      const int width = min(kPassN, NC - p * kPassN);
+      const int width = min(P.PW, NC - p * P.PW);
       const bool ok = mbar_wait(&ctrl->bar_full[buf], (p >> 1) & 1);
       tc_fence_after();
       if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-      for (int q = 0; ok && !ctrl->abort && q < width; q += kPieceN) {
-        const int cols = min(kPieceN, width - q);
-        bulk_wait_read<0>();  // this row's previous reduction has finished reading the stage
-        float v[16];
-        for (int c0 = 0; c0 < cols; c0 += 16) {
-          tmem_ld16(lane_base + buf * kPassN + q + c0, v);
+      for (int q = 0; ok && !ctrl->abort && q < width; q += P.piece) {
+        const int cols = min(P.piece, width - q);
+        if (P.epi == kEpiBulk) bulk_wait_read<0>();  // this row's previous reduction has read the stage
+        for (int c0 = 0; c0 < cols; c0 += 32) {
+          float v[32];
+          tmem_ld32(lane_base + buf * P.PW + q + c0, v);
           float4* dst = reinterpret_cast<float4*>(srow + c0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
-        fence_proxy_async_smem();
-        if (tok >= 0) {
-          bulk_reduce_add_f32(y + (int64_t)tok * d_out + crank * NC + p * kPassN + q, smem_u32(srow), cols * 4);
-          bulk_commit();
+        const int col_base = crank * NC + p * P.PW + q + col4;
+        if (P.epi == kEpiBulk || P.epi == kEpiMixed) {
+          // one bulk reduction per row segment, performed by the TMA unit in L2; in the mixed
+          // mode only the even rows go this way and the warp adds the odd rows itself with
+          // 16-byte reductions, so the TMA unit and the load/store path work side by side
+          fence_proxy_async_smem();
+          if (my_tok >= 0 && (P.epi == kEpiBulk || (row & 1) == 0)) {
+            bulk_reduce_add_f32(y + (int64_t)my_tok * d_out + crank * NC + p * P.PW + q, smem_u32(srow),
+                                (uint32_t)cols * 4u);
+            bulk_commit();
+          }
+          if (P.epi == kEpiMixed) {
+            __syncwarp();
+            for (int j = 1; j < 32; j += 2 * rows_per_step) {
+              // rows_per_step rows at a time among the odd ones: j, j+2, ...
+              const int rr = warp * 32 + j + 2 * sub_row;
+              const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
+              if (tok >= 0 && col4 < cols) {
+                const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
+                red_add_v4(y + (int64_t)tok * d_out + col_base, d);
+              }
+            }
+            __syncwarp();
+          }
+        } else if (P.epi == kEpiPlain) {
+          // k == 1: this tile row is the only writer of its y row segment, so a plain
+          // read-modify-write (one fp32 add per element, as the reduction would do); eight
+          // loads in flight per lane before the adds and stores
+          __syncwarp();
+          for (int j0 = 0; j0 < 32; j0 += rows_per_step * 8) {
+            float4 yv[8];
+            float* yp[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int rr = warp * 32 + j0 + u * rows_per_step + sub_row;
+              const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
+              yp[u] = (tok >= 0 && col4 < cols) ? y + (int64_t)tok * d_out + col_base : nullptr;
+              if (yp[u]) yv[u] = *reinterpret_cast<const float4*>(yp[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (!yp[u]) continue;
+              const int rr = warp * 32 + j0 + u * rows_per_step + sub_row;
+              const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
+              yv[u].x += d.x, yv[u].y += d.y, yv[u].z += d.z, yv[u].w += d.w;
+              *reinterpret_cast<float4*>(yp[u]) = yv[u];
+            }
+          }
+          __syncwarp();
+        } else {
+          // coalesced 16-byte L2 reductions, lanes over consecutive columns of one row
+          __syncwarp();
+          for (int j = 0; j < 32; j += rows_per_step) {
+            const int rr = warp * 32 + j + sub_row;
+            const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
+            if (tok >= 0 && col4 < cols) {
+              const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
+              red_add_v4(y + (int64_t)tok * d_out + col_base, d);
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
       mbar_arrive(&ctrl->bar_empty[buf]);
     }
-    bulk_wait_all();
+    if (P.epi == kEpiBulk) bulk_wait_all();
   }
   __syncthreads();
-  cluster_wait();  // no CTA leaves while another may still read its partials
+  cluster_arrive();
+  cluster_wait();  // no CTA leaves while another may still write into its shared memory
   if (warp == 4) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, P.tmem_cols);
   }
 }
 
@@ -410,6 +604,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
   });
   return fn;
 }
@@ -431,10 +627,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }  // namespace
 
 bool grouped_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, int32_t k) {
-  (void)N, (void)K, (void)k;
   if (dtype != MOLORA_BF16 || !(r == 16 || r == 32 || r == 64)) return false;
-  GroupedShape s;
-  return choose(d_in, d_out, r, &s) && encoder() != nullptr;
+  GroupedPlan s;
+  return choose(d_in, d_out, r, N * (int64_t)k, K, &s) && encoder() != nullptr;
 }
 
 cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
@@ -442,8 +637,16 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
                                 const int32_t* counts, const int32_t* offsets, const int32_t* perm, float scale,
                                 float* y, int32_t mask_adapter, int32_t* err_word, cudaStream_t stream) {
   (void)counts;
-  GroupedShape s;
-  if (!choose(d_in, d_out, r, &s)) return cudaErrorNotSupported;
+  GroupedPlan s;
+  if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
+    return cudaErrorNotSupported;
+  s.epi = kEpiBulk;
+  s.prefetch_y = 0;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_EPI")) s.epi = atoi(e);
+  if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
+  if (s.epi == kEpiPlain && k != 1) s.epi = kEpiRed;
+#endif
   CUtensorMap map_a, map_b;
   const CUtensorMapSwizzle swa =
       r == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
@@ -457,27 +660,11 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
     if (attr_err != cudaSuccess) cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return attr_err;
-  static_assert(sizeof(Ctrl) <= 2048, "control block");
 
-  const int64_t tiles = mask_adapter >= 0 ? (N + kTileM - 1) / kTileM : (N * k + kTileM - 1) / kTileM + K;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * s.C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = s.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)s.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, lora_grouped_kernel, static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r,
-                            k, ids, w, offsets, perm, scale, y, mask_adapter, (int32_t)s.C, (int32_t)s.KS,
-                            (int32_t)s.NC, (uint32_t)s.off_a, (uint32_t)s.off_g, (uint32_t)s.off_b,
-                            (uint32_t)s.off_s, (uint32_t)align_up(s.region, 1024), err_word, map_a, map_b);
-  const cudaError_t last = cudaGetLastError();  // clears the runtime's error state either way
-  return e != cudaSuccess ? e : last;
+  const int64_t tiles = mask_adapter >= 0 ? (N + s.TM - 1) / s.TM : (N * k + s.TM - 1) / s.TM + K;
+  return launch_kernel(lora_grouped_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C,
+                       static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r, k, ids, w, offsets, perm, scale, y,
+                       mask_adapter, s, err_word, map_a, map_b);
 }
 
 }  // namespace molora

@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kScalarThreads)
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const T* xr = x + t * (int64_t)d_in;
+  pdl_wait();
+  pdl_launch_dependents();
 
   for (int j = 0; j < k; ++j) {
     int32_t a;
@@ -185,25 +187,24 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
   const T* Bp = static_cast<const T*>(B);
   switch (r) {
     case 8:
-      lora_scalar_kernel<T, 8><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k, scale,
-                                                                       y, cols, mask_adapter, err_word);
+      return launch_kernel(lora_scalar_kernel<T, 8>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
+                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
       break;
     case 16:
-      lora_scalar_kernel<T, 16><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
-                                                                        scale, y, cols, mask_adapter, err_word);
+      return launch_kernel(lora_scalar_kernel<T, 16>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
+                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
       break;
     case 32:
-      lora_scalar_kernel<T, 32><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
-                                                                        scale, y, cols, mask_adapter, err_word);
+      return launch_kernel(lora_scalar_kernel<T, 32>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
+                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
       break;
     case 64:
-      lora_scalar_kernel<T, 64><<<grid, kScalarThreads, smem, stream>>>(xp, d_in, d_out, Ap, Bp, K, ids, w, k,
-                                                                        scale, y, cols, mask_adapter, err_word);
+      return launch_kernel(lora_scalar_kernel<T, 64>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
+                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
       break;
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
@@ -235,6 +236,8 @@ __global__ void __launch_bounds__(256)
   __shared__ float lg[kRouterTok][kMaxAdapters];
   const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
   const int j = threadIdx.x & 63, grp = threadIdx.x >> 6;
+  pdl_wait();
+  pdl_launch_dependents();
   float acc[kRouterTok];
 #pragma unroll
   for (int q = 0; q < kRouterTok; ++q) acc[q] = 0.f;
@@ -289,14 +292,12 @@ cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, i
                                  float* logits, int32_t* ids, float* w, cudaStream_t stream) {
   const unsigned grid = (unsigned)((N + kRouterTok - 1) / kRouterTok);
   if (dtype == MOLORA_BF16)
-    router_scalar_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), N, d_in, static_cast<const __nv_bfloat16*>(W1), b1,
-        static_cast<const __nv_bfloat16*>(W2), b2, K, k, logits, ids, w);
-  else
-    router_scalar_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), N, d_in,
-                                                          static_cast<const float*>(W1), b1,
-                                                          static_cast<const float*>(W2), b2, K, k, logits, ids, w);
-  return cudaGetLastError();
+    return launch_kernel(router_scalar_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, 0,
+                         static_cast<const __nv_bfloat16*>(x), N, d_in, static_cast<const __nv_bfloat16*>(W1), b1,
+                         static_cast<const __nv_bfloat16*>(W2), b2, K, k, logits, ids, w);
+  return launch_kernel(router_scalar_kernel<float>, dim3(grid), dim3(256), 0, stream, 0, static_cast<const float*>(x),
+                       N, d_in, static_cast<const float*>(W1), b1, static_cast<const float*>(W2), b2, K, k, logits, ids,
+                       w);
 }
 
 }  // namespace molora

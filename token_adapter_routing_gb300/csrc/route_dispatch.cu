@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) route_vocab_kernel(const int32_t* __restr
                                                           const int32_t* __restrict__ starts, int32_t K,
                                                           int32_t* __restrict__ adapter, int32_t* err_word) {
   __shared__ int32_t s_starts[kMaxAdapters + 1];
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = threadIdx.x; i <= K; i += blockDim.x) s_starts[i] = starts[i];
   __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -48,8 +50,7 @@ cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* sta
                                int32_t* err_word, cudaStream_t stream) {
   const int64_t blocks = (N + 255) / 256;
   const int grid = (int)(blocks < 8 * num_sms() ? blocks : 8 * num_sms());
-  route_vocab_kernel<<<grid, 256, 0, stream>>>(tok, N, starts, K, adapter, err_word);
-  return cudaGetLastError();
+  return launch_kernel(route_vocab_kernel, dim3(grid), dim3(256), 0, stream, 0, tok, N, starts, K, adapter, err_word);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -70,6 +71,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   __shared__ int32_t s_off[kMaxAdapters + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
 
   const int64_t per_warp = ((S + kDispatchWarps * 32 - 1) / (kDispatchWarps * 32)) * 32;
@@ -140,8 +143,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
 
 cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* err_word, cudaStream_t stream) {
-  dispatch_kernel<<<1, kDispatchWarps * 32, 0, stream>>>(ids, N * (int64_t)k, K, counts, offsets, perm, err_word);
-  return cudaGetLastError();
+  return launch_kernel(dispatch_kernel, dim3(1), dim3(kDispatchWarps * 32), 0, stream, 0, ids, N * (int64_t)k, K,
+                       counts, offsets, perm, err_word);
 }
 
 }  // namespace molora

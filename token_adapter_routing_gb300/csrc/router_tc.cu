@@ -98,7 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_w1);
     }
-  } else {
+  }
+  pdl_wait();  // the inputs may come from the previous kernel; the prologue above overlapped it
+  pdl_launch_dependents();
+  if (warp < 4) {
     for (int i = tid; i < kRouterHidden * K; i += kTileM) w2s[i] = __bfloat162float(W2[i]);
     if (tid < kRouterHidden) b1s[tid] = b1 ? b1[tid] : 0.f;
     if (tid < K) b2s[tid] = b2 ? b2[tid] : 0.f;
@@ -262,23 +265,9 @@ cudaError_t launch_router_tc(const void* x, int64_t N, int32_t d_in, const void*
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = (N + kTileM - 1) / kTileM;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * s.C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = s.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)s.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, router_tc_kernel, N, d_in, static_cast<const __nv_bfloat16*>(W2), b1, b2, K, k,
-                            logits, ids, w, (int32_t)s.C, (int32_t)s.KS, (uint32_t)s.off_w1, (uint32_t)s.off_w2,
-                            (uint32_t)s.region, map_x, map_w1);
-  const cudaError_t last = cudaGetLastError();  // clears the runtime's error state either way
-  return e != cudaSuccess ? e : last;
+  return launch_kernel(router_tc_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C, N, d_in,
+                       static_cast<const __nv_bfloat16*>(W2), b1, b2, K, k, logits, ids, w, (int32_t)s.C,
+                       (int32_t)s.KS, (uint32_t)s.off_w1, (uint32_t)s.off_w2, (uint32_t)s.region, map_x, map_w1);
 }
 
 }  // namespace molora
