@@ -6,8 +6,8 @@ bf16 x / A / B, fp32 y updated in place, tokens in runs of geometric length (mea
 uniformly drawn modality (vocabulary range) per run; synthetic, seeded.
 
 One step = the whole path over one batch: vocabulary routing -> dispatch (histogram, scan,
-permutation) -> grouped LoRA apply, as two CUDA graphs (route+dispatch, apply) with CUDA
-events around each.  Between timed steps a 256 MiB buffer (about twice the 129 MB L2) is
+permutation) -> grouped LoRA apply, captured as one CUDA graph (the kernels overlap their
+prologues through programmatic dependent launch) with CUDA events around each replay.  Between timed steps a 256 MiB buffer (about twice the 129 MB L2) is
 written so every step starts with cold caches.  ``value`` = tokens / mean step time;
 ``apply_only`` gives the same for the apply kernel alone, and ``roofline`` relates that
 kernel's algorithmic bytes per launch (x read once, y read and written once, the adapters
@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq"], default="step",
+                   help="step: the contract line; the others print extra measurement lines (see run_mode)")
+    p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     return p.parse_args(argv)
 
 
@@ -187,58 +190,54 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     stream = torch.cuda.Stream(device=dev)
-    g_rd, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        # eager run first (loads the module, sets kernel attributes), then capture
+    g_step, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+
+    def path_calls():
         m.molora_route_vocab(tok, starts, adapter=adapter, err_word=err)
         m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm, err_word=err)
         m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
                             err_word=err, path=args.path)
+
+    with torch.cuda.stream(stream):
+        path_calls()  # eager run first (loads the module, sets kernel attributes), then capture
         stream.synchronize()
-        with torch.cuda.graph(g_rd, stream=stream):
-            m.molora_route_vocab(tok, starts, adapter=adapter, err_word=err)
-            m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm, err_word=err)
+        with torch.cuda.graph(g_step, stream=stream):
+            path_calls()
         with torch.cuda.graph(g_apply, stream=stream):
             m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
                                 err_word=err, path=args.path)
     n_active = int((torch.bincount(adapter.cpu().long(), minlength=wl.K) > 0).sum().item())
     launches_per_step = 3  # route_vocab, dispatch, apply
 
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        g_rd.replay()
-        if evs is not None:
-            evs[1].record(stream)
-        g_apply.replay()
-        if evs is not None:
-            evs[2].record(stream)
+    def timed(graph, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()  # outside the events: each step starts with a cold L2
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        stream.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             flush.zero_()
-            step()
+            g_step.replay()
         stream.synchronize()
         clocks = ClockSampler(local)
         clocks.start()
         t_end = time.time() + args.soak_s
         while time.time() < t_end:
-            for _ in range(50):
-                flush.zero_()
-                step()
-            stream.synchronize()
+            timed(g_step, 50)
         barrier(world)
         torch.cuda.synchronize()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.zero_()  # outside the events: each step starts with a cold L2
-            step(evs[i])
-        stream.synchronize()
+        step_ms = timed(g_step, args.steps)      # the whole path, one CUDA graph per step
+        torch.cuda.synchronize()
+        barrier(world)
+        apply_ms = timed(g_apply, args.steps)    # the apply kernel alone, for its roofline
         torch.cuda.synchronize()
         barrier(world)
         clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    apply_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
     apply_s = max_over_ranks(sum(apply_ms) / 1e3, world, dev)
     agg = aggregate(wl.N, world, total_s, args.steps)
@@ -271,7 +270,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": "4-modality kernel benchmark: N=2048 tokens, d_in=d_out=4096, K=4, r=16, "
                                "bf16 x/A/B, fp32 y, vocabulary routing, geometric runs (mean 64)",
                    "global_batch": wl.N * world, "tokens_per_rank": wl.N, "path": args.path,
-                   "step": "route_vocab -> dispatch -> lora_apply (2 CUDA graphs)",
+                   "step": "route_vocab -> dispatch -> lora_apply, one CUDA graph (PDL between kernels)",
                    "l2": "256 MiB buffer written between timed steps (outside the timed events)",
                    "parallelism": f"dp{world}" if world > 1 else "single-gpu"},
         "apply_only": {"value": round(wl.N * world / apply_mean_s, 1), "unit": UNIT,
@@ -279,6 +278,8 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
+        "apply_timing": "the apply kernel replayed alone from its own CUDA graph, same inputs, same L2 flush, "
+                        "timed in a second loop of the same run",
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -398,9 +399,163 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# --------------------------------------------------------------------------- extra modes
+
+def _graph(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def _replay_ms(g, stream, reps, flush=None):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            if flush is not None:
+                flush.zero_()
+            g.replay()
+        for e0, e1 in evs:
+            if flush is not None:
+                flush.zero_()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+    return sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def _pct(v, q):
+    return v[min(len(v) - 1, int(q * len(v)))]
+
+
+def run_mode(args):
+    """Extra measurements, one JSON line per point:
+    crossover  decode sweep (Figures 5 and 9): batch 1..512 x K 4..64 hot-set adapters, d=4096,
+               r=16, top-1, uniform and Zipf(1.1) adapter draws; route -> dispatch -> apply as
+               one CUDA graph on the scalar and on the grouped path, L2 flushed between replays.
+    topk       top-k scaling (Table 16): N=8192, d=4096, K=8, r=64, k=1..4, router -> dispatch
+               -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
+    router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
+               K=4, r=16, top-2): router alone, and router -> dispatch -> apply.
+    perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
+               passes over all tokens against one per-token pass."""
+    import token_adapter_routing_gb300 as m
+    from token_adapter_routing_gb300 import build as lib_build
+    lib_build.build()
+    m.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    if args.mode == "crossover":
+        for dist in ("uniform", "zipf"):
+            for K in (4, 8, 16, 32, 64):
+                for b in (1, 8, 32, 64, 128, 160, 256, 512):
+                    wl = workloads.make("decode_sweep", N=b, K=K, dist=dist)
+                    tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+                    x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+                    adapter = torch.empty(b, dtype=torch.int32, device=dev)
+                    counts = torch.empty(K, dtype=torch.int32, device=dev)
+                    offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
+                    perm = torch.empty(b, dtype=torch.int32, device=dev)
+                    row = {"mode": "crossover", "dist": dist, "K": K, "batch": b}
+                    for path in ("scalar", "grouped"):
+                        def fn(path=path):
+                            m.molora_route_vocab(tok, starts, adapter=adapter)
+                            m.molora_dispatch(adapter, K, counts=counts, offsets=offsets, perm=perm)
+                            m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets,
+                                                perm=perm, path=path)
+                        ms = _replay_ms(_graph(fn, stream), stream, 30, flush)
+                        row[f"{path}_us_p50"] = round(_pct(ms, 0.5) * 1e3, 2)
+                    row["distinct_adapters"] = int(torch.unique(adapter).numel())
+                    row["faster"] = "grouped" if row["grouped_us_p50"] < row["scalar_us_p50"] else "scalar"
+                    emit(row)
+    elif args.mode == "topk":
+        for k in (1, 2, 3, 4):
+            wl = workloads.make("topk_scaling", k=k)
+            x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),
+                                  wl.y0.to(dev))
+            ids = torch.empty(wl.N, k, dtype=torch.int32, device=dev)
+            w = torch.empty(wl.N, k, dtype=torch.float32, device=dev)
+            counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+            offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(wl.N * k, dtype=torch.int32, device=dev)
+
+            def fn():
+                m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False)
+                m.molora_dispatch(ids, wl.K, counts=counts, offsets=offsets, perm=perm)
+                m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm)
+            ms = _replay_ms(_graph(fn, stream), stream, args.replays)
+            p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
+            emit({"mode": "topk", "workload": "N=8192, d=4096, K=8, r=64, router d->64->K", "k": k,
+                  "replays": args.replays, "p50_ms": round(p50, 5), "p99_ms": round(p99, 5),
+                  "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1), "l2": "not flushed (back-to-back replays)"})
+    elif args.mode == "router":
+        wl = workloads.make("topk_mlp")
+        x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),
+                              wl.y0.to(dev))
+        logits = torch.empty(wl.N, wl.K, dtype=torch.float32, device=dev)
+        ids = torch.empty(wl.N, wl.k, dtype=torch.int32, device=dev)
+        w = torch.empty(wl.N, wl.k, dtype=torch.float32, device=dev)
+        counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+        offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(wl.N * wl.k, dtype=torch.int32, device=dev)
+        g_router = _graph(lambda: m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w), stream)
+
+        def full():
+            m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w)
+            m.molora_dispatch(ids, wl.K, counts=counts, offsets=offsets, perm=perm)
+            m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm)
+        g_full = _graph(full, stream)
+        r_ms = _replay_ms(g_router, stream, 100, flush)
+        f_ms = _replay_ms(g_full, stream, 100, flush)
+        rb = wl.N * wl.d_in * 2 + wl.d_in * 64 * 2 + wl.N * (wl.K + 2 * wl.k) * 4
+        emit({"mode": "router", "workload": "N=4096, d_in=2048, d_out=6144, K=4, r=16, k=2",
+              "router_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
+              "router_GBps": round(rb / (_pct(r_ms, 0.5) * 1e-3) / 1e9, 1),
+              "router_tflops": round(2 * wl.N * wl.d_in * 64 / (_pct(r_ms, 0.5) * 1e-3) / 1e12, 1),
+              "path_us_p50": round(_pct(f_ms, 0.5) * 1e3, 2),
+              "path_tokens_per_s": round(wl.N / (_pct(f_ms, 0.5) * 1e-3), 1), "l2": "flushed between replays"})
+    elif args.mode == "perseq":
+        wl = workloads.make(WORKLOAD)
+        tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+        x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+        adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+        counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+        offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+
+        def per_token():
+            m.molora_route_vocab(tok, starts, adapter=adapter)
+            m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm)
+            m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
+
+        def per_sequence():
+            m.molora_route_vocab(tok, starts, adapter=adapter)
+            for a in range(wl.K):
+                m.molora_lora_apply_masked_pass(x, A, B, adapter, a, y, wl.scale)
+        t_ms = _replay_ms(_graph(per_token, stream), stream, 100, flush)
+        s_ms = _replay_ms(_graph(per_sequence, stream), stream, 100, flush)
+        emit({"mode": "perseq", "workload": "N=2048, d=4096, K=4, r=16 (4-modality benchmark)",
+              "per_token_us_p50": round(_pct(t_ms, 0.5) * 1e3, 2), "per_sequence_us_p50": round(_pct(s_ms, 0.5) * 1e3, 2),
+              "passes": {"per_token": 1, "per_sequence": wl.K},
+              "speedup": round(_pct(s_ms, 0.5) / _pct(t_ms, 0.5), 2), "l2": "flushed between replays"})
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
+    if args.mode != "step":
+        return run_mode(args) if rank == 0 else 0
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:

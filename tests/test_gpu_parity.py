@@ -347,3 +347,49 @@ def test_graph_captured_learned_path(m, path):
     check_router(wl, 2, logits, ids, w)
     y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids.cpu(), wl.y0, wl.scale, w.cpu())
     assert_apply_close(y, y_ref)
+
+
+# ------------------------------------------------------------------------- full-size workloads
+
+def test_full_size_topk_mlp_path(m):
+    # N=4096, d_in=2048, d_out=6144, K=4, r=16, top-2: the whole path against the oracle
+    wl = workloads.make("topk_mlp")
+    x = dev(wl.x)
+    logits, ids, w = m.molora_router_topk(x, dev(wl.W1), dev(wl.W2), 2)
+    counts, offsets, perm = m.molora_dispatch(ids, wl.K)
+    y = dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(x, dev(wl.A), dev(wl.B), ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm,
+                        err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    check_router(wl, 2, logits, ids, w)
+    rc, ro, rp, _ = oracle.dispatch(ids.cpu(), wl.K)
+    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids.cpu(), wl.y0, wl.scale, w.cpu())
+    assert_apply_close(y, y_ref)
+
+
+@pytest.mark.parametrize("k", [1, 4])
+def test_full_size_topk_scaling_sampled(m, k):
+    # N=8192, d=4096, K=8, r=64: full-size run, oracle on 96 sampled tokens (rows are independent)
+    wl = workloads.make("topk_scaling", k=k)
+    x = dev(wl.x)
+    logits, ids, w = m.molora_router_topk(x, dev(wl.W1), dev(wl.W2), k)
+    counts, offsets, perm = m.molora_dispatch(ids, wl.K)
+    y = dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(x, dev(wl.A), dev(wl.B), ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm,
+                        err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    g = torch.Generator().manual_seed(k)
+    rows = torch.cat([torch.tensor([0, wl.N - 1]), torch.randperm(wl.N, generator=g)[:94]])
+    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x[rows], wl.W1, wl.W2, k)
+    assert torch.allclose(logits.cpu()[rows], ref_logits, rtol=1e-4, atol=1e-4)
+    y_ref, _ = oracle.lora_apply(wl.x[rows].contiguous(), wl.A, wl.B, ids.cpu()[rows].contiguous(), wl.y0[rows].contiguous(),
+                                 wl.scale, w.cpu()[rows].contiguous())
+    assert_apply_close(y.cpu()[rows], y_ref)
+    # dispatch over all 8192*k slots stays bit-exact
+    rc, ro, rp, _ = oracle.dispatch(ids.cpu(), wl.K)
+    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)

@@ -83,6 +83,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t sdst, const void* gsrc, uin
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Wait until at most N committed cp.async groups of this thread are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ proxies / bulk async
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -261,6 +266,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
 // rows are 128 bytes and which uses the 128-byte swizzle (8-row, 1024-byte atoms).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a K-major tile whose rows are
+// `row_bytes` long (32, 64 or 128) and which uses the swizzle of that width (8-row atoms):
+// the chunk index is XOR-ed with the row bits that sit at address bits 7.. of the atom.
+__device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uint32_t row_bytes) {
+  const uint32_t f = row_bytes == 32 ? (row >> 2) & 1u : (row_bytes == 64 ? (row >> 1) & 3u : row & 7u);
+  return row * row_bytes + ((chunk ^ f) << 4);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

@@ -63,7 +63,7 @@ struct GroupedPlan {
   int piece;         // columns per bulk reduction
   uint32_t tmem_cols;
   uint32_t off_a;    // phase 1: A slice after the x round buffer
-  uint32_t off_g;    // phase 2: g_hi (g_lo follows at +16 KB)
+  uint32_t off_g;    // phase 2: g_hi (g_lo follows at +128*r*2 bytes)
   uint32_t off_b;    // phase 2: B column chunk
   uint32_t off_s;    // phase 2: epilogue staging
   uint32_t off_recv; // receive slots for partial h, [C sources][128/C rows][r] fp32
@@ -75,6 +75,8 @@ struct GroupedPlan {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, GroupedPlan* s);
+
 bool plan_one(int32_t d_in, int32_t d_out, int32_t r, int C, int TM, bool two_per_sm, GroupedPlan* s) {
   if (d_in % (C * kKBlock) || d_out % (C * 64)) return false;
   s->TM = TM;
@@ -82,15 +84,24 @@ bool plan_one(int32_t d_in, int32_t d_out, int32_t r, int C, int TM, bool two_pe
   s->KS = d_in / C;
   s->NC = d_out / C;
   s->PW = two_per_sm ? 128 : 256;
-  s->piece = two_per_sm ? 64 : 128;
   s->tmem_cols = two_per_sm ? 256 : 512;
   const size_t budget = two_per_sm ? kSmemPerSm / 2 - kSmemReservedPerCta : kMaxSmem;
+  // g tiles are K-major with rows of r bf16 and the swizzle that matches that row width
+  const size_t g_tile = (size_t)kTileM * r * 2;
+  for (int piece : {128, 64}) {
+    s->piece = piece;
+    if (plan_layout(r, g_tile, budget, two_per_sm, s)) return true;
+  }
+  return false;
+}
+
+bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, GroupedPlan* s) {
   // phase 2 (after this CTA's shrink): g tiles, B chunk, epilogue staging.  g arrives from
   // the row owners only after every CTA of the cluster finished its shrink, so it may reuse
   // phase-1 space.  The receive slots for partial h get their own region: other CTAs may
   // push into them while this CTA's tensor core still reads its x tile.
   const size_t stage = (size_t)kTileM * (s->piece * 4 + 16);
-  const size_t off_b = 2 * 16384;
+  const size_t off_b = align_up(2 * g_tile, 1024);
   const size_t off_s = align_up(off_b + (size_t)s->NC * r * 2, 1024);
   const size_t phase2 = off_s + stage;
   const size_t recv = align_up((size_t)kTileM * r * 4, 1024);
@@ -99,13 +110,14 @@ bool plan_one(int32_t d_in, int32_t d_out, int32_t r, int C, int TM, bool two_pe
   s->off_s = (uint32_t)off_s;
   for (int XR = s->KS > 256 ? 256 : s->KS; XR >= kKBlock; XR -= kKBlock) {
     if (s->KS % XR) continue;
-    const size_t phase1 = (size_t)XR * kTileM * 2 + (size_t)s->KS * r * 2;
+    const int nbuf = s->KS / XR > 1 ? 2 : 1;  // rounds alternate between two x buffers
+    const size_t phase1 = (size_t)nbuf * XR * kTileM * 2 + (size_t)s->KS * r * 2;
     const size_t shared_region = align_up(phase1 > phase2 ? phase1 : phase2, 1024);
     size_t smem = shared_region + recv + 1024 /* base alignment slack */ + kCtrlBytes;
     if (!two_per_sm && smem < kSmemPerSm / 2) smem = kSmemPerSm / 2;  // keep it at one CTA per SM
     if (smem <= budget) {
       s->XR = XR;
-      s->off_a = (uint32_t)((size_t)XR * kTileM * 2);
+      s->off_a = (uint32_t)((size_t)nbuf * XR * kTileM * 2);
       s->off_recv = (uint32_t)shared_region;
       s->region = (uint32_t)(shared_region + recv);
       s->smem = (uint32_t)smem;
@@ -147,7 +159,7 @@ struct TileInfo {
 struct __align__(8) Ctrl {
   uint64_t bar_a;         // TMA of the A slice
   uint64_t bar_b;         // TMA of the B chunk
-  uint64_t bar_x;         // shrink MMAs of one x round done (one phase per round)
+  uint64_t bar_x[2];      // shrink MMAs reading x buffer b done (one phase per use of the buffer)
   uint64_t bar_full[2];   // expand pass done, per TMEM buffer
   uint64_t bar_empty[2];  // epilogue drained a TMEM buffer
   uint64_t bar_recv;      // partial-h rows this CTA owns have arrived from every CTA
@@ -191,7 +203,8 @@ __global__ void __maxnreg__(168)
     if (lane == 0) {
       mbar_init(&ctrl->bar_a, 1);
       mbar_init(&ctrl->bar_b, 1);
-      mbar_init(&ctrl->bar_x, 1);
+      mbar_init(&ctrl->bar_x[0], 1);
+      mbar_init(&ctrl->bar_x[1], 1);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&ctrl->bar_full[i], 1);
         mbar_init(&ctrl->bar_empty[i], kEpilogueThreads);
@@ -253,10 +266,11 @@ __global__ void __maxnreg__(168)
   }
   const int a = tile.adapter;
 
-  uint8_t* xs = sm;              // phase 1: x round, XR/64 blocks of [128 rows x 128 B], 128B swizzle
+  uint8_t* xs = sm;              // phase 1: two x round buffers, XR/64 blocks of [128 rows x 128 B], 128B swizzle
   uint8_t* as = sm + P.off_a;    // phase 1: A slice [KS x r], MN-major, swizzled by TMA
-  uint8_t* g_hi = sm + P.off_g;  // phase 2: g as two bf16 K-major tiles
-  uint8_t* g_lo = g_hi + 16384;
+  uint8_t* g_hi = sm + P.off_g;  // phase 2: g as two bf16 K-major tiles, rows of r elements
+  uint8_t* g_lo = g_hi + (size_t)kTileM * r * 2;
+  const uint32_t g_row_bytes = (uint32_t)r * 2u;
   uint8_t* bs = sm + P.off_b;    // phase 2: B chunk, NC/64 boxes of [r rows x 128 B]
   uint8_t* stage = sm + P.off_s;
   const uint32_t stage_stride = (uint32_t)P.piece * 4u + 16u;
@@ -274,6 +288,8 @@ __global__ void __maxnreg__(168)
       }
     }
     ctrl->tok[row] = tok;
+    // the row's whole K-slice heads for L2 now; the rounds below then gather from L2
+    if (tok >= 0 && KS > P.XR) prefetch_l2_bulk(x + (int64_t)tok * d_in + crank * KS, (uint32_t)KS * 2u);
     if (tok >= 0 && P.prefetch_y) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
   }
   __syncthreads();
@@ -282,8 +298,11 @@ __global__ void __maxnreg__(168)
   __syncwarp();
   cluster_arrive();  // barriers of every CTA initialised and armed (waited on before the first remote store)
 
-  // ---- shrink: rounds of XR columns, each gathered, then consumed by XR/16 MMAs
+  // ---- shrink: rounds of XR columns, each gathered, then consumed by XR/16 MMAs.  Rounds
+  // alternate between two x buffers: round rd+1 is in flight while round rd is multiplied.
   const int rounds = KS / P.XR;
+  const int nbuf = rounds > 1 ? 2 : 1;
+  const size_t buf_bytes = (size_t)P.XR * kTileM * 2;
   const uint32_t idesc_shrink = idesc_bf16_f32(kTileM, r, false, true);
   if (warp == 4 && lane == 0) {
     mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
@@ -293,55 +312,67 @@ __global__ void __maxnreg__(168)
   }
   if (TM < kTileM && warp < 4) {
     // MMA rows the tile does not use stay zero in every round
-    for (int i = tid; i < (kTileM - TM) * (P.XR / 8); i += kEpilogueThreads) {
-      const int row = TM + i % (kTileM - TM), cidx = i / (kTileM - TM);
-      *reinterpret_cast<uint4*>(xs + (size_t)(cidx / 8) * kTileM * 128 + sw128_offset(row, cidx % 8)) =
+    for (int i = tid; i < nbuf * (kTileM - TM) * (P.XR / 8); i += kEpilogueThreads) {
+      const int row = TM + i % (kTileM - TM), cidx = (i / (kTileM - TM)) % (P.XR / 8);
+      const int b = i / ((kTileM - TM) * (P.XR / 8));
+      *reinterpret_cast<uint4*>(xs + b * buf_bytes + (size_t)(cidx / 8) * kTileM * 128 + sw128_offset(row, cidx % 8)) =
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
+  auto gather = [&](int rd) {
+    uint8_t* xb = xs + (rd % nbuf) * buf_bytes;
+    const int sub = lane >> 3, chunk = lane & 7;
+    for (int kb = 0; kb < P.XR / kKBlock; ++kb) {
+      const uint32_t blk = smem_u32(xb + (size_t)kb * kTileM * 128);
+      const int col = crank * KS + rd * P.XR + kb * kKBlock + chunk * 8;
+#pragma unroll 4
+      for (int it = 0; it < TM / 16; ++it) {
+        const int row = it * 16 + warp * 4 + sub;
+        const int32_t tok = ctrl->tok[row];
+        const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
+        cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+  if (warp < 4) {
+    gather(0);
+    // validate this row's slot while the gather is in flight
+    const int row = tid;
+    int32_t live = 0;
+    float wt = 0.f;
+    const int32_t tok = ctrl->tok[row];
+    if (tok >= 0) {
+      if (mask_adapter >= 0) {
+        live = 1;
+        wt = ids[tok] == mask_adapter ? 1.f : 0.f;
+      } else if (ids[slot] == a) {
+        live = 1;
+        wt = w ? w[slot] : 1.f;
+      } else if (crank == 0) {
+        report(err_word, MOLORA_DEV_BAD_PERMUTATION);
+      }
+    } else if (row < tile.nvalid && crank == 0) {
+      report(err_word, MOLORA_DEV_BAD_PERMUTATION);
+    }
+    ctrl->live[row] = live;
+    ctrl->wgt[row] = wt;
+  }
   for (int rd = 0; rd < rounds; ++rd) {
     if (warp < 4) {
-      if (rd > 0 && !mbar_wait(&ctrl->bar_x, (rd - 1) & 1)) {  // previous round consumed
-        ctrl->abort = 1;
-        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-      }
-      // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
-      const int sub = lane >> 3, chunk = lane & 7;
-      for (int kb = 0; kb < P.XR / kKBlock; ++kb) {
-        const uint32_t blk = smem_u32(xs + (size_t)kb * kTileM * 128);
-        const int col = crank * KS + rd * P.XR + kb * kKBlock + chunk * 8;
-#pragma unroll 4
-        for (int it = 0; it < TM / 16; ++it) {
-          const int row = it * 16 + warp * 4 + sub;
-          const int32_t tok = ctrl->tok[row];
-          const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
-          cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
+      if (rd + 1 < rounds) {
+        const int nb = (rd + 1) % nbuf;
+        // buffer nb was last read by the MMAs of round rd-1 (its ((rd-1)/2)-th use)
+        if (rd >= 1 && !mbar_wait(&ctrl->bar_x[nb], ((rd - 1) >> 1) & 1)) {
+          ctrl->abort = 1;
+          report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
         }
+        gather(rd + 1);
+        cp_async_wait_group<1>();  // round rd has landed; round rd+1 stays in flight
+      } else {
+        cp_async_wait_all();
       }
-      cp_async_commit();
-      if (rd == 0) {
-        // validate this row's slot while the gather is in flight
-        const int row = tid;
-        int32_t live = 0;
-        float wt = 0.f;
-        const int32_t tok = ctrl->tok[row];
-        if (tok >= 0) {
-          if (mask_adapter >= 0) {
-            live = 1;
-            wt = ids[tok] == mask_adapter ? 1.f : 0.f;
-          } else if (ids[slot] == a) {
-            live = 1;
-            wt = w ? w[slot] : 1.f;
-          } else if (crank == 0) {
-            report(err_word, MOLORA_DEV_BAD_PERMUTATION);
-          }
-        } else if (row < tile.nvalid && crank == 0) {
-          report(err_word, MOLORA_DEV_BAD_PERMUTATION);
-        }
-        ctrl->live[row] = live;
-        ctrl->wgt[row] = wt;
-      }
-      cp_async_wait_all();
       fence_proxy_async_smem();
     }
     __syncwarp();
@@ -350,28 +381,32 @@ __global__ void __maxnreg__(168)
       bool ok = !ctrl->abort;
       if (ok && rd == 0) ok = mbar_wait(&ctrl->bar_a, 0);
       tc_fence_after();
+      uint64_t* done = &ctrl->bar_x[rd % nbuf];
       if (ok) {
         const uint32_t atom = 8u * r * 2u;
         const SmemLayout swz = sw_for_rank(r);
+        const uint8_t* xb = xs + (rd % nbuf) * buf_bytes;
         for (int kb = 0; kb < P.XR / kKBlock; ++kb)
           for (int ks = 0; ks < kKBlock / 16; ++ks) {
             const int krow = rd * P.XR + kb * kKBlock + ks * 16;
-            const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
+            const uint64_t da = smem_desc(smem_u32(xb + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
             const uint64_t db = smem_desc(smem_u32(as + (size_t)krow * r * 2), atom, atom, swz);
             umma_f16(tmem, da, db, idesc_shrink, (rd | kb | ks) != 0);
           }
-        umma_commit(&ctrl->bar_x);
+        umma_commit(done);
       } else {
         ctrl->abort = 1;
         report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-        mbar_arrive(&ctrl->bar_x);
+        mbar_arrive(done);
       }
     }
   }
-  const uint32_t last_parity = (uint32_t)(rounds - 1) & 1u;
+  // the last round's commit covers every shrink MMA issued before it
+  uint64_t* const last_bar = &ctrl->bar_x[(rounds - 1) % nbuf];
+  const uint32_t last_parity = (uint32_t)((rounds - 1) / nbuf) & 1u;
   if (warp == 4 && lane == 0) {
     // B chunk lands in the phase-1 region once the last shrink MMAs have read it
-    if (mbar_wait(&ctrl->bar_x, last_parity)) {
+    if (mbar_wait(last_bar, last_parity)) {
       mbar_arrive_expect_tx(&ctrl->bar_b, (uint32_t)NC * r * 2);
       for (int q = 0; q < NC / 64; ++q)
         tma_load_2d(smem_u32(bs + (size_t)q * r * 128), &map_b, crank * NC + q * 64, a * r, &ctrl->bar_b);
@@ -390,7 +425,7 @@ __global__ void __maxnreg__(168)
   float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [C sources][RPC rows][r]
   bool have_h = true;
   if (warp < 4) {
-    have_h = mbar_wait(&ctrl->bar_x, last_parity);
+    have_h = mbar_wait(last_bar, last_parity);
     tc_fence_after();
     if (!have_h) {
       ctrl->abort = 1;
@@ -447,7 +482,7 @@ __global__ void __maxnreg__(168)
         hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
         lo[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
       }
-      const uint32_t off = sw128_offset(trow, c0 / 8);
+      const uint32_t off = swz_offset(trow, c0 / 8, g_row_bytes);
       const uint4 vh = make_uint4(hi[0], hi[1], hi[2], hi[3]), vl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       for (int d = 0; d < C; ++d) {
         const uint32_t bar_d = dsmem_addr(smem_u32(&ctrl->bar_g), (uint32_t)d);
@@ -480,8 +515,9 @@ __global__ void __maxnreg__(168)
         for (int ks = 0; ks < r / 16; ++ks) {
           const uint64_t db = smem_desc(smem_u32(bs + (size_t)(p * (P.PW / 64)) * r * 128 + ks * 2048), r * 128,
                                         1024, kSwizzle128B);
-          umma_f16(d, smem_desc(smem_u32(g_hi + ks * 32), 16, 1024, kSwizzle128B), db, idesc, ks != 0);
-          umma_f16(d, smem_desc(smem_u32(g_lo + ks * 32), 16, 1024, kSwizzle128B), db, idesc, 1);
+          const SmemLayout gl = sw_for_rank(r);
+          umma_f16(d, smem_desc(smem_u32(g_hi + ks * 32), 16, 8 * g_row_bytes, gl), db, idesc, ks != 0);
+          umma_f16(d, smem_desc(smem_u32(g_lo + ks * 32), 16, 8 * g_row_bytes, gl), db, idesc, 1);
         }
         umma_commit(&ctrl->bar_full[buf]);
       }

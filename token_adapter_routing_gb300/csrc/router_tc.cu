@@ -5,10 +5,13 @@
 // The d_in x 64 projection is the only dense contraction (64 flops per byte of x), so it
 // runs as a tcgen05 GEMM: a cluster of C CTAs owns 128 consecutive tokens and splits d_in;
 // each CTA TMA-loads its x tile (K-major, 128-byte swizzle) and the matching W1 rows
-// (MN-major), accumulates 128 x 64 fp32 partials in TMEM, and the partials are summed
-// through distributed shared memory in a fixed order.  Each CTA then finishes 128/C of the
-// tokens on CUDA cores: ReLU, the 64 x K second layer, top-k selection (strictly greater
-// wins, so equal logits keep the lower index) and the softmax renormalised over the k.
+// (MN-major), and accumulates 128 x 64 fp32 partials in TMEM.  CTA c owns tokens
+// [c*128/C, (c+1)*128/C) of the tile: every CTA pushes those rows' partials to their owner
+// with st.async (counted by the owner's mbarrier), and the owner sums the C partials in rank
+// order (deterministic).  The owner's 128 threads then split each token's 64 hidden units
+// into 8 groups: ReLU, partial logits over the group's 8 units, and a fixed-order sum of the
+// 8 group partials; one thread per token selects the top k (strictly greater wins, so equal
+// logits keep the lower index) and renormalises the softmax over the k.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -23,41 +26,54 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kKBlock = 64;
 constexpr int kThreads = 160;
+constexpr int kGroups = 8;  // hidden units per token split into 8 groups of 8
 constexpr uint32_t kTmemCols = 64;
-constexpr uint32_t kPStride = kRouterHidden * 4 + 16;
 constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kTwoPerSm = 113 * 1024;
 
 struct RouterShape {
-  int C, KS;
-  size_t off_w1, off_w2, region, smem;
+  int C, KS, XR;  // XR: x columns loaded per round (the x and W1 buffers are reused per round)
+  size_t off_w1, off_recv, off_w2, region, smem;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool plan(int32_t d_in, int32_t K, int C, RouterShape* s) {
+bool plan(int32_t d_in, int32_t K, int C, size_t budget, RouterShape* s) {
   if (d_in % (C * kKBlock) || kTileM % C) return false;
   s->C = C;
   s->KS = d_in / C;
-  s->off_w1 = (size_t)s->KS * kTileM * 2;
-  const size_t phase1 = s->off_w1 + (size_t)s->KS * kRouterHidden * 2;
-  const size_t phase2 = (size_t)kTileM * kPStride;
-  s->off_w2 = align_up(phase1 > phase2 ? phase1 : phase2, 1024);
-  // W2 as fp32 [64 x K], b1 [64], b2 [K], per-row logits [128/C x K]
-  s->region = s->off_w2 + sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + K + (kTileM / C) * K);
-  s->region = align_up(s->region, 1024);
-  s->smem = s->region + 1024 + 256;
-  return s->smem <= kMaxSmem;
+  for (int XR = s->KS > 512 ? 512 : s->KS; XR >= kKBlock; XR -= kKBlock) {
+    if (s->KS % XR) continue;
+    s->XR = XR;
+    s->off_w1 = (size_t)XR * kTileM * 2;
+    const size_t phase1 = s->off_w1 + (size_t)XR * kRouterHidden * 2;
+    // partial logits of the owner's rows reuse the phase-1 space (x and W1 are consumed by then)
+    const size_t plog = (size_t)(kTileM / C) * kGroups * K * 4;
+    // receive slots: other CTAs may push while this CTA's tensor core still reads x
+    s->off_recv = align_up(phase1 > plog ? phase1 : plog, 1024);
+    s->off_w2 = s->off_recv + (size_t)kTileM * kRouterHidden * 4;
+    // W2 as fp32 [64 x K], b1 [64], b2 [K]
+    s->region = align_up(s->off_w2 + sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + K), 1024);
+    s->smem = s->region + 1024 + 256;
+    if (s->smem <= budget) return true;
+  }
+  return false;
 }
 
+// Clusters of 8 first; the widest x round that still fits two CTAs per SM (so a cluster's
+// rounds overlap another CTA's), else one CTA per SM.
 bool choose(int32_t d_in, int32_t K, RouterShape* s) {
-  for (int C : {8, 4, 2, 1})
-    if (plan(d_in, K, C, s)) return true;
+  for (size_t budget : {kTwoPerSm, kMaxSmem})
+    for (int C : {8, 4, 2, 1})
+      if (plan(d_in, K, C, budget, s)) return true;
   return false;
 }
 
 struct __align__(8) RCtrl {
-  uint64_t bar_load;
-  uint64_t bar_mma;
+  uint64_t bar_load;   // TMA of one round (one phase per round)
+  uint64_t bar_round;  // MMAs of one round done (one phase per round; waited only by the producer)
+  uint64_t bar_mma;    // all MMAs done (one phase)
+  uint64_t bar_recv;
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -67,34 +83,40 @@ struct __align__(8) RCtrl {
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(int64_t N, int32_t d_in, const __nv_bfloat16* __restrict__ W2, const float* __restrict__ b1,
                      const float* __restrict__ b2, int32_t K, int32_t k, float* __restrict__ logits,
-                     int32_t* __restrict__ ids, float* __restrict__ w, int32_t C, int32_t KS, uint32_t off_w1,
-                     uint32_t off_w2, uint32_t region, const __grid_constant__ CUtensorMap map_x,
+                     int32_t* __restrict__ ids, float* __restrict__ w, int32_t C, int32_t KS, int32_t XR,
+                     uint32_t off_w1,
+                     uint32_t off_recv, uint32_t off_w2, uint32_t region, const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_w1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   RCtrl* ctrl = reinterpret_cast<RCtrl*>(sm + region);
   uint8_t* xs = sm;
   uint8_t* w1s = sm + off_w1;
-  uint8_t* ps = sm;  // partial hidden, after the MMA has consumed x
+  float* plog = reinterpret_cast<float*>(sm);  // [RPC rows][8 groups][K], after the MMA
+  float* recv = reinterpret_cast<float*>(sm + off_recv);  // [C sources][RPC rows][64]
   float* w2s = reinterpret_cast<float*>(sm + off_w2);
   float* b1s = w2s + kRouterHidden * K;
   float* b2s = b1s + kRouterHidden;
-  float* lgs = b2s + K;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int crank = (int)cluster_ctarank();
   const int64_t tile = blockIdx.x / C;
   const int64_t t0 = tile * kTileM;
-  const int nkb = KS / kKBlock;
+  const int nkb = XR / kKBlock;  // K-blocks per round
+  const int rounds = KS / XR;
+  const int RPC = kTileM / C;
 
   if (warp == 4) {
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
     if (lane == 0) {
       mbar_init(&ctrl->bar_load, 1);
+      mbar_init(&ctrl->bar_round, 1);
       mbar_init(&ctrl->bar_mma, 1);
+      mbar_init(&ctrl->bar_recv, 1);
       ctrl->abort = 0;
       mbar_fence_init();
+      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)kTileM * kRouterHidden * 4u);
       tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_w1);
     }
@@ -109,104 +131,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  __syncwarp();
+  cluster_arrive();  // every CTA's receive barrier is initialised and armed
 
   if (warp == 4 && lane == 0) {
-    mbar_arrive_expect_tx(&ctrl->bar_load, (uint32_t)KS * (kTileM + kRouterHidden) * 2);
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int32_t col = crank * KS + kb * kKBlock;
-      tma_load_2d(smem_u32(xs + (size_t)kb * kTileM * 128), &map_x, col, (int32_t)t0, &ctrl->bar_load);
-      tma_load_2d(smem_u32(w1s + (size_t)kb * kKBlock * 128), &map_w1, 0, col, &ctrl->bar_load);
-    }
-    const bool ok = mbar_wait(&ctrl->bar_load, 0);
-    tc_fence_after();
-    if (ok) {
-      const uint32_t idesc = idesc_bf16_f32(kTileM, kRouterHidden, false, true);
+    bool ok = true;
+    const uint32_t idesc = idesc_bf16_f32(kTileM, kRouterHidden, false, true);
+    for (int rd = 0; rd < rounds && ok; ++rd) {
+      if (rd > 0) ok = mbar_wait(&ctrl->bar_round, (rd - 1) & 1);  // the buffers are free again
+      if (!ok) break;
+      mbar_arrive_expect_tx(&ctrl->bar_load, (uint32_t)XR * (kTileM + kRouterHidden) * 2);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int32_t col = crank * KS + rd * XR + kb * kKBlock;
+        tma_load_2d(smem_u32(xs + (size_t)kb * kTileM * 128), &map_x, col, (int32_t)t0, &ctrl->bar_load);
+        tma_load_2d(smem_u32(w1s + (size_t)kb * kKBlock * 128), &map_w1, 0, col, &ctrl->bar_load);
+      }
+      ok = mbar_wait(&ctrl->bar_load, rd & 1);
+      tc_fence_after();
+      if (!ok) break;
       for (int kb = 0; kb < nkb; ++kb)
         for (int ks = 0; ks < kKBlock / 16; ++ks) {
           const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
           const uint64_t db =
               smem_desc(smem_u32(w1s + (size_t)kb * kKBlock * 128 + ks * 2048), 1024, 1024, kSwizzle128B);
-          umma_f16(tmem, da, db, idesc, (kb | ks) != 0);
+          umma_f16(tmem, da, db, idesc, (rd | kb | ks) != 0);
         }
-      umma_commit(&ctrl->bar_mma);
+      umma_commit(&ctrl->bar_round);
+    }
+    if (ok) {
+      umma_commit(&ctrl->bar_mma);  // covers every MMA issued above
     } else {
       ctrl->abort = 1;
       mbar_arrive(&ctrl->bar_mma);
     }
   }
-  bool timed_out = false;
+  bool have = true;
   if (warp < 4) {
-    const bool ok = mbar_wait(&ctrl->bar_mma, 0);
+    have = mbar_wait(&ctrl->bar_mma, 0) && !ctrl->abort;
     tc_fence_after();
-    if (ok && !ctrl->abort) {
-      float v[16];
-      float* prow = reinterpret_cast<float*>(ps + tid * kPStride);
-      for (int c0 = 0; c0 < kRouterHidden; c0 += 16) {
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(prow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      }
-    } else {
-      timed_out = true;
-    }
-    tc_fence_before();
   }
   __syncwarp();
-  cluster_sync();
-
-  const int rows_per = kTileM / C;
-  if (tid < rows_per) {
-    const int row = crank * rows_per + tid;
-    const int64_t t = t0 + row;
-    if (t < N && !timed_out) {
-      float h[kRouterHidden];
+  cluster_wait();
+  if (warp < 4) {
+    // push this row's 64 partial hidden sums to the row's owner
+    const int row = tid;
+    const uint32_t owner = (uint32_t)(row / RPC);
+    const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * kRouterHidden), owner);
+    const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
+    float v[16];
+    for (int c0 = 0; c0 < kRouterHidden; c0 += 16) {
+      if (have)
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      else
 #pragma unroll
-      for (int j = 0; j < kRouterHidden; ++j) h[j] = 0.f;
-      const uint32_t mine = smem_u32(ps + row * kPStride);
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        st_async_v4(dst + (c0 + 4 * i) * 4,
+                    make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                               __float_as_uint(v[4 * i + 3])),
+                    dst_bar);
+    }
+    tc_fence_before();
+    const bool got = mbar_wait(&ctrl->bar_recv, 0);
+    // owner: hidden unit group (row, g) -> ReLU -> partial logits over the group's 8 units
+    for (int item = tid; item < RPC * kGroups; item += kTileM) {
+      const int rl = item / kGroups, g = item % kGroups;
+      float h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = 0.f;
       for (int cc = 0; cc < C; ++cc) {
-        const uint32_t src = dsmem_addr(mine, (uint32_t)cc);
-#pragma unroll
-        for (int j = 0; j < kRouterHidden; j += 4) {
-          const float4 p = dsmem_ld_f4(src + j * 4);
-          h[j] += p.x, h[j + 1] += p.y, h[j + 2] += p.z, h[j + 3] += p.w;
-        }
+        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * RPC + rl) * kRouterHidden + g * 8);
+        const float4 p0 = src[0], p1 = src[1];
+        h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
+        h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
       }
 #pragma unroll
-      for (int j = 0; j < kRouterHidden; ++j) h[j] = fmaxf(h[j] + b1s[j], 0.f);
-      float* lg = lgs + tid * K;
+      for (int i = 0; i < 8; ++i) h[i] = fmaxf(h[i] + b1s[g * 8 + i], 0.f);
+      float* dstp = plog + ((size_t)rl * kGroups + g) * K;
       for (int a = 0; a < K; ++a) {
         float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < kRouterHidden; ++j) s = fmaf(h[j], w2s[j * K + a], s);
-        s += b2s[a];
-        lg[a] = s;
-        if (logits) logits[t * K + a] = s;
+        for (int i = 0; i < 8; ++i) s = fmaf(h[i], w2s[(g * 8 + i) * K + a], s);
+        dstp[a] = s;
       }
-      uint64_t used = 0;
-      float m = 0.f, denom = 0.f;
-      float e[kMaxAdapters];
-      int sel[kMaxAdapters];
-      for (int js = 0; js < k; ++js) {
-        int best = -1;
-        for (int a = 0; a < K; ++a)
-          if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
-        used |= 1ull << best;
-        if (js == 0) m = lg[best];
-        sel[js] = best;
-        e[js] = expf(lg[best] - m);
-        denom += e[js];
-      }
-      const float inv = 1.f / denom;
-      for (int js = 0; js < k; ++js) {
-        ids[t * k + js] = sel[js];
-        w[t * k + js] = e[js] * inv;
+    }
+    named_barrier(1, kTileM);  // partial logits of the owner's rows are in shared memory
+    if (tid < RPC) {
+      const int rl = tid;
+      const int64_t t = t0 + crank * RPC + rl;
+      if (t < N && got && have) {
+        float* lg = plog + (size_t)rl * kGroups * K;  // group 0's slot collects the sum
+        for (int a = 0; a < K; ++a) {
+          float s = lg[a];
+          for (int g = 1; g < kGroups; ++g) s += lg[g * K + a];
+          s += b2s[a];
+          lg[a] = s;
+          if (logits) logits[t * K + a] = s;
+        }
+        uint64_t used = 0;
+        float m = 0.f, denom = 0.f;
+        for (int js = 0; js < k; ++js) {
+          int best = -1;
+          for (int a = 0; a < K; ++a)
+            if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
+          used |= 1ull << best;
+          if (js == 0) m = lg[best];
+          const float e = expf(lg[best] - m);
+          ids[t * k + js] = best;
+          w[t * k + js] = e;
+          denom += e;
+        }
+        const float inv = 1.f / denom;
+        for (int js = 0; js < k; ++js) w[t * k + js] *= inv;
       }
     }
   }
   __syncwarp();
+  __syncthreads();
   cluster_arrive();
-  cluster_wait();
+  cluster_wait();  // no CTA leaves while another may still write into its shared memory
   if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -225,6 +269,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
   });
   return fn;
 }
@@ -267,7 +313,8 @@ cudaError_t launch_router_tc(const void* x, int64_t N, int32_t d_in, const void*
   const int64_t tiles = (N + kTileM - 1) / kTileM;
   return launch_kernel(router_tc_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C, N, d_in,
                        static_cast<const __nv_bfloat16*>(W2), b1, b2, K, k, logits, ids, w, (int32_t)s.C,
-                       (int32_t)s.KS, (uint32_t)s.off_w1, (uint32_t)s.off_w2, (uint32_t)s.region, map_x, map_w1);
+                       (int32_t)s.KS, (int32_t)s.XR, (uint32_t)s.off_w1, (uint32_t)s.off_recv, (uint32_t)s.off_w2,
+                       (uint32_t)s.region, map_x, map_w1);
 }
 
 }  // namespace molora
