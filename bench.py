@@ -334,16 +334,18 @@ def run_e2e(m, wl, dev, args, world):
 
 
 def load_profiled_traffic(path):
-    """DRAM bytes per apply launch from the committed ncu summary, if it matches this kernel."""
-    fn = os.path.join(ROOT, "profiles", "lora_grouped_kernel_modality4.json")
+    """DRAM bytes (read + write) per apply launch from the committed ncu summary of the
+    grouped kernel on this workload (a line `dram_bytes_per_launch: <int>`), or None."""
+    fn = os.path.join(ROOT, "profiles", "lora_grouped_kernel_modality4.md")
     if path == "scalar" or not os.path.exists(fn):
         return None
     try:
-        with open(fn) as f:
-            d = json.load(f)
-        return d.get("dram_bytes_per_launch")
+        for line in open(fn):
+            if line.strip().startswith("dram_bytes_per_launch:"):
+                return int(line.split(":", 1)[1].strip().split()[0])
     except (OSError, ValueError):
         return None
+    return None
 
 
 # --------------------------------------------------------------------------- CPU oracle

@@ -196,6 +196,14 @@ MOLORA_API molora_status molora_lora_apply_masked_pass(const void* x, molora_dty
 MOLORA_API molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                int32_t K, int32_t r, int32_t k);
 
+/*
+ * molora_selftest_bounded_wait -- checks the bounded on-chip waits every kernel here relies
+ * on: one CTA waits on an mbarrier phase that nothing completes, gives up after `limit_us`
+ * microseconds (1 .. 1e6), ORs MOLORA_DEV_WAIT_TIMEOUT into *err_word (a device int32,
+ * required) and exits normally, leaving the context usable.  Not part of the method.
+ */
+MOLORA_API molora_status molora_selftest_bounded_wait(uint32_t limit_us, int32_t* err_word, cudaStream_t stream);
+
 /* Short text for a status code (static storage). */
 MOLORA_API const char* molora_status_string(molora_status status);
 

@@ -393,3 +393,19 @@ def test_full_size_topk_scaling_sampled(m, k):
     # dispatch over all 8192*k slots stays bit-exact
     rc, ro, rp, _ = oracle.dispatch(ids.cpu(), wl.K)
     assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+
+
+# ------------------------------------------------------------------------- failure handling
+
+def test_bounded_wait_reports_timeout_and_context_survives(m):
+    # a wait that nothing can complete gives up after 2 ms, reports the timeout bit, and the
+    # context stays usable for the next call
+    e = err_word()
+    m.molora_selftest_bounded_wait(e, limit_us=2000)
+    torch.cuda.synchronize()
+    assert int(e.item()) == m.DEV_WAIT_TIMEOUT
+    wl = workloads.make("modality4", N=200, d_in=512, d_out=512)
+    adapter, counts, offsets, perm, y, err = run_vocab_path(m, wl, "grouped")
+    assert err == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    assert_apply_close(y, y_ref)

@@ -24,7 +24,8 @@ from . import build as _build
 
 __all__ = [
     "molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
-    "molora_lora_apply_masked_pass", "molora_select_path", "library_path", "load_library",
+    "molora_lora_apply_masked_pass", "molora_select_path", "molora_selftest_bounded_wait", "library_path",
+    "load_library",
     "MoloraError", "PATHS", "DEV_TOKEN_OUTSIDE_RANGES", "DEV_BAD_RANGES", "DEV_BAD_ADAPTER_ID",
     "DEV_BAD_PERMUTATION", "DEV_WAIT_TIMEOUT", "MAX_ADAPTERS", "ROUTER_HIDDEN",
 ]
@@ -43,7 +44,7 @@ ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path",
-            "molora_status_string", "molora_version")
+            "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
 
 class MoloraError(RuntimeError):
@@ -79,8 +80,10 @@ def load_library():
     lib.molora_status_string.argtypes = [S]
     lib.molora_status_string.restype = ctypes.c_char_p
     lib.molora_version.argtypes = []
+    lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
-                 "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path", "molora_version"):
+                 "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path", "molora_version",
+                 "molora_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -218,6 +221,15 @@ def molora_lora_apply_masked_pass(x, A, B, adapter_of, a, y, scale, err_word=Non
         _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(adapter_of), int(a), float(scale), _p(y),
         _p(err_word), PATHS[path], _stream(stream)))
     return y
+
+
+def molora_selftest_bounded_wait(err_word, limit_us=1000, stream=None):
+    """Runs one CTA whose mbarrier wait can never complete; it must give up after limit_us and
+    set DEV_WAIT_TIMEOUT in err_word (a device int32 tensor)."""
+    _cuda(err_word, "err_word", torch.int32)
+    _check("molora_selftest_bounded_wait", load_library().molora_selftest_bounded_wait(
+        int(limit_us), _p(err_word), _stream(stream)))
+    return err_word
 
 
 def molora_select_path(dtype: torch.dtype, N: int, d_in: int, d_out: int, K: int, r: int, k: int) -> str:

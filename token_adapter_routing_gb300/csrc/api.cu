@@ -151,4 +151,9 @@ const char* molora_status_string(molora_status status) {
 
 int32_t molora_version(void) { return 100; }
 
+molora_status molora_selftest_bounded_wait(uint32_t limit_us, int32_t* err_word, cudaStream_t stream) {
+  if (!err_word || limit_us == 0 || limit_us > 1000000u) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_bounded_wait_selftest((uint64_t)limit_us * 1000ull, err_word, stream));
+}
+
 }  // extern "C"

@@ -48,6 +48,8 @@ cudaError_t launch_router_tc(const void* x, int64_t N, int32_t d_in, const void*
 
 int num_sms();
 
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* err_word, cudaStream_t stream);
+
 // Launches `kernel` with programmatic stream serialization (see pdl_wait in common.cuh) and,
 // when cluster >= 1, an explicit 1-D thread-block cluster of that size.  Kernels that use
 // cluster-scope instructions (mapa, st.async, barrier.cluster) must pass their cluster size,

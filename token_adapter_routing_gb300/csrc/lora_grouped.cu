@@ -51,7 +51,7 @@ constexpr size_t kSmemReservedPerCta = 1024;
 constexpr size_t kMaxSmem = 227 * 1024;
 constexpr size_t kCtrlBytes = 2048;
 constexpr uint32_t kBarX = 1;  // named barrier: x round staged (warps 0-4)
-constexpr int kEpiBulk = 0, kEpiPlain = 1, kEpiRed = 2, kEpiMixed = 3;
+constexpr int kEpiBulk = 0, kEpiPlain = 1, kEpiRed = 2, kEpiMixed = 3, kEpiAlt = 4;
 
 struct GroupedPlan {
   int TM;            // valid rows per tile (64 or 128; the MMA always has M = 128)
@@ -70,6 +70,7 @@ struct GroupedPlan {
   uint32_t region;   // bytes before the control block (1024-aligned)
   int epi;           // epilogue: kEpiBulk, kEpiPlain (k == 1 only), kEpiRed or kEpiMixed
   int prefetch_y;    // prefetch this CTA's y rows into L2 at the start
+  int prefetch_x;    // prefetch this CTA's x K-slices into L2 at the start
   uint32_t smem;     // dynamic shared memory requested
 };
 
@@ -89,6 +90,10 @@ bool plan_one(int32_t d_in, int32_t d_out, int32_t r, int C, int TM, bool two_pe
   // g tiles are K-major with rows of r bf16 and the swizzle that matches that row width
   const size_t g_tile = (size_t)kTileM * r * 2;
   for (int piece : {128, 64}) {
+#ifdef MOLORA_TUNING_ENV
+    if (const char* e = getenv("MOLORA_PIECE"))
+      if (piece != atoi(e)) continue;
+#endif
     s->piece = piece;
     if (plan_layout(r, g_tile, budget, two_per_sm, s)) return true;
   }
@@ -108,7 +113,11 @@ bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, Group
   s->off_g = 0;
   s->off_b = (uint32_t)off_b;
   s->off_s = (uint32_t)off_s;
-  for (int XR = s->KS > 256 ? 256 : s->KS; XR >= kKBlock; XR -= kKBlock) {
+  int max_xr = 256;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_XR")) max_xr = atoi(e);
+#endif
+  for (int XR = s->KS > max_xr ? max_xr : s->KS; XR >= kKBlock; XR -= kKBlock) {
     if (s->KS % XR) continue;
     const int nbuf = s->KS / XR > 1 ? 2 : 1;  // rounds alternate between two x buffers
     const size_t phase1 = (size_t)nbuf * XR * kTileM * 2 + (size_t)s->KS * r * 2;
@@ -289,7 +298,8 @@ __global__ void __maxnreg__(168)
     }
     ctrl->tok[row] = tok;
     // the row's whole K-slice heads for L2 now; the rounds below then gather from L2
-    if (tok >= 0 && KS > P.XR) prefetch_l2_bulk(x + (int64_t)tok * d_in + crank * KS, (uint32_t)KS * 2u);
+    if (tok >= 0 && KS > P.XR && P.prefetch_x)
+      prefetch_l2_bulk(x + (int64_t)tok * d_in + crank * KS, (uint32_t)KS * 2u);
     if (tok >= 0 && P.prefetch_y) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
   }
   __syncthreads();
@@ -542,7 +552,7 @@ __global__ void __maxnreg__(168)
       if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
       for (int q = 0; ok && !ctrl->abort && q < width; q += P.piece) {
         const int cols = min(P.piece, width - q);
-        if (P.epi == kEpiBulk) bulk_wait_read<0>();  // this row's previous reduction has read the stage
+        if (P.epi != kEpiRed && P.epi != kEpiPlain) bulk_wait_read<0>();  // previous reduction has read the stage
         for (int c0 = 0; c0 < cols; c0 += 32) {
           float v[32];
           tmem_ld32(lane_base + buf * P.PW + q + c0, v);
@@ -551,17 +561,20 @@ __global__ void __maxnreg__(168)
           for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         const int col_base = crank * NC + p * P.PW + q + col4;
-        if (P.epi == kEpiBulk || P.epi == kEpiMixed) {
+        // kEpiAlt (k == 1): even passes go to the TMA unit, odd passes are a plain
+        // read-modify-write by the warps, so both paths to L2 work at once
+        const int epi = P.epi == kEpiAlt ? ((p & 1) ? kEpiPlain : kEpiBulk) : P.epi;
+        if (epi == kEpiBulk || epi == kEpiMixed) {
           // one bulk reduction per row segment, performed by the TMA unit in L2; in the mixed
           // mode only the even rows go this way and the warp adds the odd rows itself with
           // 16-byte reductions, so the TMA unit and the load/store path work side by side
           fence_proxy_async_smem();
-          if (my_tok >= 0 && (P.epi == kEpiBulk || (row & 1) == 0)) {
+          if (my_tok >= 0 && (epi == kEpiBulk || (row & 1) == 0)) {
             bulk_reduce_add_f32(y + (int64_t)my_tok * d_out + crank * NC + p * P.PW + q, smem_u32(srow),
                                 (uint32_t)cols * 4u);
             bulk_commit();
           }
-          if (P.epi == kEpiMixed) {
+          if (epi == kEpiMixed) {
             __syncwarp();
             for (int j = 1; j < 32; j += 2 * rows_per_step) {
               // rows_per_step rows at a time among the odd ones: j, j+2, ...
@@ -574,7 +587,7 @@ __global__ void __maxnreg__(168)
             }
             __syncwarp();
           }
-        } else if (P.epi == kEpiPlain) {
+        } else if (epi == kEpiPlain) {
           // k == 1: this tile row is the only writer of its y row segment, so a plain
           // read-modify-write (one fp32 add per element, as the reduction would do); eight
           // loads in flight per lane before the adds and stores
@@ -616,7 +629,7 @@ __global__ void __maxnreg__(168)
       tc_fence_before();
       mbar_arrive(&ctrl->bar_empty[buf]);
     }
-    if (P.epi == kEpiBulk) bulk_wait_all();
+    if (P.epi != kEpiRed && P.epi != kEpiPlain) bulk_wait_all();
   }
   __syncthreads();
   cluster_arrive();
@@ -678,10 +691,12 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
     return cudaErrorNotSupported;
   s.epi = kEpiBulk;
   s.prefetch_y = 0;
+  s.prefetch_x = 0;  // measured: gathering straight from DRAM is slightly faster here
 #ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_PREFETCH_X")) s.prefetch_x = atoi(e);
   if (const char* e = getenv("MOLORA_EPI")) s.epi = atoi(e);
   if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
-  if (s.epi == kEpiPlain && k != 1) s.epi = kEpiRed;
+  if ((s.epi == kEpiPlain || s.epi == kEpiAlt) && k != 1) s.epi = kEpiBulk;
 #endif
   CUtensorMap map_a, map_b;
   const CUtensorMapSwizzle swa =

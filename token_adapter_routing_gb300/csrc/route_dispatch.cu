@@ -147,4 +147,22 @@ cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K,
                        counts, offsets, perm, err_word);
 }
 
+// ---------------------------------------------------------------------------------------
+// Self-test of the bounded waits every kernel uses: one CTA waits on an mbarrier whose phase
+// nothing completes (armed for one arrival that never comes), gives up after `limit_ns`,
+// reports MOLORA_DEV_WAIT_TIMEOUT and returns normally.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int32_t* err_word) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+}
+
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* err_word, cudaStream_t stream) {
+  return launch_kernel(bounded_wait_selftest_kernel, dim3(1), dim3(32), 0, stream, 0, limit_ns, err_word);
+}
+
 }  // namespace molora
