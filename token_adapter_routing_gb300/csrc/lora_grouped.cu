@@ -136,11 +136,13 @@ bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, Group
   return false;
 }
 
-// Picks cluster size, tile rows and CTAs per SM.  Clusters of 8 with two CTAs per SM are
-// preferred (they fit a whole small batch in one wave); shapes that do not fit fall back to
-// one CTA per SM, then to smaller clusters.
+// Picks cluster size, tile rows and CTAs per SM.  Clusters of 8 with two CTAs per SM come
+// first.  A launch covers at most ceil(S/TM) + K tiles; when 64-row tiles still fit one wave
+// at two CTAs per SM, they win: twice as many half-size CTAs spread over all SMs instead of
+// leaving a few SMs with two full tiles (clusters of 8 reach only ~130 distinct SMs at one
+// CTA each), which halves the tail of the y update.  Larger batches keep 128-row tiles.
+// Shapes that fit neither fall back to one CTA per SM, then to smaller clusters.
 bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, GroupedPlan* s) {
-  (void)S, (void)K;
   int only_c = 0, only_one = 0, only_tm = 0;
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_CLUSTER")) only_c = atoi(e);
@@ -148,13 +150,19 @@ bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, Groupe
   if (const char* e = getenv("MOLORA_TILE_ROWS")) only_tm = atoi(e);
 #endif
   struct Cand { int C, TM; bool two; };
+  const bool small = ((S + 63) / 64 + K) * 8 <= 2 * (int64_t)num_sms();
+  static const Cand small_first[] = {{8, 64, true}};
   static const Cand order[] = {{8, 128, true}, {8, 128, false}, {4, 128, true}, {4, 128, false},
                                {2, 128, true}, {2, 128, false}, {1, 128, true}, {1, 128, false},
-                               {4, 64, false}, {8, 64, true}};
-  for (const Cand& c : order) {
-    if ((only_c && c.C != only_c) || (only_one && c.two) || (only_tm && c.TM != only_tm)) continue;
-    if (plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
-  }
+                               {8, 64, true}, {4, 64, true}, {4, 64, false}};
+  auto allowed = [&](const Cand& c) {
+    return !((only_c && c.C != only_c) || (only_one && c.two) || (only_tm && c.TM != only_tm));
+  };
+  if (small)
+    for (const Cand& c : small_first)
+      if (allowed(c) && plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
+  for (const Cand& c : order)
+    if (allowed(c) && plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
   return false;
 }
 
