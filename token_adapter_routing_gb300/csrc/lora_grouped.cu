@@ -120,13 +120,18 @@ bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, Group
   for (int XR = s->KS > max_xr ? max_xr : s->KS; XR >= kKBlock; XR -= kKBlock) {
     if (s->KS % XR) continue;
     const int nbuf = s->KS / XR > 1 ? 2 : 1;  // rounds alternate between two x buffers
-    const size_t phase1 = (size_t)nbuf * XR * kTileM * 2 + (size_t)s->KS * r * 2;
+    // x buffers hold TM rows; the M = 128 MMA over a 64-row buffer also reads the next 64 rows'
+    // worth of shared memory (finite, unused), so at least 8 KB of this region follows the ring
+    const size_t ring = (size_t)nbuf * XR * s->TM * 2;
+    const size_t a_bytes = (size_t)s->KS * r * 2;
+    const size_t over = s->TM < kTileM ? (size_t)(kTileM - s->TM) * 128 : 0;
+    const size_t phase1 = ring + (a_bytes > over ? a_bytes : over);
     const size_t shared_region = align_up(phase1 > phase2 ? phase1 : phase2, 1024);
     size_t smem = shared_region + recv + 1024 /* base alignment slack */ + kCtrlBytes;
     if (!two_per_sm && smem < kSmemPerSm / 2) smem = kSmemPerSm / 2;  // keep it at one CTA per SM
     if (smem <= budget) {
       s->XR = XR;
-      s->off_a = (uint32_t)((size_t)nbuf * XR * kTileM * 2);
+      s->off_a = (uint32_t)ring;
       s->off_recv = (uint32_t)shared_region;
       s->region = (uint32_t)(shared_region + recv);
       s->smem = (uint32_t)smem;
@@ -283,7 +288,7 @@ __global__ void __maxnreg__(168)
   }
   const int a = tile.adapter;
 
-  uint8_t* xs = sm;              // phase 1: two x round buffers, XR/64 blocks of [128 rows x 128 B], 128B swizzle
+  uint8_t* xs = sm;              // phase 1: two x round buffers, XR/64 blocks of [TM rows x 128 B], 128B swizzle
   uint8_t* as = sm + P.off_a;    // phase 1: A slice [KS x r], MN-major, swizzled by TMA
   uint8_t* g_hi = sm + P.off_g;  // phase 2: g as two bf16 K-major tiles, rows of r elements
   uint8_t* g_lo = g_hi + (size_t)kTileM * r * 2;
@@ -320,7 +325,8 @@ __global__ void __maxnreg__(168)
   // alternate between two x buffers: round rd+1 is in flight while round rd is multiplied.
   const int rounds = KS / P.XR;
   const int nbuf = rounds > 1 ? 2 : 1;
-  const size_t buf_bytes = (size_t)P.XR * kTileM * 2;
+  const size_t blk_bytes = (size_t)TM * 128;          // one 64-column K-block of a buffer
+  const size_t buf_bytes = (size_t)(P.XR / kKBlock) * blk_bytes;
   const uint32_t idesc_shrink = idesc_bf16_f32(kTileM, r, false, true);
   if (warp == 4 && lane == 0) {
     mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
@@ -328,21 +334,12 @@ __global__ void __maxnreg__(168)
       tma_load_2d(smem_u32(as + (size_t)kb * kKBlock * r * 2), &map_a, 0, a * d_in + crank * KS + kb * kKBlock,
                   &ctrl->bar_a);
   }
-  if (TM < kTileM && warp < 4) {
-    // MMA rows the tile does not use stay zero in every round
-    for (int i = tid; i < nbuf * (kTileM - TM) * (P.XR / 8); i += kEpilogueThreads) {
-      const int row = TM + i % (kTileM - TM), cidx = (i / (kTileM - TM)) % (P.XR / 8);
-      const int b = i / ((kTileM - TM) * (P.XR / 8));
-      *reinterpret_cast<uint4*>(xs + b * buf_bytes + (size_t)(cidx / 8) * kTileM * 128 + sw128_offset(row, cidx % 8)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
   // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
   auto gather = [&](int rd) {
     uint8_t* xb = xs + (rd % nbuf) * buf_bytes;
     const int sub = lane >> 3, chunk = lane & 7;
     for (int kb = 0; kb < P.XR / kKBlock; ++kb) {
-      const uint32_t blk = smem_u32(xb + (size_t)kb * kTileM * 128);
+      const uint32_t blk = smem_u32(xb + (size_t)kb * blk_bytes);
       const int col = crank * KS + rd * P.XR + kb * kKBlock + chunk * 8;
 #pragma unroll 4
       for (int it = 0; it < TM / 16; ++it) {
@@ -407,7 +404,8 @@ __global__ void __maxnreg__(168)
         for (int kb = 0; kb < P.XR / kKBlock; ++kb)
           for (int ks = 0; ks < kKBlock / 16; ++ks) {
             const int krow = rd * P.XR + kb * kKBlock + ks * 16;
-            const uint64_t da = smem_desc(smem_u32(xb + (size_t)kb * kTileM * 128 + ks * 32), 16, 1024, kSwizzle128B);
+            // 128 MMA rows from here: the tile's TM rows, then (TM = 64) 64 unused rows
+            const uint64_t da = smem_desc(smem_u32(xb + (size_t)kb * blk_bytes + ks * 32), 16, 1024, kSwizzle128B);
             const uint64_t db = smem_desc(smem_u32(as + (size_t)krow * r * 2), atom, atom, swz);
             umma_f16(tmem, da, db, idesc_shrink, (rd | kb | ks) != 0);
           }
@@ -459,7 +457,7 @@ __global__ void __maxnreg__(168)
     const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
     float v[16];
     for (int c0 = 0; c0 < r; c0 += 16) {
-      if (have_h)
+      if (have_h && warp * 32 < TM)  // rows past the tile hold unused MMA rows: send zeros
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
       else
 #pragma unroll
