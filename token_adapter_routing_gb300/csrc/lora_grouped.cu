@@ -313,7 +313,7 @@ __global__ void __maxnreg__(168)
     // the row's whole K-slice heads for L2 now; the rounds below then gather from L2
     if (tok >= 0 && KS > P.XR && P.prefetch_x)
       prefetch_l2_bulk(x + (int64_t)tok * d_in + crank * KS, (uint32_t)KS * 2u);
-    if (tok >= 0 && P.prefetch_y) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
+    if (tok >= 0 && P.prefetch_y == 1) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
   }
   __syncthreads();
   tc_fence_after();
@@ -384,6 +384,8 @@ __global__ void __maxnreg__(168)
           report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
         }
         gather(rd + 1);
+        if (rd + 2 == rounds && P.prefetch_y == 2 && ctrl->tok[tid] >= 0)
+          prefetch_l2_bulk(y + (int64_t)ctrl->tok[tid] * d_out + crank * NC, (uint32_t)NC * 4u);
         cp_async_wait_group<1>();  // round rd has landed; round rd+1 stays in flight
       } else {
         cp_async_wait_all();
@@ -441,6 +443,8 @@ __global__ void __maxnreg__(168)
   float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [C sources][RPC rows][r]
   bool have_h = true;
   if (warp < 4) {
+    if (P.prefetch_y == 3 && ctrl->tok[tid] >= 0)
+      prefetch_l2_bulk(y + (int64_t)ctrl->tok[tid] * d_out + crank * NC, (uint32_t)NC * 4u);
     have_h = mbar_wait(last_bar, last_parity);
     tc_fence_after();
     if (!have_h) {
