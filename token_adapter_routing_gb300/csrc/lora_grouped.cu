@@ -51,7 +51,6 @@ constexpr size_t kSmemReservedPerCta = 1024;
 constexpr size_t kMaxSmem = 227 * 1024;
 constexpr size_t kCtrlBytes = 2048;
 constexpr uint32_t kBarX = 1;  // named barrier: x round staged (warps 0-4)
-constexpr int kEpiBulk = 0, kEpiPlain = 1, kEpiRed = 2, kEpiMixed = 3, kEpiAlt = 4;
 
 struct GroupedPlan {
   int TM;            // valid rows per tile (64 or 128; the MMA always has M = 128)
@@ -68,9 +67,7 @@ struct GroupedPlan {
   uint32_t off_s;    // phase 2: epilogue staging
   uint32_t off_recv; // receive slots for partial h, [C sources][128/C rows][r] fp32
   uint32_t region;   // bytes before the control block (1024-aligned)
-  int epi;           // epilogue: kEpiBulk, kEpiPlain (k == 1 only), kEpiRed or kEpiMixed
-  int prefetch_y;    // prefetch this CTA's y rows into L2 at the start
-  int prefetch_x;    // prefetch this CTA's x K-slices into L2 at the start
+  int prefetch_y;    // send this CTA's y row segments to L2 once its x gather has landed
   uint32_t smem;     // dynamic shared memory requested
 };
 
@@ -310,10 +307,6 @@ __global__ void __maxnreg__(168)
       }
     }
     ctrl->tok[row] = tok;
-    // the row's whole K-slice heads for L2 now; the rounds below then gather from L2
-    if (tok >= 0 && KS > P.XR && P.prefetch_x)
-      prefetch_l2_bulk(x + (int64_t)tok * d_in + crank * KS, (uint32_t)KS * 2u);
-    if (tok >= 0 && P.prefetch_y == 1) prefetch_l2_bulk(y + (int64_t)tok * d_out + crank * NC, (uint32_t)NC * 4u);
   }
   __syncthreads();
   tc_fence_after();
@@ -384,8 +377,6 @@ __global__ void __maxnreg__(168)
           report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
         }
         gather(rd + 1);
-        if (rd + 2 == rounds && P.prefetch_y == 2 && ctrl->tok[tid] >= 0)
-          prefetch_l2_bulk(y + (int64_t)ctrl->tok[tid] * d_out + crank * NC, (uint32_t)NC * 4u);
         cp_async_wait_group<1>();  // round rd has landed; round rd+1 stays in flight
       } else {
         cp_async_wait_all();
@@ -443,7 +434,10 @@ __global__ void __maxnreg__(168)
   float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [C sources][RPC rows][r]
   bool have_h = true;
   if (warp < 4) {
-    if (P.prefetch_y == 3 && ctrl->tok[tid] >= 0)
+    // x has landed and only the last shrink MMAs are running: start pulling this row's y
+    // segment into L2, so the reductions of the expand find it there.  Earlier, the prefetch
+    // competed with the x gather and slowed it more than it helped.
+    if (P.prefetch_y && ctrl->tok[tid] >= 0)
       prefetch_l2_bulk(y + (int64_t)ctrl->tok[tid] * d_out + crank * NC, (uint32_t)NC * 4u);
     have_h = mbar_wait(last_bar, last_parity);
     tc_fence_after();
@@ -544,15 +538,11 @@ __global__ void __maxnreg__(168)
     }
     __syncwarp();
   } else {
-    // Each thread drains its own TMEM lane (tile row) into the staging rows; then the warp
-    // walks its 32 rows and adds each row segment into y with coalesced 16-byte L2
-    // reductions (lanes cover consecutive columns of one row).
+    // Each thread drains its own TMEM lane (tile row) into its staging row, then hands the
+    // row segment to the TMA unit as one bulk fp32 add into y.
     const int row = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float* srow = reinterpret_cast<float*>(stage + row * stage_stride);
-    const int lanes_per_row = P.piece / 4;           // 16 or 32
-    const int rows_per_step = 32 / lanes_per_row;    // 2 or 1
-    const int sub_row = lane / lanes_per_row, col4 = (lane % lanes_per_row) * 4;
     const int32_t my_tok = ctrl->live[row] ? ctrl->tok[row] : -1;
     for (int p = 0; p < npass; ++p) {
       const int buf = p & 1;
@@ -562,7 +552,7 @@ __global__ void __maxnreg__(168)
       if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
       for (int q = 0; ok && !ctrl->abort && q < width; q += P.piece) {
         const int cols = min(P.piece, width - q);
-        if (P.epi != kEpiRed && P.epi != kEpiPlain) bulk_wait_read<0>();  // previous reduction has read the stage
+        bulk_wait_read<0>();  // the previous reduction has read the stage
         for (int c0 = 0; c0 < cols; c0 += 32) {
           float v[32];
           tmem_ld32(lane_base + buf * P.PW + q + c0, v);
@@ -570,76 +560,18 @@ __global__ void __maxnreg__(168)
 #pragma unroll
           for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
-        const int col_base = crank * NC + p * P.PW + q + col4;
-        // kEpiAlt (k == 1): even passes go to the TMA unit, odd passes are a plain
-        // read-modify-write by the warps, so both paths to L2 work at once
-        const int epi = P.epi == kEpiAlt ? ((p & 1) ? kEpiPlain : kEpiBulk) : P.epi;
-        if (epi == kEpiBulk || epi == kEpiMixed) {
-          // one bulk reduction per row segment, performed by the TMA unit in L2; in the mixed
-          // mode only the even rows go this way and the warp adds the odd rows itself with
-          // 16-byte reductions, so the TMA unit and the load/store path work side by side
-          fence_proxy_async_smem();
-          if (my_tok >= 0 && (epi == kEpiBulk || (row & 1) == 0)) {
-            bulk_reduce_add_f32(y + (int64_t)my_tok * d_out + crank * NC + p * P.PW + q, smem_u32(srow),
-                                (uint32_t)cols * 4u);
-            bulk_commit();
-          }
-          if (epi == kEpiMixed) {
-            __syncwarp();
-            for (int j = 1; j < 32; j += 2 * rows_per_step) {
-              // rows_per_step rows at a time among the odd ones: j, j+2, ...
-              const int rr = warp * 32 + j + 2 * sub_row;
-              const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
-              if (tok >= 0 && col4 < cols) {
-                const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
-                red_add_v4(y + (int64_t)tok * d_out + col_base, d);
-              }
-            }
-            __syncwarp();
-          }
-        } else if (epi == kEpiPlain) {
-          // k == 1: this tile row is the only writer of its y row segment, so a plain
-          // read-modify-write (one fp32 add per element, as the reduction would do); eight
-          // loads in flight per lane before the adds and stores
-          __syncwarp();
-          for (int j0 = 0; j0 < 32; j0 += rows_per_step * 8) {
-            float4 yv[8];
-            float* yp[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int rr = warp * 32 + j0 + u * rows_per_step + sub_row;
-              const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
-              yp[u] = (tok >= 0 && col4 < cols) ? y + (int64_t)tok * d_out + col_base : nullptr;
-              if (yp[u]) yv[u] = *reinterpret_cast<const float4*>(yp[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              if (!yp[u]) continue;
-              const int rr = warp * 32 + j0 + u * rows_per_step + sub_row;
-              const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
-              yv[u].x += d.x, yv[u].y += d.y, yv[u].z += d.z, yv[u].w += d.w;
-              *reinterpret_cast<float4*>(yp[u]) = yv[u];
-            }
-          }
-          __syncwarp();
-        } else {
-          // coalesced 16-byte L2 reductions, lanes over consecutive columns of one row
-          __syncwarp();
-          for (int j = 0; j < 32; j += rows_per_step) {
-            const int rr = warp * 32 + j + sub_row;
-            const int32_t tok = ctrl->live[rr] ? ctrl->tok[rr] : -1;
-            if (tok >= 0 && col4 < cols) {
-              const float4 d = *reinterpret_cast<const float4*>(stage + rr * stage_stride + (size_t)col4 * 4);
-              red_add_v4(y + (int64_t)tok * d_out + col_base, d);
-            }
-          }
-          __syncwarp();
+        // one bulk reduction per row segment, performed by the TMA unit in L2
+        fence_proxy_async_smem();
+        if (my_tok >= 0) {
+          bulk_reduce_add_f32(y + (int64_t)my_tok * d_out + crank * NC + p * P.PW + q, smem_u32(srow),
+                              (uint32_t)cols * 4u);
+          bulk_commit();
         }
       }
       tc_fence_before();
       mbar_arrive(&ctrl->bar_empty[buf]);
     }
-    if (P.epi != kEpiRed && P.epi != kEpiPlain) bulk_wait_all();
+    bulk_wait_all();
   }
   __syncthreads();
   cluster_arrive();
@@ -699,14 +631,9 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   GroupedPlan s;
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
     return cudaErrorNotSupported;
-  s.epi = kEpiBulk;
-  s.prefetch_y = 0;
-  s.prefetch_x = 0;  // measured: gathering straight from DRAM is slightly faster here
+  s.prefetch_y = 1;
 #ifdef MOLORA_TUNING_ENV
-  if (const char* e = getenv("MOLORA_PREFETCH_X")) s.prefetch_x = atoi(e);
-  if (const char* e = getenv("MOLORA_EPI")) s.epi = atoi(e);
   if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
-  if ((s.epi == kEpiPlain || s.epi == kEpiAlt) && k != 1) s.epi = kEpiBulk;
 #endif
   CUtensorMap map_a, map_b;
   const CUtensorMapSwizzle swa =
