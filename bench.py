@@ -5,8 +5,8 @@ Per-Token Adapter Routing" (Table 3: K = 4 modalities, 2048 tokens, d = 4096), w
 bf16 x / A / B, fp32 y updated in place, tokens in runs of geometric length (mean 64) with one
 uniformly drawn modality (vocabulary range) per run; synthetic, seeded.
 
-One step = the whole path over one batch: vocabulary routing -> dispatch (histogram, scan,
-permutation) -> grouped LoRA apply.  The timed steps are captured back to back as one CUDA
+One step = the whole path over one batch: vocabulary routing and dispatch (histogram, scan,
+permutation; one kernel) -> grouped LoRA apply.  The timed steps are captured back to back as one CUDA
 graph (consecutive kernels overlap their prologues through programmatic dependent launch)
 between one pair of CUDA events.  The steps cycle through six resident batches of about
 50 MB each, so a batch's x and y have been evicted from the 129 MB L2 by the time the batch
@@ -202,8 +202,8 @@ def run_ours(args, rank, world, local):
 
     def step(i):
         b = batches[i % N_BATCHES]
-        m.molora_route_vocab(b["tok"], starts, adapter=b["adapter"], err_word=err)
-        m.molora_dispatch(b["adapter"], wl.K, counts=b["counts"], offsets=b["offsets"], perm=b["perm"], err_word=err)
+        m.molora_route_vocab_dispatch(b["tok"], starts, adapter=b["adapter"], counts=b["counts"],
+                                      offsets=b["offsets"], perm=b["perm"], err_word=err)
         apply(i)
 
     def apply(i):
@@ -226,7 +226,7 @@ def run_ours(args, rank, world, local):
         g_warm, g_steps, g_applies = capture(step, warm), capture(step, args.steps), capture(apply, args.steps)
         g_one = capture(step, 1)
     n_active = [int((torch.bincount(b["adapter"].cpu().long(), minlength=wl.K) > 0).sum().item()) for b in batches]
-    launches_per_step = 3  # route_vocab, dispatch, apply
+    launches_per_step = 2  # route_vocab + dispatch (one kernel), apply
 
     def timed_block(g):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -298,7 +298,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": "4-modality kernel benchmark: N=2048 tokens, d_in=d_out=4096, K=4, r=16, "
                                "bf16 x/A/B, fp32 y, vocabulary routing, geometric runs (mean 64)",
                    "global_batch": wl.N * world, "tokens_per_rank": wl.N, "path": args.path,
-                   "step": "route_vocab -> dispatch -> lora_apply, one CUDA graph (PDL between kernels)",
+                   "step": "route_vocab_dispatch (vocabulary routing, histogram, scan, permutation in one "
+                           "kernel) -> lora_apply",
                    "l2": (f"inputs larger than L2: the steps cycle through {N_BATCHES} resident batches "
                           f"(x, y, indices: {batch_mb:.0f} MB each), so a batch's data is evicted before it "
                           "comes round again"),
@@ -343,8 +344,7 @@ def run_e2e(m, wl, dev, args, world):
         tok.copy_(tok_h, non_blocking=True)
         x.copy_(x_h, non_blocking=True)
         y.copy_(y0_h, non_blocking=True)
-        m.molora_route_vocab(tok, starts, adapter=adapter)
-        m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm)
+        m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
         m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
                             path=args.path)
         y_h.copy_(y, non_blocking=True)
@@ -472,8 +472,9 @@ def _pct(v, q):
 def run_mode(args):
     """Extra measurements, one JSON line per point:
     crossover  decode sweep (Figures 5 and 9): batch 1..512 x K 4..64 hot-set adapters, d=4096,
-               r=16, top-1, uniform and Zipf(1.1) adapter draws; route -> dispatch -> apply as
-               one CUDA graph on the scalar and on the grouped path, L2 flushed between replays.
+               r=16, top-1, uniform and Zipf(1.1) adapter draws; routing -> apply as one CUDA
+               graph, L2 flushed between replays: route_vocab -> scalar apply, and
+               route_vocab_dispatch -> grouped apply.
     topk       top-k scaling (Table 16): N=8192, d=4096, K=8, r=64, k=1..4, router -> dispatch
                -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
@@ -506,8 +507,13 @@ def run_mode(args):
                     row = {"mode": "crossover", "dist": dist, "K": K, "batch": b}
                     for path in ("scalar", "grouped"):
                         def fn(path=path):
-                            m.molora_route_vocab(tok, starts, adapter=adapter)
-                            m.molora_dispatch(adapter, K, counts=counts, offsets=offsets, perm=perm)
+                            # each path with the routing it needs: the token-major scalar apply
+                            # takes the ids as they are; the grouped apply needs the dispatch
+                            if path == "scalar":
+                                m.molora_route_vocab(tok, starts, adapter=adapter)
+                            else:
+                                m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts,
+                                                              offsets=offsets, perm=perm)
                             m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets,
                                                 perm=perm, path=path)
                         ms = _replay_ms(_graph(fn, stream), stream, 30, flush)
@@ -571,8 +577,7 @@ def run_mode(args):
         perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
 
         def per_token():
-            m.molora_route_vocab(tok, starts, adapter=adapter)
-            m.molora_dispatch(adapter, wl.K, counts=counts, offsets=offsets, perm=perm)
+            m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
             m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
 
         def per_sequence():

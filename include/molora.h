@@ -136,6 +136,21 @@ MOLORA_API molora_status molora_dispatch(const int32_t* ids, int64_t N, int32_t 
                               cudaStream_t stream);
 
 /*
+ * molora_route_vocab_dispatch -- molora_route_vocab followed by molora_dispatch with k = 1,
+ * as one kernel (Table 1: vocabulary routing, then the histogram and pointer arrays both
+ * routing decisions share).  Every output, and every bit set in *err_word, equals what the
+ * two calls in sequence produce:
+ *
+ *   adapter[t] as molora_route_vocab;  counts, offsets, perm as molora_dispatch(adapter, N, 1, K)
+ *
+ * tok int32 [N];  starts int32 [K+1];  adapter int32 [N];  counts int32 [K];
+ * offsets int32 [K+1];  perm int32 [N].  N == 0 writes the empty histogram.
+ */
+MOLORA_API molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t N, const int32_t* starts,
+                                          int32_t K, int32_t* adapter, int32_t* counts, int32_t* offsets,
+                                          int32_t* perm, int32_t* err_word, cudaStream_t stream);
+
+/*
  * molora_lora_apply -- batched per-token LoRA apply over the hot set (Figure 2; Table 10
  * shapes; Figure 4 hot set):
  *

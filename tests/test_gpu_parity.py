@@ -122,6 +122,45 @@ def test_dispatch_all_on_one_adapter(m):
     assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
 
 
+@pytest.mark.parametrize("N,K,outside", [(0, 4, False), (1, 1, False), (2048, 4, False), (513, 7, True),
+                                         (40960, 64, False), (40961, 16, True), (100000, 8, False)])
+def test_route_vocab_dispatch_fused_equals_two_calls(m, N, K, outside):
+    """The fused kernel gives the oracle's routing and dispatch, and the same outputs and error
+    bits as molora_route_vocab followed by molora_dispatch (sizes on both sides of the
+    shared-memory staging limit of 40960 slots)."""
+    g = torch.Generator().manual_seed(N + 31 * K)
+    starts = torch.cat([torch.zeros(1, dtype=torch.int32),
+                        torch.sort(torch.randperm(31999, generator=g)[:K - 1] + 1).values.int(),
+                        torch.tensor([32000], dtype=torch.int32)])
+    lo, hi = (-50, 32050) if outside else (0, 32000)
+    tok = torch.randint(lo, hi, (N,), generator=g, dtype=torch.int32)
+    e1, e2 = err_word(), err_word()
+    adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(dev(tok), dev(starts), err_word=e1)
+    a2 = m.molora_route_vocab(dev(tok), dev(starts), err_word=e2)
+    c2, o2, p2 = m.molora_dispatch(a2, K, err_word=e2)
+    torch.cuda.synchronize()
+    ref_a, n_out = oracle.route_vocab(tok, starts)
+    rc, ro, rp, _ = oracle.dispatch(ref_a, K)
+    assert torch.equal(adapter.cpu(), ref_a) and torch.equal(adapter.cpu(), a2.cpu())
+    for got, sep, ref in ((counts, c2, rc), (offsets, o2, ro), (perm, p2, rp)):
+        assert torch.equal(got.cpu(), ref) and torch.equal(got.cpu(), sep.cpu())
+    assert int(e1.item()) == int(e2.item())
+    assert (int(e1.item()) != 0) == (n_out > 0)
+
+
+def test_route_vocab_dispatch_fused_bad_ranges(m):
+    starts = torch.tensor([0, 30, 20, 40], dtype=torch.int32)
+    tok = torch.arange(0, 45, dtype=torch.int32)
+    e1, e2 = err_word(), err_word()
+    adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(dev(tok), dev(starts), err_word=e1)
+    a2 = m.molora_route_vocab(dev(tok), dev(starts), err_word=e2)
+    c2, o2, p2 = m.molora_dispatch(a2, 3, err_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) & m.DEV_BAD_RANGES and int(e1.item()) == int(e2.item())
+    for got, sep in ((adapter, a2), (counts, c2), (offsets, o2), (perm, p2)):
+        assert torch.equal(got.cpu(), sep.cpu())
+
+
 # ------------------------------------------------------------------------- apply
 
 def small_int_case(N, d_in, d_out, K, r, k, seed, dtype=torch.bfloat16):

@@ -72,6 +72,14 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_dispatch(fake, 8, 0, 4, fake, fake, fake, None, None) == INVALID
     assert lib.molora_dispatch(fake, 8, 1, 65, fake, fake, fake, None, None) == INVALID
     assert lib.molora_dispatch(fake, 8, 1, 4, None, fake, fake, None, None) == INVALID
+    # fused routing + dispatch: K out of range, null pointers; N == 0 still needs counts/offsets
+    lib.molora_route_vocab_dispatch.argtypes = [P, I64, P, I32, P, P, P, P, P, P]
+    assert lib.molora_route_vocab_dispatch(fake, 8, fake, 0, fake, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_route_vocab_dispatch(fake, 8, fake, 65, fake, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_route_vocab_dispatch(None, 8, fake, 4, fake, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_route_vocab_dispatch(fake, 8, None, 4, fake, fake, fake, fake, None, None) == INVALID
+    assert lib.molora_route_vocab_dispatch(fake, 8, fake, 4, fake, fake, None, fake, None, None) == INVALID
+    assert lib.molora_route_vocab_dispatch(fake, -1, fake, 4, fake, fake, fake, fake, None, None) == INVALID
 
     def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0):
         return lib.molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, None, k, fake, fake, fake,

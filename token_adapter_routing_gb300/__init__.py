@@ -23,8 +23,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
-    "molora_lora_apply_masked_pass", "molora_select_path", "molora_selftest_bounded_wait", "library_path",
+    "molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+    "molora_lora_apply", "molora_lora_apply_masked_pass", "molora_select_path", "molora_selftest_bounded_wait", "library_path",
     "load_library",
     "MoloraError", "PATHS", "DEV_TOKEN_OUTSIDE_RANGES", "DEV_BAD_RANGES", "DEV_BAD_ADAPTER_ID",
     "DEV_BAD_PERMUTATION", "DEV_WAIT_TIMEOUT", "MAX_ADAPTERS", "ROUTER_HIDDEN",
@@ -42,7 +42,8 @@ DEV_WAIT_TIMEOUT = 0x10
 MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
-EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
+EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+            "molora_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path",
             "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
@@ -73,6 +74,7 @@ def load_library():
     lib.molora_route_vocab.argtypes = [P, I64, P, I32, P, P, P]
     lib.molora_router_topk.argtypes = [P, S, I64, I32, P, P, P, P, I32, I32, P, P, P, P]
     lib.molora_dispatch.argtypes = [P, I64, I32, I32, P, P, P, P, P]
+    lib.molora_route_vocab_dispatch.argtypes = [P, I64, P, I32, P, P, P, P, P, P]
     lib.molora_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P]
     lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
@@ -81,7 +83,8 @@ def load_library():
     lib.molora_status_string.restype = ctypes.c_char_p
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
-    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_lora_apply",
+    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+                 "molora_lora_apply",
                  "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path", "molora_version",
                  "molora_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
@@ -180,6 +183,28 @@ def molora_dispatch(ids, K, counts=None, offsets=None, perm=None, err_word=None,
     _check("molora_dispatch", load_library().molora_dispatch(
         _p(ids), N, k, K, _p(counts), _p(offsets), _p(perm), _p(err_word), _stream(stream)))
     return counts, offsets, perm
+
+
+def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=None, perm=None, err_word=None,
+                                stream=None):
+    """molora_route_vocab then molora_dispatch (k = 1) as one kernel: (adapter, counts, offsets, perm)."""
+    _cuda(tok, "tok", torch.int32, 1)
+    _cuda(starts, "starts", torch.int32, 1)
+    N, K = tok.numel(), starts.numel() - 1
+    dev = tok.device
+    if adapter is None:
+        adapter = torch.empty(N, dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty(K, dtype=torch.int32, device=dev)
+    if offsets is None:
+        offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
+    if perm is None:
+        perm = torch.empty(N, dtype=torch.int32, device=dev)
+    for name, t in (("adapter", adapter), ("counts", counts), ("offsets", offsets), ("perm", perm)):
+        _cuda(t, name, torch.int32)
+    _check("molora_route_vocab_dispatch", load_library().molora_route_vocab_dispatch(
+        _p(tok), N, _p(starts), K, _p(adapter), _p(counts), _p(offsets), _p(perm), _p(err_word), _stream(stream)))
+    return adapter, counts, offsets, perm
 
 
 def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None, perm=None, err_word=None,

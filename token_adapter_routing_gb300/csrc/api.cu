@@ -85,6 +85,14 @@ molora_status molora_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t 
   return launched(launch_dispatch(ids, N, k, K, counts, offsets, perm, err_word, stream));
 }
 
+molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                          int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                          int32_t* err_word, cudaStream_t stream) {
+  if (N < 0 || K < 1 || K > kMaxAdapters || N > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (!starts || !counts || !offsets || (N > 0 && (!tok || !adapter || !perm))) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, stream));
+}
+
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
                                int32_t k) {
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;

@@ -68,6 +68,7 @@ struct GroupedPlan {
   uint32_t off_recv; // receive slots for partial h, [C sources][128/C rows][r] fp32
   uint32_t region;   // bytes before the control block (1024-aligned)
   int prefetch_y;    // send this CTA's y row segments to L2 once its x gather has landed
+  uint64_t early_y;  // bytes at the start of y prefetched as contiguous shares before the tile is known
   uint32_t smem;     // dynamic shared memory requested
 };
 
@@ -110,7 +111,7 @@ bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, Group
   s->off_g = 0;
   s->off_b = (uint32_t)off_b;
   s->off_s = (uint32_t)off_s;
-  int max_xr = 256;
+  int max_xr = 512;  // one round when the whole K-slice fits: fewer barrier round trips
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_XR")) max_xr = atoi(e);
 #endif
@@ -189,6 +190,7 @@ struct __align__(8) Ctrl {
   int32_t tok[kTileM];    // token of each tile row, -1 for padding (drives the gather)
   int32_t live[kTileM];   // row passed validation and gets a reduction
   float wgt[kTileM];      // weight of each tile row (0 for padding or invalid)
+  int32_t offs[kMaxAdapters + 1];  // the dispatch offsets, loaded once by K+1 threads at a time
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -238,10 +240,26 @@ __global__ void __maxnreg__(168)
       tma_prefetch_desc(&map_b);
     }
   }
+  if (P.early_y > 0 && warp == 0) {
+    // The first P.early_y bytes of y, an equal contiguous share per CTA, in 32 KB pieces.
+    // Nothing here depends on the previous kernel (a prefetch only moves lines into L2), and
+    // DRAM is otherwise idle until the tile's rows are known and the x gather starts.
+    const uint64_t total = P.early_y;
+    const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) & ~uint64_t(15);
+    const uint64_t begin = (uint64_t)blockIdx.x * share;
+    const uint64_t end = begin + share < total ? begin + share : total;
+    for (uint64_t off = begin + (uint64_t)lane * 32768u; off < end; off += 32u * 32768u) {
+      const uint64_t len = end - off < 32768u ? end - off : 32768u;
+      prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(y) + off, (uint32_t)(len & ~uint64_t(15)));
+    }
+  }
   pdl_wait();
   pdl_launch_dependents();
 
   // ---- which tile this cluster owns (identical in every CTA of the cluster)
+  if (mask_adapter < 0)
+    for (int i = tid; i <= K; i += kThreads) ctrl->offs[i] = offsets[i];
+  __syncthreads();
   if (tid == 0) {
     TileInfo ti{-1, 0, 0, 0};
     if (mask_adapter >= 0) {
@@ -249,10 +267,10 @@ __global__ void __maxnreg__(168)
       if (t0 < N) ti = TileInfo{mask_adapter, (int32_t)t0, (int32_t)(N - t0 < TM ? N - t0 : TM), 0};
     } else {
       int32_t cum = 0;
-      int32_t prev = offsets[0];
+      int32_t prev = ctrl->offs[0];
       bool bad = prev != 0;
       for (int a = 0; a < K && ti.adapter < 0 && !bad; ++a) {
-        const int32_t nxt = offsets[a + 1];
+        const int32_t nxt = ctrl->offs[a + 1];
         if (nxt < prev || nxt > S) {
           bad = true;
           break;
@@ -344,9 +362,9 @@ __global__ void __maxnreg__(168)
     }
     cp_async_commit();
   };
-  if (warp < 4) {
-    gather(0);
-    // validate this row's slot while the gather is in flight
+  // checks this row's slot against the tile's adapter and records its weight; its loads go
+  // out once the x rounds are in flight, so their latency hides behind the gather
+  auto validate = [&]() {
     const int row = tid;
     int32_t live = 0;
     float wt = 0.f;
@@ -366,6 +384,10 @@ __global__ void __maxnreg__(168)
     }
     ctrl->live[row] = live;
     ctrl->wgt[row] = wt;
+  };
+  if (warp < 4) {
+    gather(0);
+    if (rounds == 1) validate();
   }
   for (int rd = 0; rd < rounds; ++rd) {
     if (warp < 4) {
@@ -377,6 +399,7 @@ __global__ void __maxnreg__(168)
           report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
         }
         gather(rd + 1);
+        if (rd == 0) validate();
         cp_async_wait_group<1>();  // round rd has landed; round rd+1 stays in flight
       } else {
         cp_async_wait_all();
@@ -632,8 +655,18 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
     return cudaErrorNotSupported;
   s.prefetch_y = 1;
+  // DRAM idles for about 2 us while the tile is decoded; prefetching 40% of y (at most
+  // 16 MiB) fills that window and measured best on GB300 (4-modality workload, back-to-back
+  // steps: 0, 25, 33, 40, 50 and 60% tried).  The rest of y follows per row, late.
+  const uint64_t y_bytes = (uint64_t)N * d_out * 4u;
+  const uint64_t early = y_bytes * 2u / 5u;
+  s.early_y = (early < (16ull << 20) ? early : (16ull << 20)) & ~uint64_t(15);
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
+  if (const char* e = getenv("MOLORA_EARLY_Y")) {
+    const int pct = atoi(e) < 0 ? 0 : (atoi(e) > 100 ? 100 : atoi(e));
+    s.early_y = (y_bytes * (uint64_t)pct / 100u) & ~uint64_t(15);
+  }
 #endif
   CUtensorMap map_a, map_b;
   const CUtensorMapSwizzle swa =

@@ -2,6 +2,8 @@
 // stable permutation) of "MoLoRA: Composable Specialization via Per-Token Adapter Routing"
 // (Table 1: R_vocab(v), histogram computation, pointer arrays; Figure 2 right: tokens
 // grouped by their selected adapter).
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -54,43 +56,94 @@ cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* sta
 }
 
 // ---------------------------------------------------------------------------------------
-// Dispatch: a single CTA of 32 warps.  Warp w owns a contiguous run of slots; it walks the
-// run 32 slots at a time, and __match_any_sync groups the lanes that carry the same adapter
-// id.  Pass 1 counts slots per (warp, adapter).  The counts, read adapter-major, give each
-// (adapter, warp) the first output position of its slots (the exclusive scan).  Pass 2
-// repeats the walk and writes each slot at base + its rank among equal lanes of lower index,
-// so the permutation is stable: within an adapter, slots appear in ascending order.  No
-// atomics whose order could change a result; no inter-CTA waiting.
+// Dispatch: a single CTA of 32 warps.  Every slot's id is read once (with coalesced loads)
+// and, up to kStageSlots slots, kept in shared memory for the two passes below.  Warp w owns
+// a contiguous run of slots; it walks the run 32 slots at a time, and __match_any_sync
+// groups the lanes that carry the same adapter id.  Pass 1 counts slots per (warp, adapter).
+// The counts, read adapter-major, give each (adapter, warp) the first output position of
+// its slots (the exclusive scan).  Pass 2 repeats the walk and writes each slot at base +
+// its rank among equal lanes of lower index, so the permutation is stable: within an
+// adapter, slots appear in ascending order.  No atomics whose order could change a result;
+// no inter-CTA waiting.
+//
+// kVocab: the slots are tokens (k = 1) and their ids come from vocabulary routing done in
+// the same pass (the routed ids are also written to `adapter`), which saves the separate
+// routing kernel and its round trip through global memory.
 constexpr int kDispatchWarps = 32;
+constexpr int64_t kStageSlots = 40960;  // 160 KB of shared memory
 
+__device__ __forceinline__ int32_t vocab_range(const int32_t* s_starts, int32_t K, int32_t v) {
+  if (v < s_starts[0] || v >= s_starts[K]) return -1;
+  int lo = 0, hi = K;  // s_starts[lo] <= v < s_starts[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_starts[mid] <= v)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+template <bool kVocab>
 __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
-    dispatch_kernel(const int32_t* __restrict__ ids, int64_t S, int32_t K, int32_t* __restrict__ counts,
-                    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* err_word) {
+    dispatch_kernel(const int32_t* __restrict__ src, const int32_t* __restrict__ starts, int64_t S, int32_t K,
+                    int32_t* adapter, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ perm, int32_t* err_word) {
+  extern __shared__ int32_t s_ids[];  // [S] when S <= kStageSlots
   __shared__ int32_t cnt[kDispatchWarps][kMaxAdapters];
   __shared__ int32_t s_total[kMaxAdapters];
   __shared__ int32_t s_off[kMaxAdapters + 1];
+  __shared__ int32_t s_starts[kMaxAdapters + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool staged = S <= kStageSlots;
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
   pdl_wait();
   pdl_launch_dependents();
-  __syncthreads();
+  if (kVocab) {
+    for (int i = threadIdx.x; i <= K; i += blockDim.x) s_starts[i] = starts[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int a = 0; a < K; ++a)
+        if (s_starts[a] >= s_starts[a + 1]) {
+          report(err_word, MOLORA_DEV_BAD_RANGES);
+          break;
+        }
+    }
+  }
+
+  // every slot's id, read once; invalid ids become -1
+  bool bad = false, outside = false;
+  for (int64_t s = threadIdx.x; s < S; s += blockDim.x) {
+    int32_t a;
+    if (kVocab) {
+      a = vocab_range(s_starts, K, src[s]);
+      outside |= a < 0;
+      adapter[s] = a;
+    } else {
+      a = src[s];
+    }
+    if (a < 0 || a >= K) {
+      bad = true;
+      a = -1;
+    }
+    if (staged) s_ids[s] = a;
+  }
+  __syncthreads();  // also orders the adapter[] stores above before the re-reads below
+  auto id_of = [&](int64_t s) -> int32_t {
+    if (staged) return s_ids[s];
+    const int32_t a = kVocab ? adapter[s] : src[s];
+    return (a < 0 || a >= K) ? -1 : a;
+  };
 
   const int64_t per_warp = ((S + kDispatchWarps * 32 - 1) / (kDispatchWarps * 32)) * 32;
   const int64_t beg = min(S, (int64_t)warp * per_warp);
   const int64_t end = min(S, beg + per_warp);
   const unsigned lanes_below = (1u << lane) - 1u;
 
-  bool bad = false;
   for (int64_t base = beg; base < end; base += 32) {
     const int64_t s = base + lane;
-    int32_t a = -1;
-    if (s < end) {
-      a = ids[s];
-      if (a < 0 || a >= K) {
-        bad = true;
-        a = -1;
-      }
-    }
+    const int32_t a = s < end ? id_of(s) : -1;
     const unsigned m = __match_any_sync(0xffffffffu, a);
     if (a >= 0 && lane == __ffs(m) - 1) cnt[warp][a] += __popc(m);
   }
@@ -126,11 +179,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
 
   for (int64_t base = beg; base < end; base += 32) {
     const int64_t s = base + lane;
-    int32_t a = -1;
-    if (s < end) {
-      a = ids[s];
-      if (a < 0 || a >= K) a = -1;
-    }
+    const int32_t a = s < end ? id_of(s) : -1;
     const unsigned m = __match_any_sync(0xffffffffu, a);
     if (a >= 0) perm[cnt[warp][a] + __popc(m & lanes_below)] = (int32_t)s;
     __syncwarp();
@@ -139,12 +188,36 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   }
   for (int64_t i = s_off[K] + threadIdx.x; i < S; i += blockDim.x) perm[i] = -1;
   if (__any_sync(0xffffffffu, bad) && lane == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
+  if (kVocab && __any_sync(0xffffffffu, outside) && lane == 0) report(err_word, MOLORA_DEV_TOKEN_OUTSIDE_RANGES);
+}
+
+template <bool kVocab>
+static cudaError_t launch_dispatch_impl(const int32_t* src, const int32_t* starts, int64_t S, int32_t K,
+                                        int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* err_word, cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(dispatch_kernel<kVocab>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(kStageSlots * 4));
+    if (attr != cudaSuccess) cudaGetLastError();
+  });
+  if (attr != cudaSuccess) return attr;
+  const size_t smem = S <= kStageSlots ? (size_t)S * 4 : 0;
+  return launch_kernel(dispatch_kernel<kVocab>, dim3(1), dim3(kDispatchWarps * 32), smem, stream, 0, src, starts, S,
+                       K, adapter, counts, offsets, perm, err_word);
 }
 
 cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* err_word, cudaStream_t stream) {
-  return launch_kernel(dispatch_kernel, dim3(1), dim3(kDispatchWarps * 32), 0, stream, 0, ids, N * (int64_t)k, K,
-                       counts, offsets, perm, err_word);
+  return launch_dispatch_impl<false>(ids, nullptr, N * (int64_t)k, K, nullptr, counts, offsets, perm, err_word,
+                                     stream);
+}
+
+cudaError_t launch_route_vocab_dispatch(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                        int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* err_word, cudaStream_t stream) {
+  return launch_dispatch_impl<true>(tok, starts, N, K, adapter, counts, offsets, perm, err_word, stream);
 }
 
 // ---------------------------------------------------------------------------------------
