@@ -24,14 +24,14 @@ static bool valid_dtype(molora_dtype d) { return d == MOLORA_F32 || d == MOLORA_
 static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_OK : MOLORA_ERR_CUDA; }
 
 // Smallest slot count (N*k) at which the grouped tensor-core apply beats the scalar apply,
-// measured on GB300 with the decode sweep (route -> dispatch -> apply in one CUDA graph,
-// d = 4096, r = 16, top-1, batch 1..512, uniform and Zipf(1.1) adapter draws, L2 flushed
-// between replays).  With up to 16 hot-set adapters the grouped path is as fast or faster from
-// batch 1; with 32 it wins from batch 128; with 64 the scalar path wins at every batch up to
-// 512, because a grouped launch then carries up to K mostly one-token tiles.
+// measured on GB300 with the decode sweep (d = 4096, r = 16, top-1, batch 1..512, uniform and
+// Zipf(1.1) adapter draws, L2 flushed between replays; vocabulary routing -> scalar apply
+// against routing with dispatch -> grouped apply, each as one CUDA graph).  With up to 32
+// hot-set adapters the grouped path is as fast or faster from batch 1; with 64 the scalar
+// path wins at every batch up to 512, because a grouped launch then carries up to K mostly
+// one-token tiles.
 static int64_t crossover_tokens(int32_t K) {
-  if (K <= 16) return 1;
-  if (K <= 32) return 128;
+  if (K <= 32) return 1;
   return 1024;
 }
 
