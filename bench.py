@@ -15,8 +15,9 @@ comes round again (inputs larger than L2 instead of a flush).  ``value`` = token
 and ``roofline`` relates that
 kernel's algorithmic bytes per launch (x read once, y read and written once, the adapters
 it touches read once) to its measured duration.  ``e2e`` runs the same path through the
-public calls with the step's inputs copied from pinned host memory and y copied back
-inside the timed region.  ``cpu_baseline`` times the CPU oracle (single thread) on the same
+public calls with every step's inputs copied from pinned host memory and its y copied back
+inside the timed region, pipelined as a serving loop would (copy-in, compute and copy-out
+of consecutive steps overlap on three streams).  ``cpu_baseline`` times the CPU oracle (single thread) on the same
 inputs.
 
 Multi-GPU: tokens are independent, so each rank runs its own batch (weak scaling, no
@@ -324,48 +325,66 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(m, wl, dev, args, world):
-    """Public calls with host buffers: H2D of the step's inputs, the path, D2H of y."""
+    """Public calls with host buffers, run as a serving loop would: step i's inputs (token ids,
+    x, y0) go host -> device on a copy-in stream while step i-1 computes and step i-2's y goes
+    device -> host on a copy-out stream (two device buffer sets, event-ordered).  Timed from
+    the first copy in to the last copy out; every step moves its own inputs and result."""
     tok_h = wl.tok.pin_memory()
     x_h = wl.x.pin_memory()
     y0_h = wl.y0.pin_memory()
-    y_h = torch.empty_like(y0_h).pin_memory()
+    y_h = [torch.empty_like(y0_h).pin_memory() for _ in range(2)]
     starts = wl.starts.to(dev)
     A, B = wl.A.to(dev), wl.B.to(dev)  # the hot set stays resident
-    tok = torch.empty_like(wl.tok, device=dev)
-    x = torch.empty_like(wl.x, device=dev)
-    y = torch.empty_like(wl.y0, device=dev)
-    adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
-    counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
-    offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
+    bufs = [{"tok": torch.empty_like(wl.tok, device=dev), "x": torch.empty_like(wl.x, device=dev),
+             "y": torch.empty_like(wl.y0, device=dev),
+             "adapter": torch.empty(wl.N, dtype=torch.int32, device=dev),
+             "counts": torch.empty(wl.K, dtype=torch.int32, device=dev),
+             "offsets": torch.empty(wl.K + 1, dtype=torch.int32, device=dev),
+             "perm": torch.empty(wl.N, dtype=torch.int32, device=dev)} for _ in range(2)]
+    s_in, s_comp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
-    def one():
-        tok.copy_(tok_h, non_blocking=True)
-        x.copy_(x_h, non_blocking=True)
-        y.copy_(y0_h, non_blocking=True)
-        m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
-        m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
-                            path=args.path)
-        y_h.copy_(y, non_blocking=True)
+    def run(steps):
+        ev_in = [torch.cuda.Event() for _ in range(steps)]
+        ev_comp = [torch.cuda.Event() for _ in range(steps)]
+        ev_out = [torch.cuda.Event() for _ in range(steps)]
+        for i in range(steps):
+            b = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_out[i - 2])  # this buffer set's last result has left
+                b["tok"].copy_(tok_h, non_blocking=True)
+                b["x"].copy_(x_h, non_blocking=True)
+                b["y"].copy_(y0_h, non_blocking=True)
+                ev_in[i].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[i])
+                m.molora_route_vocab_dispatch(b["tok"], starts, adapter=b["adapter"], counts=b["counts"],
+                                              offsets=b["offsets"], perm=b["perm"])
+                m.molora_lora_apply(b["x"], A, B, b["adapter"], b["y"], wl.scale, counts=b["counts"],
+                                    offsets=b["offsets"], perm=b["perm"], path=args.path)
+                ev_comp[i].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                y_h[i % 2].copy_(b["y"], non_blocking=True)
+                ev_out[i].record(s_out)
 
     steps = max(5, min(args.steps, 50))
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            one()
-        stream.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            one()
-        e1.record(stream)
-        stream.synchronize()
+    run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    run(steps)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    e1.record(s_out)
+    torch.cuda.synchronize()
     sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
     h2d = tok_h.numel() * 4 + x_h.numel() * x_h.element_size() + y0_h.numel() * 4
-    d2h = y_h.numel() * 4
+    d2h = y_h[0].numel() * 4
     return {"value": round(wl.N * world * steps / sec, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(sec / steps * 1e3, 4)}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(sec / steps * 1e3, 4),
+            "pipeline": "copy-in, compute and copy-out on three streams, two device buffer sets"}
 
 
 def load_profiled_traffic(path):
