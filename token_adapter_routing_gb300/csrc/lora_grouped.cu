@@ -183,7 +183,7 @@ struct __align__(8) Ctrl {
   uint64_t bar_full[2];   // expand pass done, per TMEM buffer
   uint64_t bar_empty[2];  // epilogue drained a TMEM buffer
   uint64_t bar_recv;      // partial-h rows this CTA owns have arrived from every CTA
-  uint64_t bar_g;         // all 128 rows of g (hi and lo) have arrived from their owners
+  uint64_t bar_g;         // all TM rows of g (hi and lo) have arrived from their owners
   uint32_t tmem_base;
   int32_t abort;
   TileInfo tile;
@@ -233,9 +233,9 @@ __global__ void __maxnreg__(168)
       mbar_init(&ctrl->bar_recv, 1);
       mbar_init(&ctrl->bar_g, 1);
       mbar_fence_init();
-      // both receive 128 rows x r values: fp32 partials, and g as two bf16 halves
-      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)kTileM * r * 4u);
-      mbar_arrive_expect_tx(&ctrl->bar_g, (uint32_t)kTileM * r * 4u);
+      // both receive the tile's TM rows x r values: fp32 partials, and g as two bf16 halves
+      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)P.TM * r * 4u);
+      mbar_arrive_expect_tx(&ctrl->bar_g, (uint32_t)P.TM * r * 4u);
       tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b);
     }
@@ -453,7 +453,7 @@ __global__ void __maxnreg__(168)
   // (st.async into the owner's receive slots, counted by its bar_recv); the owner sums the
   // C partials in rank order (deterministic), forms g = scale * w * h, splits it into bf16
   // hi + lo, and sends both rows to every CTA's g tiles (counted by their bar_g).
-  const int RPC = kTileM / C;
+  const int RPC = TM / C;  // only the tile's TM rows travel; MMA rows past them stay local
   float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [C sources][RPC rows][r]
   bool have_h = true;
   if (warp < 4) {
@@ -473,22 +473,24 @@ __global__ void __maxnreg__(168)
   cluster_wait();  // every CTA's barriers are armed
   if (warp < 4) {
     const int row = tid;
-    const uint32_t owner = (uint32_t)(row / RPC);
-    const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * r), owner);
-    const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
-    float v[16];
-    for (int c0 = 0; c0 < r; c0 += 16) {
-      if (have_h && warp * 32 < TM)  // rows past the tile hold unused MMA rows: send zeros
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-      else
+    if (warp * 32 < TM) {  // whole warps: TM is 64 or 128
+      const uint32_t owner = (uint32_t)(row / RPC);
+      const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * r), owner);
+      const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
+      float v[16];
+      for (int c0 = 0; c0 < r; c0 += 16) {
+        if (have_h)
+          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+        else
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        st_async_v4(dst + (c0 + 4 * i) * 4,
-                    make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
-                               __float_as_uint(v[4 * i + 3])),
-                    dst_bar);
+        for (int i = 0; i < 4; ++i)
+          st_async_v4(dst + (c0 + 4 * i) * 4,
+                      make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                 __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])),
+                      dst_bar);
+      }
     }
     tc_fence_before();
     // owner: reduce its rows once every source has delivered them
