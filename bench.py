@@ -201,10 +201,13 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(i):
+    def route(i):
         b = batches[i % N_BATCHES]
         m.molora_route_vocab_dispatch(b["tok"], starts, adapter=b["adapter"], counts=b["counts"],
                                       offsets=b["offsets"], perm=b["perm"], err_word=err)
+
+    def step(i):
+        route(i)
         apply(i)
 
     def apply(i):
@@ -226,6 +229,8 @@ def run_ours(args, rank, world, local):
         stream.synchronize()
         g_warm, g_steps, g_applies = capture(step, warm), capture(step, args.steps), capture(apply, args.steps)
         g_one = capture(step, 1)
+        g_route = capture(route, args.steps)
+        g_warm_apply = capture(lambda i: apply(0), args.steps)
     n_active = [int((torch.bincount(b["adapter"].cpu().long(), minlength=wl.K) > 0).sum().item()) for b in batches]
     launches_per_step = 2  # route_vocab + dispatch (one kernel), apply
 
@@ -267,6 +272,10 @@ def run_ours(args, rank, world, local):
         barrier(world)
         clk = clocks.stop()
         flushed_s = timed_flushed(g_one, min(args.steps, 100))
+        rd_s = timed_block(g_route)  # routing + dispatch alone, the same batches, back to back
+        g_warm_apply.replay()
+        stream.synchronize()
+        warm_s = timed_block(g_warm_apply)  # one batch over and over: x and y stay in L2
     total_s = max_over_ranks(step_s, world, dev)
     apply_s = max_over_ranks(apply_s, world, dev)
     flushed_s = max_over_ranks(flushed_s, world, dev)
@@ -308,6 +317,8 @@ def run_ours(args, rank, world, local):
                              "CUDA graph (programmatic dependent launch between consecutive kernels)",
                    "parallelism": f"dp{world}" if world > 1 else "single-gpu"},
         "ms_per_step_flushed": round(flushed_s * 1e3, 6),
+        "route_dispatch_us": round(max_over_ranks(rd_s, world, dev) / args.steps * 1e6, 3),
+        "apply_warm_us": round(max_over_ranks(warm_s, world, dev) / args.steps * 1e6, 3),
         "apply_only": {"value": round(wl.N * world / apply_mean_s, 1), "unit": UNIT,
                        "us_per_launch": round(apply_mean_s * 1e6, 3)},
         "roofline": roof,
@@ -317,10 +328,13 @@ def run_ours(args, rank, world, local):
                         "timed in a second block of the same run",
         "flushed_timing": "ms_per_step_flushed: one batch, a 256 MiB write before each step, CUDA events around "
                           "each graph replay (includes the graph launch)",
+        "extra_timing": "route_dispatch_us: the fused routing + dispatch kernel alone over the same batches, back "
+                        "to back; apply_warm_us: the apply on one batch over and over (x and y stay in L2)",
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+        result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(wl, args.cpu_budget_s / 2)
     return result
 
 
@@ -426,6 +440,36 @@ def cpu_baseline(wl, budget_s):
     return {"value": round(wl.N * reps / el, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"full batch ({wl.N} tokens: route_vocab + dispatch + lora_apply in double) x {reps} reps, "
                       f"{el:.1f} s"}
+
+
+def cpu_baseline_all_cores(wl, budget_s):
+    """The same oracle step with the apply split over the host's cores: route and dispatch once
+    on the whole batch, then one oracle apply call per token block on a thread pool (the C
+    oracle runs without the interpreter lock)."""
+    import concurrent.futures
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    bounds = [wl.N * i // cores for i in range(cores + 1)]
+
+    def step(pool):
+        adapter, _ = oracle.route_vocab(wl.tok, wl.starts)
+        oracle.dispatch(adapter, wl.K)
+        futs = [pool.submit(oracle.lora_apply, wl.x[a:b], wl.A, wl.B, adapter[a:b], wl.y0[a:b], wl.scale)
+                for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        return [f.result()[0] for f in futs]
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as pool:
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            step(pool)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= 1000:
+                break
+    return {"value": round(wl.N * reps / el, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"full batch ({wl.N} tokens), apply split into {cores} token blocks on {cores} threads, "
+                      f"x {reps} reps, {el:.1f} s"}
 
 
 def run_reference(args, rank, world):

@@ -575,15 +575,17 @@ __global__ void __maxnreg__(168)
       const bool ok = mbar_wait(&ctrl->bar_full[buf], (p >> 1) & 1);
       tc_fence_after();
       if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-      for (int q = 0; ok && !ctrl->abort && q < width; q += P.piece) {
+      // warps whose rows all lie past the tile (TM = 64) have nothing to drain
+      for (int q = 0; ok && !ctrl->abort && warp * 32 < TM && q < width; q += P.piece) {
         const int cols = min(P.piece, width - q);
         bulk_wait_read<0>();  // the previous reduction has read the stage
         for (int c0 = 0; c0 < cols; c0 += 32) {
           float v[32];
           tmem_ld32(lane_base + buf * P.PW + q + c0, v);
           float4* dst = reinterpret_cast<float4*>(srow + c0);
+          if (my_tok >= 0)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         // one bulk reduction per row segment, performed by the TMA unit in L2
         fence_proxy_async_smem();
