@@ -63,7 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq"], default="step",
+    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew"], default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     return p.parse_args(argv)
@@ -543,7 +543,10 @@ def run_mode(args):
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
                K=4, r=16, top-2): router alone, and router -> dispatch -> apply.
     perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
-               passes over all tokens against one per-token pass."""
+               passes over all tokens against one per-token pass.
+    skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
+               80/10/5/5, 95/2/2/1 modality shares per run): the apply alone and the whole step,
+               back to back over six batches as in the main line."""
     import token_adapter_routing_gb300 as m
     from token_adapter_routing_gb300 import build as lib_build
     lib_build.build()
@@ -556,7 +559,62 @@ def run_mode(args):
     def emit(d):
         print(json.dumps(d), flush=True)
 
-    if args.mode == "crossover":
+    if args.mode == "skew":
+        peaks, _ = measured_peaks()
+        for dist in ("uniform", "80-10-5-5", "95-2-2-1"):
+            wls = [workloads.make(WORKLOAD, seed=1234 + 1 + b, dist=dist) for b in range(N_BATCHES)]
+            starts, A, B = wls[0].starts.to(dev), wls[0].A.to(dev), wls[0].B.to(dev)
+            bs = [{"tok": w_.tok.to(dev), "x": w_.x.to(dev), "y": w_.y0.to(dev),
+                   "adapter": torch.empty(w_.N, dtype=torch.int32, device=dev),
+                   "counts": torch.empty(w_.K, dtype=torch.int32, device=dev),
+                   "offsets": torch.empty(w_.K + 1, dtype=torch.int32, device=dev),
+                   "perm": torch.empty(w_.N, dtype=torch.int32, device=dev)} for w_ in wls]
+
+            def route(i):
+                b = bs[i % N_BATCHES]
+                m.molora_route_vocab_dispatch(b["tok"], starts, adapter=b["adapter"], counts=b["counts"],
+                                              offsets=b["offsets"], perm=b["perm"])
+
+            def apply(i):
+                b = bs[i % N_BATCHES]
+                m.molora_lora_apply(b["x"], A, B, b["adapter"], b["y"], wls[0].scale, counts=b["counts"],
+                                    offsets=b["offsets"], perm=b["perm"], path="grouped")
+
+            n = 120
+            with torch.cuda.stream(stream):
+                for i in range(N_BATCHES):
+                    route(i)
+                    apply(i)
+                stream.synchronize()
+                gs, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, stream=stream):
+                    for i in range(n):
+                        route(i)
+                        apply(i)
+                with torch.cuda.graph(ga, stream=stream):
+                    for i in range(n):
+                        apply(i)
+                res = {}
+                for name, g in (("step", gs), ("apply", ga)):
+                    g.replay()
+                    ts = []
+                    for _ in range(5):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        stream.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e3 / n)
+                    res[name] = statistics.median(ts)
+            groups = [torch.bincount(b["adapter"].cpu().long(), minlength=wls[0].K).tolist() for b in bs]
+            n_active = [sum(1 for c in gr if c > 0) for gr in groups]
+            algo = sum(algorithmic_bytes(w_, na) for w_, na in zip(wls, n_active)) / N_BATCHES
+            emit({"mode": "skew", "dist": dist, "workload": "N=2048, d=4096, K=4, r=16 (4-modality benchmark)",
+                  "group_sizes_first_batch": groups[0], "apply_us": round(res["apply"], 3),
+                  "step_us": round(res["step"], 3), "apply_GBps": round(algo / (res["apply"] * 1e-6) / 1e9, 1),
+                  "frac_of_measured": round(algo / (res["apply"] * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                  "l2": f"inputs larger than L2 ({N_BATCHES} resident batches, back to back)"})
+    elif args.mode == "crossover":
         for dist in ("uniform", "zipf"):
             for K in (4, 8, 16, 32, 64):
                 for b in (1, 8, 32, 64, 128, 160, 256, 512):

@@ -199,6 +199,8 @@ def test_apply_small_integers_bitexact(m, path, N, d_in, d_out, K, r, k):
     ("decode_sweep", {"N": 1, "K": 4}),
     ("modality4", {"N": 333, "d_in": 2048, "d_out": 1024, "r": 32}),
     ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048, "r": 64, "K": 8}),
+    ("modality4", {"dist": "80-10-5-5"}),
+    ("modality4", {"dist": "95-2-2-1"}),
 ])
 def test_apply_vocab_routed_vs_oracle(m, path, name, kw):
     wl = workloads.make(name, **kw)

@@ -12,7 +12,9 @@ workloads measured in "MoLoRA: Composable Specialization via Per-Token Adapter R
   0 tiny_vocab    N=256, d_in=d_out=512, K=4, r=8, fp32, vocabulary routing.
   1 modality4     N=2048, d_in=d_out=4096, K=4, r=16, bf16 (Table 3's 4-modality kernel
                   benchmark: text / image / audio / video vocabulary ranges).  Tokens come in
-                  runs of geometric length (mean 64), one uniformly drawn modality per run.
+                  runs of geometric length (mean 64), one uniformly drawn modality per run;
+                  ``dist`` "80-10-5-5" or "95-2-2-1" draws each run's modality with those
+                  shares instead (Table 9's group-size distributions).
   2 topk_mlp      N=4096, d_in=2048, d_out=6144, K=4, r=16, k=2, bf16, learned router
                   (Figure 2's top-2 weighted sum at a Qwen3-1.7B MLP shape).
   3 decode_sweep  b tokens x K hot-set adapters, d_in=d_out=4096, r=16, bf16, top-1; adapter
@@ -92,16 +94,24 @@ def _tokens_in_ranges(g, modality: torch.Tensor, starts: torch.Tensor) -> torch.
     return (lo + torch.floor(u * (hi - lo).to(torch.float64)).to(torch.int64)).to(torch.int32)
 
 
-def modality_runs(g, N: int, K: int, mean_run: float = 64.0) -> torch.Tensor:
+SHARES = {"80-10-5-5": (0.80, 0.10, 0.05, 0.05), "95-2-2-1": (0.95, 0.02, 0.02, 0.01)}
+
+
+def modality_runs(g, N: int, K: int, mean_run: float = 64.0, shares=None) -> torch.Tensor:
     """Per-position modality for N tokens laid out as runs of geometric length (mean
-    ``mean_run``, success probability 1/mean_run) with a uniformly drawn modality per run."""
+    ``mean_run``, success probability 1/mean_run) with one modality per run, drawn uniformly
+    or, when ``shares`` (K probabilities) is given, with those probabilities."""
     p = 1.0 / mean_run
     out = torch.empty(N, dtype=torch.int32)
     pos = 0
+    probs = None if shares is None else torch.tensor(shares, dtype=torch.float64)
     while pos < N:
         u = torch.rand(1, generator=g, dtype=torch.float64).item()
         length = 1 + int(math.floor(math.log1p(-u) / math.log1p(-p))) if u > 0 else 1
-        m = int(torch.randint(0, K, (1,), generator=g).item())
+        if probs is None:
+            m = int(torch.randint(0, K, (1,), generator=g).item())
+        else:
+            m = int(torch.multinomial(probs, 1, generator=g).item())
         out[pos:pos + length] = m
         pos += length
     return out
@@ -135,7 +145,12 @@ def make(name: str, seed: Optional[int] = None, *, N: Optional[int] = None, d_in
         d_out = d_out or d_in
         K, r, dt = K or 4, r or 16, dtype or torch.bfloat16
         starts = equal_vocab_starts(K)
-        tok = _tokens_in_ranges(g, modality_runs(g, N, K), starts)
+        shares = None
+        if dist != "uniform":
+            shares = SHARES[dist]
+            if len(shares) != K:
+                raise ValueError(f"dist {dist} needs K = {len(shares)}")
+        tok = _tokens_in_ranges(g, modality_runs(g, N, K, shares=shares), starts)
         x = _randn(g, (N, d_in), 1.0, dt)
         A, B = _adapters(g, K, d_in, d_out, r, dt)
         y0 = _randn(g, (N, d_out), 1.0, torch.float32)
