@@ -63,7 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew"], default="step",
+    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y"],
+                   default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     return p.parse_args(argv)
@@ -546,7 +547,9 @@ def run_mode(args):
                passes over all tokens against one per-token pass.
     skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
                80/10/5/5, 95/2/2/1 modality shares per run): the apply alone and the whole step,
-               back to back over six batches as in the main line."""
+               back to back over six batches as in the main line.
+    bf16y      the 4-modality workload with y held in bf16 (molora_lora_apply_bf16y), the apply
+               alone back to back over six batches, grouped and scalar paths."""
     import token_adapter_routing_gb300 as m
     from token_adapter_routing_gb300 import build as lib_build
     lib_build.build()
@@ -559,7 +562,49 @@ def run_mode(args):
     def emit(d):
         print(json.dumps(d), flush=True)
 
-    if args.mode == "skew":
+    if args.mode == "bf16y":
+        peaks, _ = measured_peaks()
+        wls = [workloads.make(WORKLOAD, seed=1234 + 1 + b) for b in range(N_BATCHES)]
+        starts, A, B = wls[0].starts.to(dev), wls[0].A.to(dev), wls[0].B.to(dev)
+        bs = []
+        for w_ in wls:
+            adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(w_.tok.to(dev), starts)
+            bs.append({"x": w_.x.to(dev), "y": w_.y0.to(torch.bfloat16).to(dev), "adapter": adapter,
+                       "counts": counts, "offsets": offsets, "perm": perm})
+        n = 120
+        for path in ("grouped", "scalar"):
+            def apply(i, path=path):
+                b = bs[i % N_BATCHES]
+                m.molora_lora_apply(b["x"], A, B, b["adapter"], b["y"], wls[0].scale, counts=b["counts"],
+                                    offsets=b["offsets"], perm=b["perm"], path=path)
+            with torch.cuda.stream(stream):
+                for i in range(N_BATCHES):
+                    apply(i)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        apply(i)
+                g.replay()
+                ts = []
+                for _ in range(5):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3 / n)
+            us = statistics.median(ts)
+            w0 = wls[0]
+            n_active = int((torch.bincount(bs[0]["adapter"].cpu().long(), minlength=w0.K) > 0).sum().item())
+            algo = (w0.N * w0.d_in * 2 + 2 * w0.N * w0.d_out * 2
+                    + n_active * (w0.d_in * w0.r + w0.r * w0.d_out) * 2 + 2 * w0.N * 4 + (w0.K + 1) * 4)
+            emit({"mode": "bf16y", "path": path, "workload": "N=2048, d=4096, K=4, r=16, y bf16",
+                  "apply_us": round(us, 3), "tokens_per_s": round(w0.N / (us * 1e-6), 1),
+                  "algorithmic_bytes": algo, "apply_GBps": round(algo / (us * 1e-6) / 1e9, 1),
+                  "frac_of_measured": round(algo / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                  "l2": f"inputs larger than L2 ({N_BATCHES} resident batches, back to back)"})
+    elif args.mode == "skew":
         peaks, _ = measured_peaks()
         for dist in ("uniform", "80-10-5-5", "95-2-2-1"):
             wls = [workloads.make(WORKLOAD, seed=1234 + 1 + b, dist=dist) for b in range(N_BATCHES)]

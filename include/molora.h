@@ -191,6 +191,24 @@ MOLORA_API molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype,
                                    molora_path path, cudaStream_t stream);
 
 /*
+ * molora_lora_apply_bf16y -- molora_lora_apply_ex with y held in bf16 (the output dtype a
+ * bf16 model keeps its activations in; the pages leave y's dtype open).  Same arguments,
+ * except y: bf16 [N x d_out], updated in place.
+ *
+ * Rounding: the contributions are formed in fp32 as in molora_lora_apply.  The scalar path
+ * adds a token's whole fp32 sum to y and rounds once to bf16 (nearest even).  The grouped
+ * path rounds each slot's contribution to bf16 and adds it into y with a bf16 bulk
+ * reduction in L2 (one more rounding per slot), so it may differ from the once-rounded
+ * result by about one bf16 unit in the last place per slot.
+ */
+MOLORA_API molora_status molora_lora_apply_bf16y(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                      int32_t d_out, const void* A, const void* B, int32_t K, int32_t r,
+                                      const int32_t* ids, const float* w, int32_t k,
+                                      const int32_t* counts, const int32_t* offsets,
+                                      const int32_t* perm, float scale, void* y, int32_t* err_word,
+                                      molora_path path, cudaStream_t stream);
+
+/*
  * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:
  * per-sequence routing needs K passes for a K-modality batch).  Adapter `a` is evaluated
  * for EVERY token; the result is multiplied by the 0/1 mask [adapter_of[t] == a]:

@@ -241,6 +241,98 @@ def test_apply_topk_weighted_vs_oracle(m, path, k):
     assert_apply_close(y, y_ref)
 
 
+# ------------------------------------------------------------------------- bf16 y
+
+def bf16_ulp(v):
+    """One bf16 unit in the last place at magnitude |v| (8 significant bits)."""
+    a = v.abs().double().clamp_min(2.0 ** -126)
+    return torch.exp2(torch.floor(torch.log2(a)) - 7)
+
+
+def assert_bf16y_close(y_gpu, y0_bf16, y_ref32, rounds, slot_updates=None):
+    """bf16 y against the oracle: the oracle's result rounded once to bf16 (nearest even),
+    allowing `rounds` bf16 units in the last place at the largest magnitude any partial sum
+    can reach: max(|result|, |y0|) plus the sum of the slots' |updates| (each rounding adds at
+    most half a unit at the magnitude of the value it rounds)."""
+    got = y_gpu.cpu().double()
+    ref = y_ref32.to(torch.bfloat16).double()
+    if slot_updates is None:
+        slot_updates = [y_ref32.double() - y0_bf16.double()]
+    mag = torch.maximum(ref.abs(), y0_bf16.double().abs()) + sum(u.double().abs() for u in slot_updates)
+    err = (got - ref).abs()
+    tol = rounds * bf16_ulp(mag)
+    bad = err > tol
+    assert not bool(bad.any()), f"{int(bad.sum())} elements beyond {rounds} bf16 ulp; worst {err.max().item():.3e}"
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("k", [1, 2])
+def test_apply_bf16y_small_integers_bitexact(m, path, k):
+    # every value and partial sum is a small integer, exact in fp32 and in bf16: each column
+    # of A_a has two entries of +-1, B in {-1, 0, 1}, so |h| <= 6, |update| <= 96 per slot
+    N, d_in, d_out, K, r = 200, 256, 384, 4, 16
+    g = torch.Generator().manual_seed(71 + k)
+    x = torch.randint(-3, 4, (N, d_in), generator=g).to(torch.bfloat16)
+    A = torch.zeros(K, d_in, r)
+    for a in range(K):
+        for q in range(r):
+            rows = torch.randperm(d_in, generator=g)[:2]
+            A[a, rows, q] = torch.where(torch.rand(2, generator=g) < 0.5, -1.0, 1.0)
+    A = A.to(torch.bfloat16)
+    B = torch.randint(-1, 2, (K, r, d_out), generator=g).to(torch.bfloat16)
+    y0b = torch.randint(-8, 9, (N, d_out), generator=g).to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(K, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.ones(N, k)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), 4)
+    y = dev(y0b).clone()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 1.0, w=dev(w), counts=counts, offsets=offsets,
+                        perm=perm, path=path)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0b.float(), 1.0, w)
+    assert y_ref.abs().max().item() < 256
+    assert torch.equal(y.cpu(), y_ref.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name,kw", [("modality4", {}), ("modality4", {"N": 1000, "d_in": 1024, "d_out": 3072})])
+def test_apply_bf16y_vocab_routed_vs_oracle(m, path, name, kw):
+    wl = workloads.make(name, **kw)
+    y0b = wl.y0.to(torch.bfloat16)
+    e = err_word()
+    adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(dev(wl.tok), dev(wl.starts), err_word=e)
+    y = dev(y0b).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), adapter, y, wl.scale, counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), y0b.float(), wl.scale)
+    # scalar: one rounding of the fp32 sum; grouped: the slot's contribution and the sum
+    assert_bf16y_close(y, y0b, y_ref, 1 if path == "scalar" else 2)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_apply_bf16y_topk_weighted_vs_oracle(m, path):
+    k = 2
+    wl = workloads.make("topk_scaling", N=600, d_in=1024, d_out=1536, k=k)
+    g = torch.Generator().manual_seed(7)
+    ids = torch.stack([torch.randperm(wl.K, generator=g)[:k] for _ in range(wl.N)]).to(torch.int32)
+    w = torch.softmax(torch.randn(wl.N, k, generator=g), dim=1)
+    y0b = wl.y0.to(torch.bfloat16)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K)
+    y = dev(y0b).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(ids), y, wl.scale, w=dev(w), counts=counts,
+                        offsets=offsets, perm=perm, path=path)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, y0b.float(), wl.scale, w)
+    # each slot's own update (the other slot's id set to -1, which the oracle skips)
+    parts = []
+    for j in range(k):
+        ids_j = ids.clone()
+        ids_j[:, [i for i in range(k) if i != j]] = -1
+        parts.append(oracle.lora_apply(wl.x, wl.A, wl.B, ids_j, torch.zeros_like(wl.y0), wl.scale, w)[0])
+    assert_bf16y_close(y, y0b, y_ref, 1 if path == "scalar" else 1 + k, parts)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_apply_degenerate_cases(m, path):
     wl = workloads.make("modality4", N=300, d_in=512, d_out=512)

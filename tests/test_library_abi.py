@@ -97,6 +97,15 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert apply(dtype=0, path=2) == UNSUPPORTED
     assert apply(r=8, path=2) == UNSUPPORTED
     assert apply(N=0) == 0
+    # bf16 y: the same checks through the bf16-y entry point
+    lib.molora_lora_apply_bf16y.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
+
+    def apply16(y=fake, r=16, path=0):
+        return lib.molora_lora_apply_bf16y(fake, 1, 16, 64, 64, fake, fake, 4, r, fake, None, 1, fake, fake, fake,
+                                           2.0, y, None, path, None)
+
+    assert apply16(y=None) == INVALID and apply16(y=odd) == INVALID and apply16(r=12) == INVALID
+    assert apply16(r=8, path=2) == UNSUPPORTED
     # router: k > K, K > 64, null outputs
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 5, None, fake, fake, None) == INVALID
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 65, 1, None, fake, fake, None) == INVALID

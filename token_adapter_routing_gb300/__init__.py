@@ -44,7 +44,7 @@ ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
             "molora_lora_apply",
-            "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path",
+            "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_masked_pass", "molora_select_path",
             "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
 
@@ -77,6 +77,7 @@ def load_library():
     lib.molora_route_vocab_dispatch.argtypes = [P, I64, P, I32, P, P, P, P, P, P]
     lib.molora_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P]
     lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
+    lib.molora_lora_apply_bf16y.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
     lib.molora_status_string.argtypes = [S]
@@ -84,8 +85,8 @@ def load_library():
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_lora_apply",
-                 "molora_lora_apply_ex", "molora_lora_apply_masked_pass", "molora_select_path", "molora_version",
+                 "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y",
+                 "molora_lora_apply_masked_pass", "molora_select_path", "molora_version",
                  "molora_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -209,7 +210,8 @@ def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=
 
 def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None, perm=None, err_word=None,
                       path="auto", stream=None):
-    """y[t] += scale * sum_j w[t,j] (x[t] A_{ids[t,j]}) B_{ids[t,j]}, in place on y (fp32)."""
+    """y[t] += scale * sum_j w[t,j] (x[t] A_{ids[t,j]}) B_{ids[t,j]}, in place on y (fp32, or bf16
+    through molora_lora_apply_bf16y)."""
     _cuda(x, "x", None, 2)
     N, d_in = x.shape
     _cuda(A, "A", x.dtype, 3)
@@ -220,13 +222,17 @@ def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None,
         raise ValueError("A must be [K, d_in, r] and B [K, r, d_out]")
     _cuda(ids, "ids", torch.int32)
     k = 1 if ids.dim() == 1 else ids.shape[1]
-    _cuda(y, "y", torch.float32, 2)
+    _cuda(y, "y", None, 2)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"y must be float32 or bfloat16, got {y.dtype}")
     if w is not None:
         _cuda(w, "w", torch.float32)
     for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm)):
         if t is not None:
             _cuda(t, name, torch.int32)
-    _check("molora_lora_apply", load_library().molora_lora_apply_ex(
+    lib = load_library()
+    fn = lib.molora_lora_apply_bf16y if y.dtype == torch.bfloat16 else lib.molora_lora_apply_ex
+    _check("molora_lora_apply", fn(
         _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(ids), _p(w), k, _p(counts), _p(offsets),
         _p(perm), float(scale), _p(y), _p(err_word), PATHS[path], _stream(stream)))
     return y

@@ -37,7 +37,7 @@ static int64_t crossover_tokens(int32_t K) {
 
 static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                       const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
-                                      int32_t k, const float* y) {
+                                      int32_t k, const void* y) {
   if (!valid_dtype(dtype) || N < 0 || d_in < 1 || d_out < 1 || K < 1 || K > kMaxAdapters || k < 1 || k > K)
     return MOLORA_ERR_INVALID_ARG;
   if (!(r == 8 || r == 16 || r == 32 || r == 64)) return MOLORA_ERR_INVALID_ARG;
@@ -46,6 +46,24 @@ static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t
   if (!x || !A || !B || !ids || !y) return MOLORA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y)) return MOLORA_ERR_INVALID_ARG;
   return MOLORA_OK;
+}
+
+static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
+                                int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                                float scale, void* y, bool y_bf16, int32_t* err_word, molora_path path,
+                                cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+  if (st != MOLORA_OK || N == 0) return st;
+  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+  if (path == MOLORA_PATH_SCALAR)
+    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, -1,
+                                       err_word, stream));
+  if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
+  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !perm) return MOLORA_ERR_INVALID_ARG;
+  return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y,
+                                      y_bf16, -1, err_word, stream));
 }
 
 }  // namespace molora
@@ -104,17 +122,17 @@ molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype, int64_t N,
                                    const float* w, int32_t k, const int32_t* counts, const int32_t* offsets,
                                    const int32_t* perm, float scale, float* y, int32_t* err_word, molora_path path,
                                    cudaStream_t stream) {
-  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
-  if (st != MOLORA_OK || N == 0) return st;
-  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
-  if (path == MOLORA_PATH_SCALAR)
-    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, -1, err_word,
-                                       stream));
-  if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
-  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_ERR_UNSUPPORTED;
-  if (!counts || !offsets || !perm) return MOLORA_ERR_INVALID_ARG;
-  return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, -1,
-                                      err_word, stream));
+  return molora::apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, false,
+                            err_word, path, stream);
+}
+
+molora_status molora_lora_apply_bf16y(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                      const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                                      const float* w, int32_t k, const int32_t* counts, const int32_t* offsets,
+                                      const int32_t* perm, float scale, void* y, int32_t* err_word,
+                                      molora_path path, cudaStream_t stream) {
+  return molora::apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, true,
+                            err_word, path, stream);
 }
 
 molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
@@ -135,12 +153,12 @@ molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, i
   if (N == 0) return MOLORA_OK;
   if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, 1);
   if (path == MOLORA_PATH_SCALAR)
-    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, scale, y, a,
-                                       err_word, stream));
+    return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, scale, y, false,
+                                       a, err_word, stream));
   if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, 1)) return MOLORA_ERR_UNSUPPORTED;
   return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, nullptr, nullptr,
-                                      nullptr, scale, y, a, err_word, stream));
+                                      nullptr, scale, y, false, a, err_word, stream));
 }
 
 const char* molora_status_string(molora_status status) {

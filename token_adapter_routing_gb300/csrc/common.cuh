@@ -99,6 +99,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, 
                "r"(ssrc), "r"(bytes)
                : "memory");
 }
+// The same for bf16 elements: each destination element becomes the bf16 sum of itself and
+// the staged bf16 value.
+__device__ __forceinline__ void bulk_reduce_add_bf16(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.noftz.bf16 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
 // *gdst += v, four consecutive fp32, as one L2 reduction (no value returned).
 __device__ __forceinline__ void red_add_v4(float* gdst, float4 v) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)

@@ -24,7 +24,7 @@ cudaError_t launch_route_vocab_dispatch(const int32_t* tok, int64_t N, const int
 // adapter mask_adapter for every token, weight [ids[t] == mask_adapter] (k must be 1).
 cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
-                               const float* w, int32_t k, float scale, float* y, int32_t mask_adapter,
+                               const float* w, int32_t k, float scale, void* y, bool y_bf16, int32_t mask_adapter,
                                int32_t* err_word, cudaStream_t stream);
 
 // CUDA-core learned router (any dtype / shape).
@@ -41,7 +41,7 @@ bool grouped_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_ou
 cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
                                 const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
-                                float scale, float* y, int32_t mask_adapter, int32_t* err_word,
+                                float scale, void* y, bool y_bf16, int32_t mask_adapter, int32_t* err_word,
                                 cudaStream_t stream);
 
 // tcgen05 learned router: true if this shape is supported.

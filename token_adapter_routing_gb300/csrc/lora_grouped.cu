@@ -205,7 +205,8 @@ __global__ void __maxnreg__(168)
     lora_grouped_kernel(const __nv_bfloat16* __restrict__ x, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
                         int32_t r, int32_t k, const int32_t* __restrict__ ids, const float* __restrict__ w,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, float scale,
-                        float* __restrict__ y, int32_t mask_adapter, const GroupedPlan P, int32_t* err_word,
+                        void* __restrict__ y, int32_t y_bf16, int32_t mask_adapter, const GroupedPlan P,
+                        int32_t* err_word,
                         const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,6 +214,8 @@ __global__ void __maxnreg__(168)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = P.C, KS = P.KS, NC = P.NC, TM = P.TM;
+  uint8_t* const yb = static_cast<uint8_t*>(y);
+  const uint32_t ysz = y_bf16 ? 2u : 4u;  // bytes per y element: fp32, or bf16
   const int crank = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x / C;
   const int64_t S = N * (int64_t)k;
@@ -461,7 +464,7 @@ __global__ void __maxnreg__(168)
     // segment into L2, so the reductions of the expand find it there.  Earlier, the prefetch
     // competed with the x gather and slowed it more than it helped.
     if (P.prefetch_y && ctrl->tok[tid] >= 0)
-      prefetch_l2_bulk(y + (int64_t)ctrl->tok[tid] * d_out + crank * NC, (uint32_t)NC * 4u);
+      prefetch_l2_bulk(yb + ((int64_t)ctrl->tok[tid] * d_out + crank * NC) * ysz, (uint32_t)NC * ysz);
     have_h = mbar_wait(last_bar, last_parity);
     tc_fence_after();
     if (!have_h) {
@@ -582,16 +585,35 @@ __global__ void __maxnreg__(168)
         for (int c0 = 0; c0 < cols; c0 += 32) {
           float v[32];
           tmem_ld32(lane_base + buf * P.PW + q + c0, v);
-          float4* dst = reinterpret_cast<float4*>(srow + c0);
-          if (my_tok >= 0)
+          if (my_tok >= 0) {
+            if (y_bf16) {
+              // round each contribution to bf16 (nearest even); the bulk add rounds the sum
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(srow) + c0 * 2);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) {
+                uint32_t u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
+                  u[j] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                dst[i] = make_uint4(u[0], u[1], u[2], u[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(srow + c0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+          }
         }
         // one bulk reduction per row segment, performed by the TMA unit in L2
         fence_proxy_async_smem();
         if (my_tok >= 0) {
-          bulk_reduce_add_f32(y + (int64_t)my_tok * d_out + crank * NC + p * P.PW + q, smem_u32(srow),
-                              (uint32_t)cols * 4u);
+          void* dst = yb + ((int64_t)my_tok * d_out + crank * NC + p * P.PW + q) * ysz;
+          if (y_bf16)
+            bulk_reduce_add_bf16(dst, smem_u32(srow), (uint32_t)cols * 2u);
+          else
+            bulk_reduce_add_f32(static_cast<float*>(dst), smem_u32(srow), (uint32_t)cols * 4u);
           bulk_commit();
         }
       }
@@ -653,7 +675,8 @@ bool grouped_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_ou
 cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
                                 int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k,
                                 const int32_t* counts, const int32_t* offsets, const int32_t* perm, float scale,
-                                float* y, int32_t mask_adapter, int32_t* err_word, cudaStream_t stream) {
+                                void* y, bool y_bf16, int32_t mask_adapter, int32_t* err_word,
+                                cudaStream_t stream) {
   (void)counts;
   GroupedPlan s;
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
@@ -662,7 +685,7 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   // DRAM idles for about 2 us while the tile is decoded; prefetching 40% of y (at most
   // 16 MiB) fills that window and measured best on GB300 (4-modality workload, back-to-back
   // steps: 0, 25, 33, 40, 50 and 60% tried).  The rest of y follows per row, late.
-  const uint64_t y_bytes = (uint64_t)N * d_out * 4u;
+  const uint64_t y_bytes = (uint64_t)N * d_out * (y_bf16 ? 2u : 4u);
   const uint64_t early = y_bytes * 2u / 5u;
   s.early_y = (early < (16ull << 20) ? early : (16ull << 20)) & ~uint64_t(15);
 #ifdef MOLORA_TUNING_ENV
@@ -689,7 +712,7 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   const int64_t tiles = mask_adapter >= 0 ? (N + s.TM - 1) / s.TM : (N * k + s.TM - 1) / s.TM + K;
   return launch_kernel(lora_grouped_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C,
                        static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r, k, ids, w, offsets, perm, scale, y,
-                       mask_adapter, s, err_word, map_a, map_b);
+                       (int32_t)(y_bf16 ? 1 : 0), mask_adapter, s, err_word, map_a, map_b);
 }
 
 }  // namespace molora

@@ -50,17 +50,38 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 
 constexpr int kScalarThreads = 256;
 
+// y element access: fp32, or bf16 (the fp32 sum rounded to nearest even once per update).
+__device__ __forceinline__ void y_add4(float* p, const float (&a)[4]) {
+  float4 v = *reinterpret_cast<float4*>(p);
+  v.x += a[0], v.y += a[1], v.z += a[2], v.w += a[3];
+  *reinterpret_cast<float4*>(p) = v;
+}
+__device__ __forceinline__ void y_add4(__nv_bfloat16* p, const float (&a)[4]) {
+  uint2 q = *reinterpret_cast<uint2*>(p);
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(__uint_as_float(q.x << 16) + a[0],
+                                                  __uint_as_float(q.x & 0xFFFF0000u) + a[1]);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(__uint_as_float(q.y << 16) + a[2],
+                                                  __uint_as_float(q.y & 0xFFFF0000u) + a[3]);
+  q.x = *reinterpret_cast<const uint32_t*>(&lo);
+  q.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+__device__ __forceinline__ void y_add1(float* p, float a) { *p += a; }
+__device__ __forceinline__ void y_add1(__nv_bfloat16* p, float a) {
+  *p = __float2bfloat16_rn(__bfloat162float(*p) + a);
+}
+
 // One CTA per (token, column split).  Phase 1: for each of the token's k slots the CTA
 // reduces h = x[t] A_a over d_in (each thread streams 16-byte chunks of A_a, which is
 // row-major [d_in x R], so a warp reads 512 contiguous bytes per step) and stores
 // g_j = scale * w_j * h.  Phase 2: each thread owns 4 output columns and accumulates
 // sum_j sum_q g_j[q] B_a[q, c..c+3] in registers, then updates y once.  Every y element is
 // read and written exactly once whatever k is, so the result is deterministic.
-template <typename T, int R>
+template <typename T, typename YT, int R>
 __global__ void __launch_bounds__(kScalarThreads)
     lora_scalar_kernel(const T* __restrict__ x, int32_t d_in, int32_t d_out, const T* __restrict__ A,
                        const T* __restrict__ B, int32_t K, const int32_t* __restrict__ ids,
-                       const float* __restrict__ w, int32_t k, float scale, float* __restrict__ y,
+                       const float* __restrict__ w, int32_t k, float scale, YT* __restrict__ y,
                        int32_t cols_per_split, int32_t mask_adapter, int32_t* err_word) {
   using C16 = Chunk16<T>;
   constexpr int VEC = C16::kVec;
@@ -130,7 +151,7 @@ __global__ void __launch_bounds__(kScalarThreads)
 
   const int32_t c_begin = blockIdx.y * cols_per_split;
   const int32_t c_end = min(d_out, c_begin + cols_per_split);
-  float* yr = y + t * (int64_t)d_out;
+  YT* yr = y + t * (int64_t)d_out;
   if ((d_out & 3) == 0) {
     for (int32_t c = c_begin + 4 * tid; c < c_end; c += 4 * kScalarThreads) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -148,9 +169,7 @@ __global__ void __launch_bounds__(kScalarThreads)
           for (int v = 0; v < 4; ++v) acc[v] = fmaf(gq, b[v], acc[v]);
         }
       }
-      float4 yv = *reinterpret_cast<float4*>(yr + c);
-      yv.x += acc[0], yv.y += acc[1], yv.z += acc[2], yv.w += acc[3];
-      *reinterpret_cast<float4*>(yr + c) = yv;
+      y_add4(yr + c, acc);
     }
   } else {
     for (int32_t c = c_begin + tid; c < c_end; c += kScalarThreads) {
@@ -161,15 +180,15 @@ __global__ void __launch_bounds__(kScalarThreads)
         const T* Bq = B + (int64_t)a * R * d_out + c;
         for (int q = 0; q < R; ++q) acc = fmaf(g[j * R + q], to_f(Bq[(int64_t)q * d_out]), acc);
       }
-      yr[c] += acc;
+      y_add1(yr + c, acc);
     }
   }
 }
 
-template <typename T>
+template <typename T, typename YT>
 static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
                                    const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
-                                   int32_t k, float scale, float* y, int32_t mask_adapter, int32_t* err_word,
+                                   int32_t k, float scale, void* y, int32_t mask_adapter, int32_t* err_word,
                                    cudaStream_t stream) {
   // Enough CTAs to cover the GPU twice: small batches split the output columns (each split
   // recomputes the token's cheap shrink).
@@ -185,23 +204,20 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
   const T* xp = static_cast<const T*>(x);
   const T* Ap = static_cast<const T*>(A);
   const T* Bp = static_cast<const T*>(B);
+  YT* yp = static_cast<YT*>(y);
   switch (r) {
     case 8:
-      return launch_kernel(lora_scalar_kernel<T, 8>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
-                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
-      break;
+      return launch_kernel(lora_scalar_kernel<T, YT, 8>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
     case 16:
-      return launch_kernel(lora_scalar_kernel<T, 16>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
-                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
-      break;
+      return launch_kernel(lora_scalar_kernel<T, YT, 16>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
     case 32:
-      return launch_kernel(lora_scalar_kernel<T, 32>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
-                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
-      break;
+      return launch_kernel(lora_scalar_kernel<T, YT, 32>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
     case 64:
-      return launch_kernel(lora_scalar_kernel<T, 64>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in, d_out, Ap,
-                           Bp, K, ids, w, k, scale, y, cols, mask_adapter, err_word);
-      break;
+      return launch_kernel(lora_scalar_kernel<T, YT, 64>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
     default:
       return cudaErrorInvalidValue;
   }
@@ -209,13 +225,17 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
 
 cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
-                               const float* w, int32_t k, float scale, float* y, int32_t mask_adapter,
+                               const float* w, int32_t k, float scale, void* y, bool y_bf16, int32_t mask_adapter,
                                int32_t* err_word, cudaStream_t stream) {
   if (dtype == MOLORA_BF16)
-    return launch_scalar_t<__nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter,
-                                          err_word, stream);
-  return launch_scalar_t<float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter, err_word,
-                                stream);
+    return y_bf16 ? launch_scalar_t<__nv_bfloat16, __nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
+                                                                   mask_adapter, err_word, stream)
+                  : launch_scalar_t<__nv_bfloat16, float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
+                                                          mask_adapter, err_word, stream);
+  return y_bf16 ? launch_scalar_t<float, __nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
+                                                         mask_adapter, err_word, stream)
+                : launch_scalar_t<float, float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter,
+                                                err_word, stream);
 }
 
 // ---------------------------------------------------------------------------------------
