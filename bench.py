@@ -63,7 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y"],
+    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y", "indirect"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
@@ -549,7 +549,10 @@ def run_mode(args):
                80/10/5/5, 95/2/2/1 modality shares per run): the apply alone and the whole step,
                back to back over six batches as in the main line.
     bf16y      the 4-modality workload with y held in bf16 (molora_lora_apply_bf16y), the apply
-               alone back to back over six batches, grouped and scalar paths."""
+               alone back to back over six batches, grouped and scalar paths.
+    indirect   Table 2: the hot set as two slabs (direct) against K separately allocated
+               adapters (indirect, molora_lora_apply_indirect), N=2048, d=4096, r=16, top-1,
+               uniform adapters, K = 4, 16, 64; the apply alone back to back over six batches."""
     import token_adapter_routing_gb300 as m
     from token_adapter_routing_gb300 import build as lib_build
     lib_build.build()
@@ -562,7 +565,46 @@ def run_mode(args):
     def emit(d):
         print(json.dumps(d), flush=True)
 
-    if args.mode == "bf16y":
+    if args.mode == "indirect":
+        for K in (4, 16, 64):
+            wls = [workloads.make("decode_sweep", seed=4000 + b, N=2048, K=K) for b in range(N_BATCHES)]
+            starts, A, B = wls[0].starts.to(dev), wls[0].A.to(dev), wls[0].B.to(dev)
+            A_list = [A[i].clone() for i in range(K)]
+            B_list = [B[i].clone() for i in range(K)]
+            bs = []
+            for w_ in wls:
+                adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(w_.tok.to(dev), starts)
+                bs.append({"x": w_.x.to(dev), "y": w_.y0.to(dev), "adapter": adapter, "counts": counts,
+                           "offsets": offsets, "perm": perm})
+            row = {"mode": "indirect", "workload": f"N=2048, d=4096, K={K}, r=16, top-1 uniform",
+                   "path": m.molora_select_path(torch.bfloat16, 2048, 4096, 4096, K, 16, 1)}
+            for layout, (AA, BB) in (("direct", (A, B)), ("indirect", (A_list, B_list))):
+                def apply(i, AA=AA, BB=BB):
+                    b = bs[i % N_BATCHES]
+                    m.molora_lora_apply(b["x"], AA, BB, b["adapter"], b["y"], wls[0].scale, counts=b["counts"],
+                                        offsets=b["offsets"], perm=b["perm"])
+                n = 120
+                with torch.cuda.stream(stream):
+                    for i in range(N_BATCHES):
+                        apply(i)
+                    stream.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(n):
+                            apply(i)
+                    g.replay()
+                    ts = []
+                    for _ in range(5):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        stream.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e3 / n)
+                row[f"{layout}_us"] = round(statistics.median(ts), 3)
+            row["indirect_over_direct"] = round(row["indirect_us"] / row["direct_us"], 3)
+            emit(row)
+    elif args.mode == "bf16y":
         peaks, _ = measured_peaks()
         wls = [workloads.make(WORKLOAD, seed=1234 + 1 + b) for b in range(N_BATCHES)]
         starts, A, B = wls[0].starts.to(dev), wls[0].A.to(dev), wls[0].B.to(dev)

@@ -209,6 +209,26 @@ MOLORA_API molora_status molora_lora_apply_bf16y(const void* x, molora_dtype dty
                                       molora_path path, cudaStream_t stream);
 
 /*
+ * molora_lora_apply_indirect -- the apply with the hot set given adapter by adapter
+ * instead of as two contiguous slabs (Table 2: indirect, pointer-array adapter addressing).
+ *
+ * A_ptrs[i]  device address of adapter i's A, [d_in x r] of dtype, row-major, 16-byte aligned
+ * B_ptrs[i]  device address of adapter i's B, [r x d_out], 16-byte aligned
+ * A_ptrs and B_ptrs are HOST arrays of K entries.  Their values are read when the call is
+ * made (a CUDA graph captures them by value), so the adapters must stay at those addresses
+ * while enqueued work and captured graphs use them.  y is fp32 (y_bf16 = 0) or bf16
+ * (y_bf16 = 1, rounding as molora_lora_apply_bf16y).  Every other argument, the path choice
+ * and the results are those of molora_lora_apply_ex on the same adapters held in slabs.
+ */
+MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype dtype, int64_t N,
+                                         int32_t d_in, int32_t d_out, const void* const* A_ptrs,
+                                         const void* const* B_ptrs, int32_t K, int32_t r,
+                                         const int32_t* ids, const float* w, int32_t k,
+                                         const int32_t* counts, const int32_t* offsets,
+                                         const int32_t* perm, float scale, void* y, int32_t y_bf16,
+                                         int32_t* err_word, molora_path path, cudaStream_t stream);
+
+/*
  * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:
  * per-sequence routing needs K passes for a K-modality batch).  Adapter `a` is evaluated
  * for EVERY token; the result is multiplied by the 0/1 mask [adapter_of[t] == a]:

@@ -333,6 +333,66 @@ def test_apply_bf16y_topk_weighted_vs_oracle(m, path):
     assert_bf16y_close(y, y0b, y_ref, 1 if path == "scalar" else 1 + k, parts)
 
 
+# ------------------------------------------------------------------------- indirect layout
+
+def separate_adapters(wl):
+    """The hot set as K separately allocated tensors per side (no common slab)."""
+    A_list = [dev(wl.A[i]).clone() for i in range(wl.K)]
+    B_list = [dev(wl.B[i]).clone() for i in range(wl.K)]
+    return A_list, B_list
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name,kw", [("modality4", {}), ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048,
+                                                                       "r": 64, "K": 8}),
+                                     ("modality4", {"N": 333, "d_in": 2048, "d_out": 1024, "r": 32}),
+                                     ("decode_sweep", {"N": 160, "K": 64})])
+def test_apply_indirect_equals_slab(m, path, name, kw):
+    # same arithmetic in the same order: the indirect layout must match the slab bit for bit
+    wl = workloads.make(name, **kw)
+    adapter, counts, offsets, perm = m.molora_route_vocab_dispatch(dev(wl.tok), dev(wl.starts))
+    A_list, B_list = separate_adapters(wl)
+    y_slab, y_ind = dev(wl.y0).clone(), dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), adapter, y_slab, wl.scale, counts=counts, offsets=offsets,
+                        perm=perm, path=path)
+    m.molora_lora_apply(dev(wl.x), A_list, B_list, adapter, y_ind, wl.scale, counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(y_ind.cpu(), y_slab.cpu())
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    assert_apply_close(y_ind, y_ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_apply_indirect_topk_and_bf16y(m, path):
+    k = 2
+    wl = workloads.make("topk_scaling", N=600, d_in=1024, d_out=1536, k=k)
+    g = torch.Generator().manual_seed(13)
+    ids = torch.stack([torch.randperm(wl.K, generator=g)[:k] for _ in range(wl.N)]).to(torch.int32)
+    w = torch.softmax(torch.randn(wl.N, k, generator=g), dim=1)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K)
+    A_list, B_list = separate_adapters(wl)
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), A_list, B_list, dev(ids), y, wl.scale, w=dev(w), counts=counts,
+                        offsets=offsets, perm=perm, path=path)
+    y0b = wl.y0.to(torch.bfloat16)
+    yb = dev(y0b).clone()
+    m.molora_lora_apply(dev(wl.x), A_list, B_list, dev(ids), yb, wl.scale, w=dev(w), counts=counts,
+                        offsets=offsets, perm=perm, path=path)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, wl.y0, wl.scale, w)
+    assert_apply_close(y, y_ref)
+    yb_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, y0b.float(), wl.scale, w)
+    parts = []
+    for j in range(k):
+        ids_j = ids.clone()
+        ids_j[:, [i for i in range(k) if i != j]] = -1
+        parts.append(oracle.lora_apply(wl.x, wl.A, wl.B, ids_j, torch.zeros_like(wl.y0), wl.scale, w)[0])
+    assert_bf16y_close(yb, y0b, yb_ref, 1 if path == "scalar" else 1 + k, parts)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_apply_degenerate_cases(m, path):
     wl = workloads.make("modality4", N=300, d_in=512, d_out=512)

@@ -106,6 +106,21 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
 
     assert apply16(y=None) == INVALID and apply16(y=odd) == INVALID and apply16(r=12) == INVALID
     assert apply16(r=8, path=2) == UNSUPPORTED
+    # indirect layout: per-adapter address tables; a null or unaligned entry is rejected
+    lib.molora_lora_apply_indirect.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P,
+                                               I32, P, S, P]
+    good = (ctypes.c_void_p * 4)(0x10000, 0x20000, 0x30000, 0x40000)
+    with_null = (ctypes.c_void_p * 4)(0x10000, None, 0x30000, 0x40000)
+    with_odd = (ctypes.c_void_p * 4)(0x10000, 0x20008, 0x30000, 0x40000)
+
+    def ind(a_tab, b_tab, K=4):
+        return lib.molora_lora_apply_indirect(fake, 1, 16, 64, 64, ctypes.cast(a_tab, P), ctypes.cast(b_tab, P), K,
+                                              16, fake, None, 1, fake, fake, fake, 2.0, fake, 0, None, 0, None)
+
+    assert ind(with_null, good) == INVALID and ind(good, with_odd) == INVALID
+    assert ind(good, good, K=0) == INVALID and ind(good, good, K=65) == INVALID
+    assert lib.molora_lora_apply_indirect(fake, 1, 16, 64, 64, None, ctypes.cast(good, P), 4, 16, fake, None, 1,
+                                          fake, fake, fake, 2.0, fake, 0, None, 0, None) == INVALID
     # router: k > K, K > 64, null outputs
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 5, None, fake, fake, None) == INVALID
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 65, 1, None, fake, fake, None) == INVALID

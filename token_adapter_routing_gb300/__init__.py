@@ -44,7 +44,7 @@ ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
             "molora_lora_apply",
-            "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_masked_pass", "molora_select_path",
+            "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect", "molora_lora_apply_masked_pass", "molora_select_path",
             "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
 
@@ -78,6 +78,8 @@ def load_library():
     lib.molora_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P]
     lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
     lib.molora_lora_apply_bf16y.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
+    lib.molora_lora_apply_indirect.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, I32,
+                                               P, S, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
     lib.molora_status_string.argtypes = [S]
@@ -85,7 +87,7 @@ def load_library():
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y",
+                 "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
                  "molora_lora_apply_masked_pass", "molora_select_path", "molora_version",
                  "molora_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
@@ -211,15 +213,28 @@ def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=
 def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None, perm=None, err_word=None,
                       path="auto", stream=None):
     """y[t] += scale * sum_j w[t,j] (x[t] A_{ids[t,j]}) B_{ids[t,j]}, in place on y (fp32, or bf16
-    through molora_lora_apply_bf16y)."""
+    through molora_lora_apply_bf16y).  A and B are the hot-set slabs [K, d_in, r] and
+    [K, r, d_out], or lists of K per-adapter tensors [d_in, r] and [r, d_out] (the indirect
+    layout, molora_lora_apply_indirect)."""
     _cuda(x, "x", None, 2)
     N, d_in = x.shape
-    _cuda(A, "A", x.dtype, 3)
-    _cuda(B, "B", x.dtype, 3)
-    K, _, r = A.shape
-    d_out = B.shape[2]
-    if A.shape[1] != d_in or B.shape[:2] != (K, r):
-        raise ValueError("A must be [K, d_in, r] and B [K, r, d_out]")
+    indirect = isinstance(A, (list, tuple))
+    if indirect:
+        if not isinstance(B, (list, tuple)) or len(A) != len(B) or not A:
+            raise ValueError("indirect layout: A and B must be lists of the same nonzero length")
+        for i, (a_i, b_i) in enumerate(zip(A, B)):
+            _cuda(a_i, f"A[{i}]", x.dtype, 2)
+            _cuda(b_i, f"B[{i}]", x.dtype, 2)
+        K, r, d_out = len(A), A[0].shape[1], B[0].shape[1]
+        if any(a_i.shape != (d_in, r) for a_i in A) or any(b_i.shape != (r, d_out) for b_i in B):
+            raise ValueError("indirect layout: every A[i] must be [d_in, r] and every B[i] [r, d_out]")
+    else:
+        _cuda(A, "A", x.dtype, 3)
+        _cuda(B, "B", x.dtype, 3)
+        K, _, r = A.shape
+        d_out = B.shape[2]
+        if A.shape[1] != d_in or B.shape[:2] != (K, r):
+            raise ValueError("A must be [K, d_in, r] and B [K, r, d_out]")
     _cuda(ids, "ids", torch.int32)
     k = 1 if ids.dim() == 1 else ids.shape[1]
     _cuda(y, "y", None, 2)
@@ -231,6 +246,14 @@ def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None,
         if t is not None:
             _cuda(t, name, torch.int32)
     lib = load_library()
+    if indirect:
+        a_ptrs = (ctypes.c_void_p * K)(*[t.data_ptr() for t in A])
+        b_ptrs = (ctypes.c_void_p * K)(*[t.data_ptr() for t in B])
+        _check("molora_lora_apply", lib.molora_lora_apply_indirect(
+            _p(x), _dtype_code(x), N, d_in, d_out, ctypes.cast(a_ptrs, ctypes.c_void_p),
+            ctypes.cast(b_ptrs, ctypes.c_void_p), K, r, _p(ids), _p(w), k, _p(counts), _p(offsets), _p(perm),
+            float(scale), _p(y), 1 if y.dtype == torch.bfloat16 else 0, _p(err_word), PATHS[path], _stream(stream)))
+        return y
     fn = lib.molora_lora_apply_bf16y if y.dtype == torch.bfloat16 else lib.molora_lora_apply_ex
     _check("molora_lora_apply", fn(
         _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(ids), _p(w), k, _p(counts), _p(offsets),

@@ -52,18 +52,18 @@ static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, in
                                 const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
                                 float scale, void* y, bool y_bf16, int32_t* err_word, molora_path path,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const AdapterTable* table = nullptr) {
   const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
   if (st != MOLORA_OK || N == 0) return st;
   if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
   if (path == MOLORA_PATH_SCALAR)
     return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, -1,
-                                       err_word, stream));
+                                       err_word, stream, table));
   if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_ERR_UNSUPPORTED;
   if (!counts || !offsets || !perm) return MOLORA_ERR_INVALID_ARG;
   return launched(launch_lora_grouped(x, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y,
-                                      y_bf16, -1, err_word, stream));
+                                      y_bf16, -1, err_word, stream, table));
 }
 
 }  // namespace molora
@@ -133,6 +133,23 @@ molora_status molora_lora_apply_bf16y(const void* x, molora_dtype dtype, int64_t
                                       molora_path path, cudaStream_t stream) {
   return molora::apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, true,
                             err_word, path, stream);
+}
+
+molora_status molora_lora_apply_indirect(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                         const void* const* A_ptrs, const void* const* B_ptrs, int32_t K, int32_t r,
+                                         const int32_t* ids, const float* w, int32_t k, const int32_t* counts,
+                                         const int32_t* offsets, const int32_t* perm, float scale, void* y,
+                                         int32_t y_bf16, int32_t* err_word, molora_path path, cudaStream_t stream) {
+  if (!A_ptrs || !B_ptrs || K < 1 || K > kMaxAdapters) return MOLORA_ERR_INVALID_ARG;
+  molora::AdapterTable table;
+  for (int i = 0; i < kMaxAdapters; ++i) table.a[i] = table.b[i] = nullptr;
+  for (int32_t i = 0; i < K; ++i) {
+    if (!A_ptrs[i] || !B_ptrs[i] || !aligned16(A_ptrs[i]) || !aligned16(B_ptrs[i])) return MOLORA_ERR_INVALID_ARG;
+    table.a[i] = A_ptrs[i];
+    table.b[i] = B_ptrs[i];
+  }
+  return molora::apply_impl(x, dtype, N, d_in, d_out, A_ptrs[0], B_ptrs[0], K, r, ids, w, k, counts, offsets, perm,
+                            scale, y, y_bf16 != 0, err_word, path, stream, &table);
 }
 
 molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,

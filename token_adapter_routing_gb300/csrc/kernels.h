@@ -10,6 +10,13 @@
 
 namespace molora {
 
+// Per-adapter base addresses for the indirect layout (adapters anywhere in memory): a[i] is
+// adapter i's A [d_in x r], b[i] its B [r x d_out].  Passed to kernels by value.
+struct AdapterTable {
+  const void* a[MOLORA_MAX_ADAPTERS];
+  const void* b[MOLORA_MAX_ADAPTERS];
+};
+
 cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
                                int32_t* adapter, int32_t* err_word, cudaStream_t stream);
 
@@ -25,7 +32,7 @@ cudaError_t launch_route_vocab_dispatch(const int32_t* tok, int64_t N, const int
 cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
                                const float* w, int32_t k, float scale, void* y, bool y_bf16, int32_t mask_adapter,
-                               int32_t* err_word, cudaStream_t stream);
+                               int32_t* err_word, cudaStream_t stream, const AdapterTable* table = nullptr);
 
 // CUDA-core learned router (any dtype / shape).
 cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
@@ -42,7 +49,7 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
                                 const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
                                 float scale, void* y, bool y_bf16, int32_t mask_adapter, int32_t* err_word,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const AdapterTable* table = nullptr);
 
 // tcgen05 learned router: true if this shape is supported.
 bool router_tc_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t K, int32_t k);

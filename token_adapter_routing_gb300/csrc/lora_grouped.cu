@@ -30,6 +30,7 @@
 // a CTA that is itself waiting at a cluster barrier.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 #ifdef MOLORA_TUNING_ENV
 #include <cstdlib>
@@ -206,8 +207,9 @@ __global__ void __maxnreg__(168)
                         int32_t r, int32_t k, const int32_t* __restrict__ ids, const float* __restrict__ w,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, float scale,
                         void* __restrict__ y, int32_t y_bf16, int32_t mask_adapter, const GroupedPlan P,
-                        int32_t* err_word,
-                        const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b) {
+                        int32_t* err_word, const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b, int32_t indirect,
+                        const __grid_constant__ AdapterTable table) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(sm + P.region);
@@ -225,8 +227,9 @@ __global__ void __maxnreg__(168)
     tmem_alloc(&ctrl->tmem_base, P.tmem_cols);
     tmem_relinquish();
     if (lane == 0) {
-      mbar_init(&ctrl->bar_a, 1);
-      mbar_init(&ctrl->bar_b, 1);
+      // indirect layout: the 32 lanes of this warp load A and B with cp.async, one arrival each
+      mbar_init(&ctrl->bar_a, indirect ? 32 : 1);
+      mbar_init(&ctrl->bar_b, indirect ? 32 : 1);
       mbar_init(&ctrl->bar_x[0], 1);
       mbar_init(&ctrl->bar_x[1], 1);
       for (int i = 0; i < 2; ++i) {
@@ -239,8 +242,10 @@ __global__ void __maxnreg__(168)
       // both receive the tile's TM rows x r values: fp32 partials, and g as two bf16 halves
       mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)P.TM * r * 4u);
       mbar_arrive_expect_tx(&ctrl->bar_g, (uint32_t)P.TM * r * 4u);
-      tma_prefetch_desc(&map_a);
-      tma_prefetch_desc(&map_b);
+      if (!indirect) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+      }
     }
   }
   if (P.early_y > 0 && warp == 0) {
@@ -342,11 +347,24 @@ __global__ void __maxnreg__(168)
   const size_t blk_bytes = (size_t)TM * 128;          // one 64-column K-block of a buffer
   const size_t buf_bytes = (size_t)(P.XR / kKBlock) * blk_bytes;
   const uint32_t idesc_shrink = idesc_bf16_f32(kTileM, r, false, true);
-  if (warp == 4 && lane == 0) {
-    mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
-    for (int kb = 0; kb < KS / kKBlock; ++kb)
-      tma_load_2d(smem_u32(as + (size_t)kb * kKBlock * r * 2), &map_a, 0, a * d_in + crank * KS + kb * kKBlock,
-                  &ctrl->bar_a);
+  if (warp == 4) {
+    if (indirect) {
+      // the same bytes the TMA box would write: rows of r elements, swizzled to match r
+      const __nv_bfloat16* Aa = static_cast<const __nv_bfloat16*>(table.a[a]) + (int64_t)crank * KS * r;
+      const int cpr = r / 8;  // 16-byte chunks per row
+      for (int i = lane; i < KS * cpr; i += 32) {
+        const int row = i / cpr, chunk = i % cpr;
+        cp_async_16(smem_u32(as) + (uint32_t)((row / kKBlock) * kKBlock * r * 2) +
+                        swz_offset(row % kKBlock, chunk, (uint32_t)r * 2u),
+                    Aa + (int64_t)row * r + chunk * 8, 16u);
+      }
+      cp_async_mbar_arrive(&ctrl->bar_a);
+    } else if (lane == 0) {
+      mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KS * r * 2);
+      for (int kb = 0; kb < KS / kKBlock; ++kb)
+        tma_load_2d(smem_u32(as + (size_t)kb * kKBlock * r * 2), &map_a, 0, a * d_in + crank * KS + kb * kKBlock,
+                    &ctrl->bar_a);
+    }
   }
   // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
   auto gather = [&](int rd) {
@@ -413,7 +431,10 @@ __global__ void __maxnreg__(168)
     named_barrier(kBarX, kThreads);  // round rd is in shared memory
     if (warp == 4 && lane == 0) {
       bool ok = !ctrl->abort;
-      if (ok && rd == 0) ok = mbar_wait(&ctrl->bar_a, 0);
+      if (ok && rd == 0) {
+        ok = mbar_wait(&ctrl->bar_a, 0);
+        fence_proxy_async_smem();  // A written by cp.async (indirect layout) is read by the MMA
+      }
       tc_fence_after();
       uint64_t* done = &ctrl->bar_x[rd % nbuf];
       if (ok) {
@@ -439,12 +460,23 @@ __global__ void __maxnreg__(168)
   // the last round's commit covers every shrink MMA issued before it
   uint64_t* const last_bar = &ctrl->bar_x[(rounds - 1) % nbuf];
   const uint32_t last_parity = (uint32_t)((rounds - 1) / nbuf) & 1u;
-  if (warp == 4 && lane == 0) {
+  if (warp == 4 && (indirect || lane == 0)) {
     // B chunk lands in the phase-1 region once the last shrink MMAs have read it
     if (mbar_wait(last_bar, last_parity)) {
-      mbar_arrive_expect_tx(&ctrl->bar_b, (uint32_t)NC * r * 2);
-      for (int q = 0; q < NC / 64; ++q)
-        tma_load_2d(smem_u32(bs + (size_t)q * r * 128), &map_b, crank * NC + q * 64, a * r, &ctrl->bar_b);
+      if (indirect) {
+        // boxes of r rows x 64 columns, 128-byte rows swizzled, as the TMA would write them
+        const __nv_bfloat16* Ba = static_cast<const __nv_bfloat16*>(table.b[a]) + (int64_t)crank * NC;
+        for (int i = lane; i < r * (NC / 8); i += 32) {
+          const int row = i / (NC / 8), c8 = i % (NC / 8);  // c8: 16-byte chunk along the columns
+          cp_async_16(smem_u32(bs) + (uint32_t)((c8 / 8) * r * 128) + sw128_offset(row, c8 % 8),
+                      Ba + (int64_t)row * d_out + c8 * 8, 16u);
+        }
+        cp_async_mbar_arrive(&ctrl->bar_b);
+      } else {
+        mbar_arrive_expect_tx(&ctrl->bar_b, (uint32_t)NC * r * 2);
+        for (int q = 0; q < NC / 64; ++q)
+          tma_load_2d(smem_u32(bs + (size_t)q * r * 128), &map_b, crank * NC + q * 64, a * r, &ctrl->bar_b);
+      }
     } else {
       ctrl->abort = 1;
       report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
@@ -676,7 +708,7 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
                                 int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k,
                                 const int32_t* counts, const int32_t* offsets, const int32_t* perm, float scale,
                                 void* y, bool y_bf16, int32_t mask_adapter, int32_t* err_word,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const AdapterTable* table) {
   (void)counts;
   GroupedPlan s;
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
@@ -696,11 +728,20 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   }
 #endif
   CUtensorMap map_a, map_b;
-  const CUtensorMapSwizzle swa =
-      r == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!make_map(&map_a, A, (uint64_t)K * d_in, (uint64_t)r, (uint32_t)r, kKBlock, swa)) return cudaErrorInvalidValue;
-  if (!make_map(&map_b, B, (uint64_t)K * r, (uint64_t)d_out, 64, (uint32_t)r, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  AdapterTable tab;
+  memset(&tab, 0, sizeof(tab));
+  if (table) {
+    // indirect layout: the kernel reads the adapters through the table; the maps stay unused
+    memset(&map_a, 0, sizeof(map_a));
+    memset(&map_b, 0, sizeof(map_b));
+    tab = *table;
+  } else {
+    const CUtensorMapSwizzle swa =
+        r == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!make_map(&map_a, A, (uint64_t)K * d_in, (uint64_t)r, (uint32_t)r, kKBlock, swa)) return cudaErrorInvalidValue;
+    if (!make_map(&map_b, B, (uint64_t)K * r, (uint64_t)d_out, 64, (uint32_t)r, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -712,7 +753,8 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   const int64_t tiles = mask_adapter >= 0 ? (N + s.TM - 1) / s.TM : (N * k + s.TM - 1) / s.TM + K;
   return launch_kernel(lora_grouped_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C,
                        static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r, k, ids, w, offsets, perm, scale, y,
-                       (int32_t)(y_bf16 ? 1 : 0), mask_adapter, s, err_word, map_a, map_b);
+                       (int32_t)(y_bf16 ? 1 : 0), mask_adapter, s, err_word, map_a, map_b, (int32_t)(table ? 1 : 0),
+                       tab);
 }
 
 }  // namespace molora

@@ -4,6 +4,8 @@
 //     below the crossover a scalar per-token kernel beats the tensor-core kernel), which
 //     also serves fp32 inputs, rank 8 and shapes the grouped tcgen05 path does not take;
 //   * a CUDA-core learned router TopK(g(x)) (Table 1) for fp32 or odd shapes.
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -82,7 +84,8 @@ __global__ void __launch_bounds__(kScalarThreads)
     lora_scalar_kernel(const T* __restrict__ x, int32_t d_in, int32_t d_out, const T* __restrict__ A,
                        const T* __restrict__ B, int32_t K, const int32_t* __restrict__ ids,
                        const float* __restrict__ w, int32_t k, float scale, YT* __restrict__ y,
-                       int32_t cols_per_split, int32_t mask_adapter, int32_t* err_word) {
+                       int32_t cols_per_split, int32_t mask_adapter, int32_t* err_word, int32_t indirect,
+                       const __grid_constant__ AdapterTable table) {
   using C16 = Chunk16<T>;
   constexpr int VEC = C16::kVec;
   constexpr int CPR = R / VEC;  // 16-byte chunks per row of A_a
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kScalarThreads)
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    const T* Aa = A + (int64_t)a * d_in * R;
+    const T* Aa = indirect ? static_cast<const T*>(table.a[a]) : A + (int64_t)a * d_in * R;
     const int64_t nchunks = (int64_t)d_in * CPR;
 #pragma unroll 4
     for (int64_t c = tid; c < nchunks; c += kScalarThreads) {
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kScalarThreads)
       for (int j = 0; j < k; ++j) {
         const int32_t a = s_adapter[j];
         if (a < 0) continue;
-        const T* Bq = B + (int64_t)a * R * d_out + c;
+        const T* Bq = (indirect ? static_cast<const T*>(table.b[a]) : B + (int64_t)a * R * d_out) + c;
         const float* gj = g + j * R;
 #pragma unroll
         for (int q = 0; q < R; ++q) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kScalarThreads)
       for (int j = 0; j < k; ++j) {
         const int32_t a = s_adapter[j];
         if (a < 0) continue;
-        const T* Bq = B + (int64_t)a * R * d_out + c;
+        const T* Bq = (indirect ? static_cast<const T*>(table.b[a]) : B + (int64_t)a * R * d_out) + c;
         for (int q = 0; q < R; ++q) acc = fmaf(g[j * R + q], to_f(Bq[(int64_t)q * d_out]), acc);
       }
       y_add1(yr + c, acc);
@@ -189,7 +192,7 @@ template <typename T, typename YT>
 static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
                                    const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                    int32_t k, float scale, void* y, int32_t mask_adapter, int32_t* err_word,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, const AdapterTable* table) {
   // Enough CTAs to cover the GPU twice: small batches split the output columns (each split
   // recomputes the token's cheap shrink).
   const int64_t want = 2 * (int64_t)num_sms();
@@ -205,19 +208,23 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
   const T* Ap = static_cast<const T*>(A);
   const T* Bp = static_cast<const T*>(B);
   YT* yp = static_cast<YT*>(y);
+  AdapterTable tab;
+  memset(&tab, 0, sizeof(tab));
+  if (table) tab = *table;
+  const int32_t ind = table ? 1 : 0;
   switch (r) {
     case 8:
       return launch_kernel(lora_scalar_kernel<T, YT, 8>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
     case 16:
       return launch_kernel(lora_scalar_kernel<T, YT, 16>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
     case 32:
       return launch_kernel(lora_scalar_kernel<T, YT, 32>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
     case 64:
       return launch_kernel(lora_scalar_kernel<T, YT, 64>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word);
+                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
     default:
       return cudaErrorInvalidValue;
   }
@@ -226,16 +233,16 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
 cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
                                const float* w, int32_t k, float scale, void* y, bool y_bf16, int32_t mask_adapter,
-                               int32_t* err_word, cudaStream_t stream) {
+                               int32_t* err_word, cudaStream_t stream, const AdapterTable* table) {
   if (dtype == MOLORA_BF16)
     return y_bf16 ? launch_scalar_t<__nv_bfloat16, __nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
-                                                                   mask_adapter, err_word, stream)
+                                                                   mask_adapter, err_word, stream, table)
                   : launch_scalar_t<__nv_bfloat16, float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
-                                                          mask_adapter, err_word, stream);
+                                                          mask_adapter, err_word, stream, table);
   return y_bf16 ? launch_scalar_t<float, __nv_bfloat16>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y,
-                                                         mask_adapter, err_word, stream)
+                                                         mask_adapter, err_word, stream, table)
                 : launch_scalar_t<float, float>(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, mask_adapter,
-                                                err_word, stream);
+                                                err_word, stream, table);
 }
 
 // ---------------------------------------------------------------------------------------
