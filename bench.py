@@ -63,7 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y", "indirect"],
+    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y", "indirect",
+                                      "split"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
@@ -552,7 +553,11 @@ def run_mode(args):
                alone back to back over six batches, grouped and scalar paths.
     indirect   Table 2: the hot set as two slabs (direct) against K separately allocated
                adapters (indirect, molora_lora_apply_indirect), N=2048, d=4096, r=16, top-1,
-               uniform adapters, K = 4, 16, 64; the apply alone back to back over six batches."""
+               uniform adapters, K = 4, 16, 64; the apply alone back to back over six batches.
+    split      Table 6: per-token routing against per-sequence routing that must split the batch
+               into its single-modality runs (one masked pass per run), on the 4-modality shape
+               with interleaved text-heavy (70/10/10/10) and balanced runs, and separated (one
+               contiguous block per modality); one CUDA graph each, L2 flushed between replays."""
     import token_adapter_routing_gb300 as m
     from token_adapter_routing_gb300 import build as lib_build
     lib_build.build()
@@ -565,7 +570,43 @@ def run_mode(args):
     def emit(d):
         print(json.dumps(d), flush=True)
 
-    if args.mode == "indirect":
+    if args.mode == "split":
+        for label, dist, separated in (("interleaved, text-heavy", "70-10-10-10", False),
+                                       ("interleaved, balanced", "uniform", False),
+                                       ("separated", "uniform", True)):
+            wl = workloads.make(WORKLOAD, dist=dist)
+            tok = wl.tok.sort().values if separated else wl.tok  # ranges are contiguous in the vocabulary
+            starts = wl.starts
+            a_host = (torch.bucketize(tok.long(), starts.long(), right=True) - 1).to(torch.int32)
+            runs, s0 = [], 0
+            for t in range(1, wl.N + 1):
+                if t == wl.N or a_host[t] != a_host[s0]:
+                    runs.append((s0, t, int(a_host[s0])))
+                    s0 = t
+            tok_d, starts_d = tok.to(dev), starts.to(dev)
+            x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+            adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+            counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+            offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+
+            def per_token():
+                m.molora_route_vocab_dispatch(tok_d, starts_d, adapter=adapter, counts=counts, offsets=offsets,
+                                              perm=perm)
+                m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
+
+            def per_sequence_split():
+                m.molora_route_vocab(tok_d, starts_d, adapter=adapter)
+                for s0_, e0_, a_ in runs:
+                    m.molora_lora_apply_masked_pass(x[s0_:e0_], A, B, adapter[s0_:e0_], a_, y[s0_:e0_], wl.scale)
+
+            t_ms = _replay_ms(_graph(per_token, stream), stream, 50, flush)
+            s_ms = _replay_ms(_graph(per_sequence_split, stream), stream, 50, flush)
+            emit({"mode": "split", "distribution": label, "workload": "N=2048, d=4096, K=4, r=16",
+                  "runs": len(runs), "per_token_us_p50": round(_pct(t_ms, 0.5) * 1e3, 2),
+                  "per_sequence_split_us_p50": round(_pct(s_ms, 0.5) * 1e3, 2),
+                  "speedup": round(_pct(s_ms, 0.5) / _pct(t_ms, 0.5), 2), "l2": "flushed between replays"})
+    elif args.mode == "indirect":
         for K in (4, 16, 64):
             wls = [workloads.make("decode_sweep", seed=4000 + b, N=2048, K=K) for b in range(N_BATCHES)]
             starts, A, B = wls[0].starts.to(dev), wls[0].A.to(dev), wls[0].B.to(dev)

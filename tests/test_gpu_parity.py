@@ -462,6 +462,30 @@ def test_masked_passes_equal_per_token(m, path):
     assert_apply_close(y_tok, y_ref)
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_sequence_split_passes_equal_per_token(m, path):
+    # per-sequence routing that splits the batch into its single-modality runs (Table 6): one
+    # masked pass per run over only that run's tokens gives the per-token result
+    wl = workloads.make("modality4", N=900, d_in=1024, d_out=1024, dist="70-10-10-10")
+    e = err_word()
+    adapter = m.molora_route_vocab(dev(wl.tok), dev(wl.starts), err_word=e)
+    a_host = adapter.cpu()
+    y = dev(wl.y0).clone()
+    x = dev(wl.x)
+    A, B = dev(wl.A), dev(wl.B)
+    s0, runs = 0, 0
+    for t in range(1, wl.N + 1):
+        if t == wl.N or a_host[t] != a_host[s0]:
+            m.molora_lora_apply_masked_pass(x[s0:t], A, B, adapter[s0:t], int(a_host[s0]), y[s0:t], wl.scale,
+                                            err_word=e, path=path)
+            runs += 1
+            s0 = t
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0 and runs > wl.K
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, a_host, wl.y0, wl.scale)
+    assert_apply_close(y, y_ref)
+
+
 # ------------------------------------------------------------------------- router
 
 def check_router(wl, k, logits, ids, w):

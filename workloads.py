@@ -14,7 +14,8 @@ workloads measured in "MoLoRA: Composable Specialization via Per-Token Adapter R
                   benchmark: text / image / audio / video vocabulary ranges).  Tokens come in
                   runs of geometric length (mean 64), one uniformly drawn modality per run;
                   ``dist`` "80-10-5-5" or "95-2-2-1" draws each run's modality with those
-                  shares instead (Table 9's group-size distributions).
+                  shares instead (Table 9's group-size distributions); "70-10-10-10" is the
+                  text-heavy interleaving of Table 6.
   2 topk_mlp      N=4096, d_in=2048, d_out=6144, K=4, r=16, k=2, bf16, learned router
                   (Figure 2's top-2 weighted sum at a Qwen3-1.7B MLP shape).
   3 decode_sweep  b tokens x K hot-set adapters, d_in=d_out=4096, r=16, bf16, top-1; adapter
@@ -94,7 +95,8 @@ def _tokens_in_ranges(g, modality: torch.Tensor, starts: torch.Tensor) -> torch.
     return (lo + torch.floor(u * (hi - lo).to(torch.float64)).to(torch.int64)).to(torch.int32)
 
 
-SHARES = {"80-10-5-5": (0.80, 0.10, 0.05, 0.05), "95-2-2-1": (0.95, 0.02, 0.02, 0.01)}
+SHARES = {"80-10-5-5": (0.80, 0.10, 0.05, 0.05), "95-2-2-1": (0.95, 0.02, 0.02, 0.01),
+          "70-10-10-10": (0.70, 0.10, 0.10, 0.10)}
 
 
 def modality_runs(g, N: int, K: int, mean_run: float = 64.0, shares=None) -> torch.Tensor:
