@@ -201,6 +201,9 @@ def test_apply_small_integers_bitexact(m, path, N, d_in, d_out, K, r, k):
     ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048, "r": 64, "K": 8}),
     ("modality4", {"dist": "80-10-5-5"}),
     ("modality4", {"dist": "95-2-2-1"}),
+    # d_in = 8192: a K-slice of 1024 columns per CTA takes two x rounds over two buffers
+    ("modality4", {"N": 300, "d_in": 8192, "d_out": 1024}),
+    ("modality4", {"N": 200, "d_in": 8192, "d_out": 1024, "r": 64}),
 ])
 def test_apply_vocab_routed_vs_oracle(m, path, name, kw):
     wl = workloads.make(name, **kw)
