@@ -59,13 +59,16 @@ typedef enum {
 
 typedef enum { MOLORA_F32 = 0, MOLORA_BF16 = 1 } molora_dtype;
 
-/* Which kernel family molora_lora_apply_ex uses.  AUTO picks by the measured crossover
- * between the two (Figures 5 and 9 put it near batch 160 on the paper's hardware; this
- * library measures its own and stores the result in its dispatch table). */
+/* Which kernel family molora_lora_apply_ex uses.  AUTO picks the dense path for k >= 2
+ * when it applies and is measured faster, else the scalar or grouped path by their measured
+ * crossover (Figures 5 and 9 put it near batch 160 on the paper's hardware; this library
+ * measures its own and stores the result in its dispatch table). */
 typedef enum {
   MOLORA_PATH_AUTO = 0,
   MOLORA_PATH_SCALAR = 1,  /* CUDA-core, token-major, one CTA per token (the memory-bound regime) */
-  MOLORA_PATH_GROUPED = 2  /* grouped tcgen05 shrink + expand over the dispatch permutation */
+  MOLORA_PATH_GROUPED = 2, /* grouped tcgen05 shrink + expand over the dispatch permutation */
+  MOLORA_PATH_DENSE = 3    /* tcgen05 over all K adapters per token, weight 0 for the unselected
+                              (K*r <= 128, bf16); needs no dispatch; one y update per token */
 } molora_path;
 
 /* Device-side error bits OR-ed into *err_word. */

@@ -336,6 +336,73 @@ def test_apply_bf16y_topk_weighted_vs_oracle(m, path):
     assert_bf16y_close(y, y0b, y_ref, 1 if path == "scalar" else 1 + k, parts)
 
 
+# ------------------------------------------------------------------------- dense path
+
+def random_topk(N, K, k, seed):
+    g = torch.Generator().manual_seed(seed)
+    ids = torch.stack([torch.randperm(K, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.softmax(torch.randn(N, k, generator=g), dim=1)
+    return ids, w
+
+
+def make_adapters(N, d_in, d_out, K, r, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(N, d_in, generator=g).to(torch.bfloat16)
+    A = (torch.randn(K, d_in, r, generator=g) / math.sqrt(d_in)).to(torch.bfloat16)
+    B = (torch.randn(K, r, d_out, generator=g) / math.sqrt(r)).to(torch.bfloat16)
+    y0 = torch.randn(N, d_out, generator=g)
+    return x, A, B, y0
+
+
+@pytest.mark.parametrize("K,r,k,N,d_in,d_out", [(4, 16, 2, 700, 1024, 1536), (4, 16, 1, 300, 512, 512),
+                                                (8, 16, 3, 513, 1024, 1024), (4, 32, 4, 200, 1024, 2048),
+                                                (8, 16, 2, 333, 2048, 1024), (2, 64, 2, 260, 1024, 512),
+                                                (4, 16, 4, 130, 1024, 1024), (4, 16, 2, 64, 4096, 1024)])
+def test_apply_dense_vs_oracle(m, K, r, k, N, d_in, d_out):
+    x, A, B, y0 = make_adapters(N, d_in, d_out, K, r, seed=N + K + r)
+    ids, w = random_topk(N, K, k, seed=k + 5)
+    y = dev(y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 2.0, w=dev(w), err_word=e, path="dense")
+    y2 = dev(y0).clone()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y2, 2.0, w=dev(w), path="dense")
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(y.cpu(), y2.cpu())  # one addition per y element: reproducible for any k
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 2.0, w)
+    assert_apply_close(y, y_ref)
+
+
+def test_apply_dense_is_auto_for_topk_and_skips_invalid_ids(m):
+    assert m.molora_select_path(torch.bfloat16, 4096, 2048, 6144, 4, 16, 2) == "dense"
+    assert m.molora_select_path(torch.bfloat16, 4096, 2048, 6144, 4, 16, 1) != "dense"
+    assert m.molora_select_path(torch.bfloat16, 4096, 2048, 6144, 16, 16, 2) != "dense"  # K*r = 256
+    N, d_in, d_out, K, r, k = 257, 1024, 1024, 4, 16, 2
+    x, A, B, y0 = make_adapters(N, d_in, d_out, K, r, seed=3)
+    ids, w = random_topk(N, K, k, seed=4)
+    ids[5, 0], ids[77, 1], ids[200, 0] = -1, K, 99
+    y = dev(y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 2.0, w=dev(w), err_word=e, path="dense")
+    torch.cuda.synchronize()
+    assert int(e.item()) == m.DEV_BAD_ADAPTER_ID
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 2.0, w)  # the oracle skips ids outside [0, K) too
+    assert_apply_close(y, y_ref)
+
+
+def test_apply_dense_bf16y(m):
+    N, d_in, d_out, K, r, k = 600, 1024, 1536, 4, 16, 2
+    x, A, B, y0 = make_adapters(N, d_in, d_out, K, r, seed=21)
+    ids, w = random_topk(N, K, k, seed=22)
+    y0b = y0.to(torch.bfloat16)
+    y = dev(y0b).clone()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 2.0, w=dev(w), path="dense")
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0b.float(), 2.0, w)
+    # the token's whole update is rounded to bf16 once, then added with one more rounding
+    assert_bf16y_close(y, y0b, y_ref, 2)
+
+
 # ------------------------------------------------------------------------- indirect layout
 
 def separate_adapters(wl):
@@ -571,7 +638,8 @@ def test_graph_captured_learned_path(m, path):
 
 # ------------------------------------------------------------------------- full-size workloads
 
-def test_full_size_topk_mlp_path(m):
+@pytest.mark.parametrize("path", ["grouped", "dense"])
+def test_full_size_topk_mlp_path(m, path):
     # N=4096, d_in=2048, d_out=6144, K=4, r=16, top-2: the whole path against the oracle
     wl = workloads.make("topk_mlp")
     x = dev(wl.x)
@@ -580,7 +648,7 @@ def test_full_size_topk_mlp_path(m):
     y = dev(wl.y0).clone()
     e = err_word()
     m.molora_lora_apply(x, dev(wl.A), dev(wl.B), ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm,
-                        err_word=e)
+                        err_word=e, path=path)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
     check_router(wl, 2, logits, ids, w)

@@ -32,7 +32,7 @@ __all__ = [
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 F32, BF16 = 0, 1
-PATHS = {"auto": 0, "scalar": 1, "grouped": 2}
+PATHS = {"auto": 0, "scalar": 1, "grouped": 2, "dense": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 DEV_TOKEN_OUTSIDE_RANGES = 0x1
 DEV_BAD_RANGES = 0x2

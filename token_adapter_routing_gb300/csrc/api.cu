@@ -30,6 +30,10 @@ static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_
 // hot-set adapters the grouped path is as fast or faster from batch 1; with 64 the scalar
 // path wins at every batch up to 512, because a grouped launch then carries up to K mostly
 // one-token tiles.
+// Largest stacked rank K*r for which AUTO prefers the dense path at k >= 2 (it evaluates every
+// adapter for every token, so its tensor-core work and B traffic grow with K*r).
+constexpr int32_t kDenseMaxKR = 128;
+
 static int64_t crossover_tokens(int32_t K) {
   if (K <= 32) return 1;
   return 1024;
@@ -55,10 +59,17 @@ static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, in
                                 cudaStream_t stream, const AdapterTable* table = nullptr) {
   const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
   if (st != MOLORA_OK || N == 0) return st;
-  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+  if (path == MOLORA_PATH_AUTO) {
+    path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+    if (path == MOLORA_PATH_DENSE && table) path = MOLORA_PATH_GROUPED;  // the dense path reads the slabs
+  }
   if (path == MOLORA_PATH_SCALAR)
     return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, -1,
                                        err_word, stream, table));
+  if (path == MOLORA_PATH_DENSE) {
+    if (table || !dense_supported(dtype, N, d_in, d_out, K, r)) return MOLORA_ERR_UNSUPPORTED;
+    return launched(launch_lora_dense(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, err_word, stream));
+  }
   if (path != MOLORA_PATH_GROUPED) return MOLORA_ERR_INVALID_ARG;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_ERR_UNSUPPORTED;
   if (!counts || !offsets || !perm) return MOLORA_ERR_INVALID_ARG;
@@ -113,6 +124,7 @@ molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t N, const i
 
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
                                int32_t k) {
+  if (k >= 2 && K * r <= kDenseMaxKR && dense_supported(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
   return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
 }
