@@ -543,7 +543,8 @@ def run_mode(args):
     topk       top-k scaling (Table 16): N=8192, d=4096, K=8, r=64, k=1..4, router -> dispatch
                -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
-               K=4, r=16, top-2): router alone, and router -> dispatch -> apply.
+               K=4, r=16, top-2): router alone; router -> dispatch -> grouped apply; router ->
+               dense apply; and each apply alone.
     perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
                passes over all tokens against one per-token pass.
     skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
@@ -802,20 +803,35 @@ def run_mode(args):
         perm = torch.empty(wl.N * wl.k, dtype=torch.int32, device=dev)
         g_router = _graph(lambda: m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w), stream)
 
-        def full():
+        def path_grouped():
             m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w)
             m.molora_dispatch(ids, wl.K, counts=counts, offsets=offsets, perm=perm)
-            m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm)
-        g_full = _graph(full, stream)
+            m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm,
+                                path="grouped")
+
+        def path_dense():  # no dispatch: the dense apply reads ids and w directly
+            m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w)
+            m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, path="dense")
+
         r_ms = _replay_ms(g_router, stream, 100, flush)
-        f_ms = _replay_ms(g_full, stream, 100, flush)
+        res = {}
+        for name, fn in (("grouped", path_grouped), ("dense", path_dense)):
+            res[f"path_{name}_us_p50"] = round(_pct(_replay_ms(_graph(fn, stream), stream, 100, flush), 0.5) * 1e3, 2)
+        path_grouped()  # ids, w, counts, offsets and perm for the apply-only graphs
+        torch.cuda.synchronize()
+        for name in ("grouped", "dense"):
+            g_ap = _graph(lambda name=name: m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts,
+                                                                 offsets=offsets, perm=perm, path=name), stream)
+            res[f"apply_{name}_us_p50"] = round(_pct(_replay_ms(g_ap, stream, 100, flush), 0.5) * 1e3, 2)
+        auto = m.molora_select_path(torch.bfloat16, wl.N, wl.d_in, wl.d_out, wl.K, wl.r, wl.k)
+        best = res[f"path_{auto}_us_p50"]
         rb = wl.N * wl.d_in * 2 + wl.d_in * 64 * 2 + wl.N * (wl.K + 2 * wl.k) * 4
         emit({"mode": "router", "workload": "N=4096, d_in=2048, d_out=6144, K=4, r=16, k=2",
               "router_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
               "router_GBps": round(rb / (_pct(r_ms, 0.5) * 1e-3) / 1e9, 1),
               "router_tflops": round(2 * wl.N * wl.d_in * 64 / (_pct(r_ms, 0.5) * 1e-3) / 1e12, 1),
-              "path_us_p50": round(_pct(f_ms, 0.5) * 1e3, 2),
-              "path_tokens_per_s": round(wl.N / (_pct(f_ms, 0.5) * 1e-3), 1), "l2": "flushed between replays"})
+              **res, "auto_path": auto, "path_us_p50": best,
+              "path_tokens_per_s": round(wl.N / (best * 1e-6), 1), "l2": "flushed between replays"})
     elif args.mode == "perseq":
         wl = workloads.make(WORKLOAD)
         tok, starts = wl.tok.to(dev), wl.starts.to(dev)

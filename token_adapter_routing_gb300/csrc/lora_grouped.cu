@@ -3,26 +3,27 @@
 // selected adapter run as grouped GEMMs; Table 1: grouped GEMM dispatch shared by both
 // routing modes; Figure 4: adapters at fixed addresses in a GPU-resident hot set).
 //
-// One fused kernel per call.  A work tile is up to 128 consecutive slots of one adapter's
-// group (dispatch order), handled by a thread-block cluster of C CTAs:
-//   0. each CTA asks L2 to prefetch the y rows it will update, so the y reads overlap the
-//      x gather instead of following it;
-//   1. shrink, split over d_in: CTA c gathers its 128 token rows x[tok, c*KS:(c+1)*KS)
-//      with 16-byte cp.async in rounds of XR columns (the gather is fused as an index
-//      list: no permuted copy of x), TMA-loads A_a's matching K-slice, and accumulates
-//      h_c = x A_a (128 x r, fp32) in TMEM with tcgen05.mma;
+// One fused kernel per call.  A work tile is TM (64 or 128) consecutive slots of one
+// adapter's group (dispatch order), handled by a thread-block cluster of C CTAs:
+//   0. before the tile is known, each CTA prefetches an equal share of the start of y into
+//      L2 (DRAM is otherwise idle then); once its x rows have landed, each row prefetches
+//      its y segment;
+//   1. shrink, split over d_in: CTA c gathers its TM token rows x[tok, c*KS:(c+1)*KS)
+//      with 16-byte cp.async (the gather is fused as an index list: no permuted copy of
+//      x), TMA-loads A_a's matching K-slice, and accumulates h_c = x A_a (fp32) in TMEM
+//      with tcgen05.mma (M = 128; with TM = 64 the other 64 rows are unused);
 //   2. the C partial h_c are summed through distributed shared memory in a fixed order
 //      (deterministic), scaled by scale * w(slot), and split into two bf16 terms
 //      g = g_hi + g_lo (relative error 2^-17) to feed the next MMA;
 //   3. expand, split over d_out: CTA c computes D = g B_a[:, c*NC:(c+1)*NC) into TMEM in
 //      double-buffered passes of PW columns, B_a's columns TMA-loaded;
-//   4. epilogue: D goes TMEM -> registers -> shared memory, then each warp adds its rows
-//      into y[tok, cols] with coalesced 16-byte accesses (this un-permutes: scatter by
-//      token).  With k = 1 every y row has one writer, so it is a plain read-modify-write;
-//      with k > 1 the k slots of a token live in different tiles and the additions are
-//      red.global.add.v4.f32 reductions in L2.
-// The same kernel runs one masked per-sequence pass when given a fixed adapter: tiles are
-// then 128 consecutive tokens and the slot weight is the 0/1 mask.
+//   4. epilogue: D goes TMEM -> registers -> shared memory, then each row segment is added
+//      into y[tok, cols] by one TMA bulk reduction in L2 (this un-permutes: scatter by
+//      token).  With k = 1 every y element receives one addition; with k > 1 a token's k
+//      slots live in different tiles and their additions may land in any order.
+// The same kernel runs one masked per-sequence pass when given a fixed adapter (tiles are
+// then consecutive tokens and the slot weight is the 0/1 mask), takes the adapters from a
+// table of addresses instead of the slabs (indirect layout), and updates a bf16 y.
 //
 // Shapes small enough for two CTAs per SM (shared memory <= 113 KB, 256 TMEM columns) use
 // 128-column passes; larger ones run one CTA per SM with 512 TMEM columns.  Either way the
