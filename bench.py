@@ -63,8 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "topk", "router", "perseq", "skew", "bf16y", "indirect",
-                                      "split"],
+    p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "topk", "router", "perseq", "skew",
+                                      "bf16y", "indirect", "split"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
@@ -540,6 +540,9 @@ def run_mode(args):
                r=16, top-1, uniform and Zipf(1.1) adapter draws; routing -> apply as one CUDA
                graph, L2 flushed between replays: route_vocab -> scalar apply, and
                route_vocab_dispatch -> grouped apply.
+    crossover_topk  top-2 with router-like weights, r = 16: d = 4096 at K = 4 and 8 over batch
+               1..2048, and 2048 -> 6144 at K = 4 over 512..8192 tokens; scalar, grouped (with
+               dispatch) and dense (without) applies, L2 flushed.
     topk       top-k scaling (Table 16): N=8192, d=4096, K=8, r=64, k=1..4, router -> dispatch
                -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
@@ -743,6 +746,34 @@ def run_mode(args):
                   "step_us": round(res["step"], 3), "apply_GBps": round(algo / (res["apply"] * 1e-6) / 1e9, 1),
                   "frac_of_measured": round(algo / (res["apply"] * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                   "l2": f"inputs larger than L2 ({N_BATCHES} resident batches, back to back)"})
+    elif args.mode == "crossover_topk":
+        for d_in, d_out, K, batches in ((4096, 4096, 4, (1, 8, 32, 128, 512, 2048)),
+                                        (4096, 4096, 8, (1, 8, 32, 128, 512, 2048)),
+                                        (2048, 6144, 4, (512, 1024, 2048, 4096, 8192))):
+            for b in batches:
+                k = 2
+                g_ = torch.Generator().manual_seed(b + K)
+                x = (torch.randn(b, d_in, generator=g_)).to(torch.bfloat16).to(dev)
+                A = (torch.randn(K, d_in, 16, generator=g_) / math.sqrt(d_in)).to(torch.bfloat16).to(dev)
+                B = (torch.randn(K, 16, d_out, generator=g_) / 4).to(torch.bfloat16).to(dev)
+                y = torch.randn(b, d_out, generator=g_).to(dev)
+                ids = torch.stack([torch.randperm(K, generator=g_)[:k] for _ in range(b)]).to(torch.int32).to(dev)
+                w = torch.softmax(torch.randn(b, k, generator=g_), dim=1).to(dev)
+                counts = torch.empty(K, dtype=torch.int32, device=dev)
+                offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
+                perm = torch.empty(b * k, dtype=torch.int32, device=dev)
+                row = {"mode": "crossover_topk", "d_in": d_in, "d_out": d_out, "K": K, "k": k, "batch": b,
+                       "auto": m.molora_select_path(torch.bfloat16, b, d_in, d_out, K, 16, k)}
+                for path in ("scalar", "grouped", "dense"):
+                    def fn(path=path):
+                        if path == "grouped":
+                            m.molora_dispatch(ids, K, counts=counts, offsets=offsets, perm=perm)
+                        m.molora_lora_apply(x, A, B, ids, y, 2.0, w=w, counts=counts, offsets=offsets, perm=perm,
+                                            path=path)
+                    ms = _replay_ms(_graph(fn, stream), stream, 30, flush)
+                    row[f"{path}_us_p50"] = round(_pct(ms, 0.5) * 1e3, 2)
+                row["fastest"] = min(("scalar", "grouped", "dense"), key=lambda p_: row[f"{p_}_us_p50"])
+                emit(row)
     elif args.mode == "crossover":
         for dist in ("uniform", "zipf"):
             for K in (4, 8, 16, 32, 64):

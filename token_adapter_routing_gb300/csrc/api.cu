@@ -30,10 +30,6 @@ static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_
 // hot-set adapters the grouped path is as fast or faster from batch 1; with 64 the scalar
 // path wins at every batch up to 512, because a grouped launch then carries up to K mostly
 // one-token tiles.
-// Largest stacked rank K*r for which AUTO prefers the dense path at k >= 2 (it evaluates every
-// adapter for every token, so its tensor-core work and B traffic grow with K*r).
-constexpr int32_t kDenseMaxKR = 128;
-
 static int64_t crossover_tokens(int32_t K) {
   if (K <= 32) return 1;
   return 1024;
@@ -124,7 +120,7 @@ molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t N, const i
 
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
                                int32_t k) {
-  if (k >= 2 && K * r <= kDenseMaxKR && dense_supported(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
+  if (k >= 2 && dense_preferred(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
   return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
 }

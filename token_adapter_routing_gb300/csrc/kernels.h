@@ -36,6 +36,8 @@ cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int
 
 // Token-major tcgen05 apply over all K adapters (K*r <= 128; weight 0 for the unselected).
 bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r);
+// True where AUTO takes the dense path (measured faster than the grouped one).
+bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r);
 cudaError_t launch_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
                               int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
                               void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream);

@@ -475,6 +475,18 @@ bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
   return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, &s) && dense_encoder() != nullptr;
 }
 
+// Where the dense path beat the grouped one on GB300 (top-2, r = 16, L2 flushed): with a plan
+// of two CTAs per SM and at least a few thousand tokens (2048 -> 6144 at N = 4096: 64 vs 82 us).
+// One CTA per SM (d_in = 4096 at K*r = 64) leaves too few clusters resident, and small batches
+// pay for the extra adapters: the grouped path won all of those points.
+bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
+  if (dtype != MOLORA_BF16 || N < 2048 || !(r == 16 || r == 32 || r == 64) || K * r > 128) return false;
+  DensePlan s;
+  for (int C : {8, 4, 2, 1})
+    if (dense_plan(d_in, d_out, K, r, C, kTwoPerSm, &s)) return dense_encoder() != nullptr;
+  return false;
+}
+
 cudaError_t launch_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
                               int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
                               void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream) {
