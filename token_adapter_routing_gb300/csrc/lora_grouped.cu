@@ -203,11 +203,13 @@ __device__ __forceinline__ SmemLayout sw_for_rank(int r) {
 }  // namespace
 
 // At most 168 registers: two CTAs (10 warps) must fit the 16K registers of an SM partition.
+// kYBf16: y is bf16 (a separate instantiation, so the fp32 epilogue carries no bf16 branch).
+template <bool kYBf16>
 __global__ void __maxnreg__(168)
     lora_grouped_kernel(const __nv_bfloat16* __restrict__ x, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
                         int32_t r, int32_t k, const int32_t* __restrict__ ids, const float* __restrict__ w,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm, float scale,
-                        void* __restrict__ y, int32_t y_bf16, int32_t mask_adapter, const GroupedPlan P,
+                        void* __restrict__ y, int32_t mask_adapter, const GroupedPlan P,
                         int32_t* err_word, const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b, int32_t indirect,
                         const __grid_constant__ AdapterTable table) {
@@ -218,7 +220,7 @@ __global__ void __maxnreg__(168)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = P.C, KS = P.KS, NC = P.NC, TM = P.TM;
   uint8_t* const yb = static_cast<uint8_t*>(y);
-  const uint32_t ysz = y_bf16 ? 2u : 4u;  // bytes per y element: fp32, or bf16
+  constexpr uint32_t ysz = kYBf16 ? 2u : 4u;  // bytes per y element: fp32, or bf16
   const int crank = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x / C;
   const int64_t S = N * (int64_t)k;
@@ -619,7 +621,7 @@ __global__ void __maxnreg__(168)
           float v[32];
           tmem_ld32(lane_base + buf * P.PW + q + c0, v);
           if (my_tok >= 0) {
-            if (y_bf16) {
+            if (kYBf16) {
               // round each contribution to bf16 (nearest even); the bulk add rounds the sum
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(srow) + c0 * 2);
 #pragma unroll
@@ -643,7 +645,7 @@ __global__ void __maxnreg__(168)
         fence_proxy_async_smem();
         if (my_tok >= 0) {
           void* dst = yb + ((int64_t)my_tok * d_out + crank * NC + p * P.PW + q) * ysz;
-          if (y_bf16)
+          if (kYBf16)
             bulk_reduce_add_bf16(dst, smem_u32(srow), (uint32_t)cols * 2u);
           else
             bulk_reduce_add_f32(static_cast<float*>(dst), smem_u32(srow), (uint32_t)cols * 4u);
@@ -746,16 +748,20 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(lora_grouped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    attr_err = cudaFuncSetAttribute(lora_grouped_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(lora_grouped_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kMaxSmem);
     if (attr_err != cudaSuccess) cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return attr_err;
 
   const int64_t tiles = mask_adapter >= 0 ? (N + s.TM - 1) / s.TM : (N * k + s.TM - 1) / s.TM + K;
-  return launch_kernel(lora_grouped_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C,
-                       static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r, k, ids, w, offsets, perm, scale, y,
-                       (int32_t)(y_bf16 ? 1 : 0), mask_adapter, s, err_word, map_a, map_b, (int32_t)(table ? 1 : 0),
-                       tab);
+  return launch_kernel(y_bf16 ? lora_grouped_kernel<true> : lora_grouped_kernel<false>, dim3((unsigned)(tiles * s.C)),
+                       dim3(kThreads), s.smem, stream, s.C, static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r,
+                       k, ids, w, offsets, perm, scale, y, mask_adapter, s, err_word, map_a, map_b,
+                       (int32_t)(table ? 1 : 0), tab);
 }
 
 }  // namespace molora
