@@ -24,15 +24,17 @@ static bool valid_dtype(molora_dtype d) { return d == MOLORA_F32 || d == MOLORA_
 static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_OK : MOLORA_ERR_CUDA; }
 
 // Smallest slot count (N*k) at which the grouped tensor-core apply beats the scalar apply,
-// measured on GB300 with the decode sweep (d = 4096, r = 16, top-1, batch 1..512, uniform and
-// Zipf(1.1) adapter draws, L2 flushed between replays; vocabulary routing -> scalar apply
-// against routing with dispatch -> grouped apply, each as one CUDA graph).  With up to 32
-// hot-set adapters the grouped path is as fast or faster from batch 1; with 64 the scalar
-// path wins at every batch up to 512, because a grouped launch then carries up to K mostly
-// one-token tiles.
+// measured on GB300 with the decode sweep (d = 4096, r = 16, top-1, batch 1..2048, uniform
+// and Zipf(1.1) adapter draws; vocabulary routing -> scalar apply against routing with
+// dispatch -> grouped apply; 50 calls back to back in one CUDA graph, the decode steady
+// state with the hot set in L2).  The scalar path wins every batch up to 512; the grouped
+// path wins from 768 tokens with up to 8 hot-set adapters, from 1024 with 16, at 2048 with
+// 32 under uniform draws; with 64 the scalar path wins at every batch measured.
 static int64_t crossover_tokens(int32_t K) {
-  if (K <= 32) return 1;
-  return 1024;
+  if (K <= 8) return 768;
+  if (K <= 16) return 1024;
+  if (K <= 32) return 2048;
+  return 4096;
 }
 
 static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
