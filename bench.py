@@ -571,7 +571,8 @@ def run_mode(args):
                -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
                K=4, r=16, top-2): router alone; router -> dispatch -> grouped apply; router ->
-               dense apply; and each apply alone.
+               dense apply; router and dense apply fused in one kernel
+               (molora_router_lora_apply); and each apply alone.
     perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
                passes over all tokens against one per-token pass.
     skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
@@ -870,9 +871,12 @@ def run_mode(args):
             m.molora_router_topk(x, W1, W2, wl.k, logits=logits, ids=ids, w=w)
             m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, path="dense")
 
+        def path_fused():  # router and dense apply in one kernel: x is read once
+            m.molora_router_lora_apply(x, W1, W2, A, B, wl.k, y, wl.scale, logits=logits, ids=ids, w=w)
+
         r_ms = _replay_ms(g_router, stream, 100, flush)
         res = {}
-        for name, fn in (("grouped", path_grouped), ("dense", path_dense)):
+        for name, fn in (("grouped", path_grouped), ("dense", path_dense), ("fused", path_fused)):
             res[f"path_{name}_us_p50"] = round(_pct(_replay_ms(_graph(fn, stream), stream, 100, flush), 0.5) * 1e3, 2)
         path_grouped()  # ids, w, counts, offsets and perm for the apply-only graphs
         torch.cuda.synchronize()
@@ -888,6 +892,7 @@ def run_mode(args):
               "router_GBps": round(rb / (_pct(r_ms, 0.5) * 1e-3) / 1e9, 1),
               "router_tflops": round(2 * wl.N * wl.d_in * 64 / (_pct(r_ms, 0.5) * 1e-3) / 1e12, 1),
               **res, "auto_path": auto, "path_us_p50": best,
+              "fused_tokens_per_s": round(wl.N / (res["path_fused_us_p50"] * 1e-6), 1),
               "path_tokens_per_s": round(wl.N / (best * 1e-6), 1), "l2": "flushed between replays"})
     elif args.mode == "perseq":
         wl = workloads.make(WORKLOAD)

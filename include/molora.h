@@ -232,6 +232,32 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
                                          int32_t* err_word, molora_path path, cudaStream_t stream);
 
 /*
+ * molora_router_lora_apply -- the learned router and the top-k apply in one pass over x
+ * (Table 1: routing cost O(64d + 64K) on top of the apply; Figure 2: top-k adapters combined
+ * by a weighted sum).  It computes exactly what molora_router_topk followed by
+ * molora_lora_apply computes, in one kernel that reads each x row once for both: the router's
+ * x W1 is 64 more columns of the apply's shrink x [A_0 | ... | A_{K-1}].
+ *
+ *   logits, ids, w   as molora_router_topk (same hidden width 64, same top-k and softmax rule)
+ *   y[t,:] += scale * sum_j w[t,j] * (x[t,:] A_{ids[t,j]}) B_{ids[t,j]}
+ *
+ * x [N x d_in] bf16;  W1 [d_in x 64] bf16;  b1 fp32 [64] or NULL;  W2 [64 x K] bf16;
+ * b2 fp32 [K] or NULL;  A [K x d_in x r] and B [K x r x d_out] bf16 slabs;  1 <= k <= K;
+ * logits fp32 [N x K] output or NULL;  ids int32 [N x k] and w fp32 [N x k] outputs;
+ * y fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1) [N x d_out], updated in place.
+ * Every y element receives one addition, so results are reproducible for any k.
+ * Supported: dtype MOLORA_BF16, r in {16, 32, 64}, K*r <= 128 (the stacked ranks of the
+ * hot set), d_in and d_out multiples of 64 that split evenly over the kernel's cluster;
+ * other shapes return MOLORA_ERR_UNSUPPORTED (use the two calls).  x, W1, A, B and y must be
+ * 16-byte aligned.
+ */
+MOLORA_API molora_status molora_router_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                       int32_t d_out, const void* W1, const float* b1, const void* W2,
+                                       const float* b2, const void* A, const void* B, int32_t K, int32_t r,
+                                       int32_t k, float scale, float* logits, int32_t* ids, float* w,
+                                       void* y, int32_t y_bf16, int32_t* err_word, cudaStream_t stream);
+
+/*
  * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:
  * per-sequence routing needs K passes for a K-modality batch).  Adapter `a` is evaluated
  * for EVERY token; the result is multiplied by the 0/1 mask [adapter_of[t] == a]:

@@ -209,7 +209,7 @@ def test_apply_vocab_routed_vs_oracle(m, path, name, kw):
     wl = workloads.make(name, **kw)
     adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, path)
     assert e == 0
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y, y_ref)
 
 
@@ -217,7 +217,7 @@ def test_apply_tiny_vocab_fp32(m):
     wl = workloads.make("tiny_vocab")
     adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, "scalar")
     assert e == 0
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y, y_ref)
     # auto must pick the scalar path for fp32 and still match
     _, _, _, _, y2, _ = run_vocab_path(m, wl, "auto")
@@ -308,7 +308,7 @@ def test_apply_bf16y_vocab_routed_vs_oracle(m, path, name, kw):
                         perm=perm, err_word=e, path=path)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), y0b.float(), wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), y0b.float(), wl.scale)
     # scalar: one rounding of the fp32 sum; grouped: the slot's contribution and the sum
     assert_bf16y_close(y, y0b, y_ref, 1 if path == "scalar" else 2)
 
@@ -337,6 +337,15 @@ def test_apply_bf16y_topk_weighted_vs_oracle(m, path):
 
 
 # ------------------------------------------------------------------------- dense path
+
+def oracle_adapter(wl, adapter=None):
+    """The oracle's vocabulary routing of wl's tokens (expected values never take the GPU's
+    ids as input); with `adapter` given, also checks that the GPU's routing equals it."""
+    ref, _ = oracle.route_vocab(wl.tok, wl.starts)
+    if adapter is not None:
+        assert torch.equal(adapter.cpu(), ref)
+    return ref
+
 
 def random_topk(N, K, k, seed):
     g = torch.Generator().manual_seed(seed)
@@ -431,7 +440,7 @@ def test_apply_indirect_equals_slab(m, path, name, kw):
     torch.cuda.synchronize()
     assert int(e.item()) == 0
     assert torch.equal(y_ind.cpu(), y_slab.cpu())
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y_ind, y_ref)
 
 
@@ -527,7 +536,7 @@ def test_masked_passes_equal_per_token(m, path):
     for a in range(wl.K):
         m.molora_lora_apply_masked_pass(dev(wl.x), dev(wl.A), dev(wl.B), adapter, a, y_seq, wl.scale, path=path)
     torch.cuda.synchronize()
-    y_ref, _ = oracle.per_sequence_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    y_ref, _ = oracle.per_sequence_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y_seq, y_ref)
     assert_apply_close(y_tok, y_ref)
 
@@ -552,30 +561,74 @@ def test_sequence_split_passes_equal_per_token(m, path):
             s0 = t
     torch.cuda.synchronize()
     assert int(e.item()) == 0 and runs > wl.K
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, a_host, wl.y0, wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y, y_ref)
 
 
 # ------------------------------------------------------------------------- router
 
-def check_router(wl, k, logits, ids, w):
-    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x, wl.W1, wl.W2, k)
-    assert torch.allclose(logits.cpu(), ref_logits, rtol=1e-4, atol=1e-4)
+def check_router(wl, k, logits, ids, w, rows=None, b1=None, b2=None):
+    """The GPU router's outputs (for `rows` of wl, or all) against the oracle router.  Returns
+    (clear, ref_ids, ref_w): the tokens whose k-th vs (k+1)-th oracle logit gap exceeds 1e-3,
+    where the ids must match exactly, and the oracle's ids and weights.  On the other tokens
+    the GPU's choice must still be a valid top k: k distinct adapters whose oracle logits are
+    within 1e-3 of the k-th largest."""
+    x = wl.x if rows is None else wl.x[rows].contiguous()
+    ref_logits, ref_ids, ref_w = oracle.router_topk(x, wl.W1, wl.W2, k, b1, b2)
+    logits, ids, w = (t.cpu() if rows is None else t.cpu()[rows] for t in (logits, ids, w))
+    assert torch.allclose(logits, ref_logits, rtol=1e-4, atol=1e-4)
     srt = torch.sort(ref_logits.double(), dim=1, descending=True).values
     if k < wl.K:
         clear = (srt[:, k - 1] - srt[:, k]) > 1e-3
     else:
-        clear = torch.ones(wl.N, dtype=torch.bool)
+        clear = torch.ones(x.shape[0], dtype=torch.bool)
     assert clear.float().mean() > 0.5
-    assert torch.equal(ids.cpu()[clear], ref_ids[clear])
-    rel = ((w.cpu()[clear].double() - ref_w[clear].double()).abs() / ref_w[clear].double().abs().clamp_min(1e-30))
+    assert torch.equal(ids[clear], ref_ids[clear])
+    rel = ((w[clear].double() - ref_w[clear].double()).abs() / ref_w[clear].double().abs().clamp_min(1e-30))
     assert rel.max().item() <= 1e-5
+    ids_l = ids.long()
+    assert ids_l.min().item() >= 0 and ids_l.max().item() < wl.K
+    assert all(len(set(row)) == k for row in ids_l.tolist())
+    picked = ref_logits.double().gather(1, ids_l)
+    assert bool((picked >= srt[:, k - 1:k] - 1e-3).all())
+    return clear, ref_ids, ref_w
+
+
+def check_learned_apply(wl, k, logits, ids, w, y, y0=None, rows=None, bf16_rounds=0, b1=None, b2=None):
+    """Router outputs as check_router; y against the oracle apply fed with the ORACLE's ids and
+    weights, on the tokens whose choice is clear (elsewhere the two may pick differently)."""
+    clear, ref_ids, ref_w = check_router(wl, k, logits, ids, w, rows, b1, b2)
+    y0 = wl.y0 if y0 is None else y0
+    sel = (lambda t: t) if rows is None else (lambda t: t[rows].contiguous())
+    y_ref, _ = oracle.lora_apply(sel(wl.x), wl.A, wl.B, ref_ids, sel(y0).float(), wl.scale, ref_w)
+    y_got = sel(y.cpu())
+    if bf16_rounds:
+        assert_bf16y_close(y_got[clear], sel(y0)[clear], y_ref[clear], bf16_rounds)
+    else:
+        assert_apply_close(y_got[clear], y_ref[clear])
     return clear
+
+
+def check_dispatch_of(ids, K, counts, offsets, perm):
+    """Dispatch of the GPU router's ids, by the definition's properties: counts are the
+    histogram, offsets its exclusive scan, and perm lists each adapter's slots in ascending
+    order (the stable grouping, unique for given ids)."""
+    flat = ids.cpu().reshape(-1).long()
+    hist = torch.bincount(flat, minlength=K)
+    assert torch.equal(counts.cpu().long(), hist)
+    assert torch.equal(offsets.cpu().long(), torch.cat([torch.zeros(1, dtype=torch.long), hist.cumsum(0)]))
+    p = perm.cpu().long()
+    assert torch.equal(torch.sort(p).values, torch.arange(flat.numel()))
+    key = flat[p] * flat.numel() + p  # adapter-major, then slot: strictly increasing iff grouped and stable
+    assert bool((key[1:] > key[:-1]).all())
 
 
 @pytest.mark.parametrize("name,kw,k", [("topk_mlp", {"N": 1000}, 2), ("topk_scaling", {"N": 777}, 1),
                                        ("topk_scaling", {"N": 513}, 3), ("topk_scaling", {"N": 300}, 4),
-                                       ("topk_mlp", {"N": 129, "d_in": 192}, 2)])
+                                       ("topk_mlp", {"N": 129, "d_in": 192}, 2),
+                                       # K > 8: the router's general second stage
+                                       ("topk_mlp", {"N": 300, "K": 16}, 3),
+                                       ("topk_mlp", {"N": 200, "d_in": 1024, "K": 64}, 2)])
 def test_router_topk_vs_oracle(m, name, kw, k):
     wl = workloads.make(name, k=k, **kw)
     logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(wl.W2), k)
@@ -631,12 +684,110 @@ def test_graph_captured_learned_path(m, path):
         y.copy_(dev(wl.y0))
         graph.replay()
     torch.cuda.synchronize()
-    check_router(wl, 2, logits, ids, w)
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids.cpu(), wl.y0, wl.scale, w.cpu())
-    assert_apply_close(y, y_ref)
+    check_learned_apply(wl, 2, logits, ids, w, y)
+    check_dispatch_of(ids, wl.K, counts, offsets, perm)
+
+
+# ------------------------------------------------------------------------- router + apply, one kernel
+
+FUSED_CASES = [({"N": 1000}, 2),                                      # 2048 -> 6144, K = 4, r = 16
+               ({"N": 129, "d_in": 512, "d_out": 1024, "r": 32}, 1),  # K*r = 128, one CTA per SM
+               ({"N": 333, "d_in": 1024, "d_out": 512, "K": 8}, 3),
+               ({"N": 64, "d_in": 1024, "d_out": 1024}, 4),            # k = K: every adapter
+               ({"N": 260, "d_in": 1024, "d_out": 512, "K": 2, "r": 64}, 2)]
+
+
+@pytest.mark.parametrize("kw,k", FUSED_CASES)
+def test_router_apply_fused_vs_oracle(m, kw, k):
+    wl = workloads.make("topk_mlp", k=k, **kw)
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    y, y2 = dev(wl.y0).clone(), dev(wl.y0).clone()
+    e = err_word()
+    logits, ids, w = m.molora_router_lora_apply(x, W1, W2, A, B, k, y, wl.scale, err_word=e)
+    logits2, ids2, w2 = m.molora_router_lora_apply(x, W1, W2, A, B, k, y2, wl.scale)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    # one addition per y element and a fixed summation order: reproducible bit for bit
+    for a_, b_ in ((y, y2), (logits, logits2), (ids, ids2), (w, w2)):
+        assert torch.equal(a_.cpu(), b_.cpu())
+    check_learned_apply(wl, k, logits, ids, w, y)
+
+
+@pytest.mark.parametrize("kw,k", FUSED_CASES[:3])
+def test_router_apply_fused_equals_two_calls(m, kw, k):
+    # the same summation orders as the separate router and dense apply: identical results
+    wl = workloads.make("topk_mlp", k=k, **kw)
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    y_f, y_s = dev(wl.y0).clone(), dev(wl.y0).clone()
+    lf, idf, wf = m.molora_router_lora_apply(x, W1, W2, A, B, k, y_f, wl.scale)
+    ls, ids_, ws = m.molora_router_topk(x, W1, W2, k)
+    m.molora_lora_apply(x, A, B, ids_, y_s, wl.scale, w=ws, path="dense")
+    torch.cuda.synchronize()
+    assert torch.equal(lf.cpu(), ls.cpu()) and torch.equal(idf.cpu(), ids_.cpu()) and torch.equal(wf.cpu(), ws.cpu())
+    assert torch.equal(y_f.cpu(), y_s.cpu())
+
+
+def test_router_apply_fused_biases_bf16y_graph(m):
+    wl = workloads.make("topk_mlp", N=515, d_in=1024, d_out=1536, k=2)
+    g = torch.Generator().manual_seed(9)
+    b1 = torch.randn(64, generator=g) * 0.1
+    b2 = torch.randn(wl.K, generator=g) * 0.1
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    # biases, fp32 y
+    y = dev(wl.y0).clone()
+    logits, ids, w = m.molora_router_lora_apply(x, W1, W2, A, B, 2, y, wl.scale, b1=dev(b1), b2=dev(b2))
+    torch.cuda.synchronize()
+    check_learned_apply(wl, 2, logits, ids, w, y, b1=b1, b2=b2)
+    # bf16 y: the token's update is rounded to bf16 once, then added with one more rounding
+    y0b = wl.y0.to(torch.bfloat16)
+    yb = dev(y0b).clone()
+    logits, ids, w = m.molora_router_lora_apply(x, W1, W2, A, B, 2, yb, wl.scale, want_logits=False)
+    torch.cuda.synchronize()
+    assert logits is None
+    lg = m.molora_router_topk(x, W1, W2, 2)[0]  # this call stored no logits
+    check_learned_apply(wl, 2, lg, ids, w, yb, y0=y0b, bf16_rounds=2)
+    # captured in a CUDA graph, replayed
+    yg = dev(wl.y0).clone()
+    lg_g = torch.empty(wl.N, wl.K, device="cuda")
+    ids_g = torch.empty(wl.N, 2, dtype=torch.int32, device="cuda")
+    w_g = torch.empty(wl.N, 2, device="cuda")
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            m.molora_router_lora_apply(x, W1, W2, A, B, 2, yg, wl.scale, logits=lg_g, ids=ids_g, w=w_g)
+    for rep in range(3):
+        yg.copy_(dev(wl.y0))
+        graph.replay()
+    torch.cuda.synchronize()
+    check_learned_apply(wl, 2, lg_g, ids_g, w_g, yg)
+
+
+def test_router_apply_fused_empty_and_unsupported(m):
+    wl = workloads.make("topk_mlp", N=64, d_in=512, d_out=512, k=2)
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    y = dev(wl.y0)[:0]
+    m.molora_router_lora_apply(x[:0], W1, W2, A, B, 2, y, wl.scale)  # N = 0: nothing launched
+    wl16 = workloads.make("topk_mlp", N=64, d_in=512, d_out=512, K=16, r=16, k=2)  # K*r = 256
+    with pytest.raises(m.MoloraError):
+        m.molora_router_lora_apply(dev(wl16.x), dev(wl16.W1), dev(wl16.W2), dev(wl16.A), dev(wl16.B), 2,
+                                   dev(wl16.y0), wl16.scale)
+    torch.cuda.synchronize()
 
 
 # ------------------------------------------------------------------------- full-size workloads
+
+def test_full_size_topk_mlp_fused(m):
+    # N=4096, d_in=2048, d_out=6144, K=4, r=16, top-2: router and apply in one kernel
+    wl = workloads.make("topk_mlp")
+    y = dev(wl.y0).clone()
+    e = err_word()
+    logits, ids, w = m.molora_router_lora_apply(dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B), 2, y,
+                                                wl.scale, err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    check_learned_apply(wl, 2, logits, ids, w, y)
+
 
 @pytest.mark.parametrize("path", ["grouped", "dense"])
 def test_full_size_topk_mlp_path(m, path):
@@ -651,11 +802,8 @@ def test_full_size_topk_mlp_path(m, path):
                         err_word=e, path=path)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
-    check_router(wl, 2, logits, ids, w)
-    rc, ro, rp, _ = oracle.dispatch(ids.cpu(), wl.K)
-    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids.cpu(), wl.y0, wl.scale, w.cpu())
-    assert_apply_close(y, y_ref)
+    check_learned_apply(wl, 2, logits, ids, w, y)
+    check_dispatch_of(ids, wl.K, counts, offsets, perm)
 
 
 @pytest.mark.parametrize("k", [1, 4])
@@ -673,14 +821,9 @@ def test_full_size_topk_scaling_sampled(m, k):
     assert int(e.item()) == 0
     g = torch.Generator().manual_seed(k)
     rows = torch.cat([torch.tensor([0, wl.N - 1]), torch.randperm(wl.N, generator=g)[:94]])
-    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x[rows], wl.W1, wl.W2, k)
-    assert torch.allclose(logits.cpu()[rows], ref_logits, rtol=1e-4, atol=1e-4)
-    y_ref, _ = oracle.lora_apply(wl.x[rows].contiguous(), wl.A, wl.B, ids.cpu()[rows].contiguous(), wl.y0[rows].contiguous(),
-                                 wl.scale, w.cpu()[rows].contiguous())
-    assert_apply_close(y.cpu()[rows], y_ref)
-    # dispatch over all 8192*k slots stays bit-exact
-    rc, ro, rp, _ = oracle.dispatch(ids.cpu(), wl.K)
-    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+    check_learned_apply(wl, k, logits, ids, w, y, rows=rows)
+    # dispatch over all 8192*k slots
+    check_dispatch_of(ids, wl.K, counts, offsets, perm)
 
 
 # ------------------------------------------------------------------------- failure handling
@@ -695,5 +838,5 @@ def test_bounded_wait_reports_timeout_and_context_survives(m):
     wl = workloads.make("modality4", N=200, d_in=512, d_out=512)
     adapter, counts, offsets, perm, y, err = run_vocab_path(m, wl, "grouped")
     assert err == 0
-    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, adapter.cpu(), wl.y0, wl.scale)
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y, y_ref)

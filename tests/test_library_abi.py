@@ -125,4 +125,17 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 5, None, fake, fake, None) == INVALID
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 65, 1, None, fake, fake, None) == INVALID
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 1, None, None, fake, None) == INVALID
+    # router + apply in one kernel: bad k, null or unaligned W1, null w; fp32 and K*r > 128 unsupported
+    lib.molora_router_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32, F, P, P, P, P,
+                                             I32, P, P]
+
+    def fused(dtype=1, K=4, r=16, k=2, W1=fake, w=fake, y=fake):
+        return lib.molora_router_lora_apply(fake, dtype, 64, 512, 512, W1, None, fake, None, fake, fake, K, r, k,
+                                            2.0, None, fake, w, y, 0, None, None)
+
+    assert fused(k=5) == INVALID and fused(k=0) == INVALID and fused(W1=None) == INVALID
+    assert fused(W1=odd) == INVALID and fused(w=None) == INVALID and fused(y=odd) == INVALID
+    assert fused(dtype=0) == UNSUPPORTED and fused(K=16, r=16) == UNSUPPORTED and fused(r=8) == UNSUPPORTED
+    assert lib.molora_router_lora_apply(None, 1, 0, 512, 512, None, None, None, None, None, None, 4, 16, 2, 2.0,
+                                        None, None, None, None, 0, None, None) == 0
     assert lib.molora_status_string(1) == b"invalid argument"

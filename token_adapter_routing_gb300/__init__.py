@@ -43,7 +43,7 @@ MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-            "molora_lora_apply",
+            "molora_lora_apply", "molora_router_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect", "molora_lora_apply_masked_pass", "molora_select_path",
             "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
@@ -80,6 +80,8 @@ def load_library():
     lib.molora_lora_apply_bf16y.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
     lib.molora_lora_apply_indirect.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, I32,
                                                P, S, P]
+    lib.molora_router_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32, F, P, P, P, P,
+                                             I32, P, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
     lib.molora_status_string.argtypes = [S]
@@ -259,6 +261,44 @@ def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None,
         _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(ids), _p(w), k, _p(counts), _p(offsets),
         _p(perm), float(scale), _p(y), _p(err_word), PATHS[path], _stream(stream)))
     return y
+
+
+def molora_router_lora_apply(x, W1, W2, A, B, k, y, scale, b1=None, b2=None, logits=None, ids=None, w=None,
+                             want_logits=True, err_word=None, stream=None):
+    """The learned router and the top-k apply in one kernel (x read once): returns
+    (logits fp32 [N,K] or None, ids int32 [N,k], w fp32 [N,k]); y (fp32 or bf16) is updated in
+    place exactly as molora_router_topk followed by molora_lora_apply would update it."""
+    _cuda(x, "x", None, 2)
+    N, d_in = x.shape
+    _cuda(W1, "W1", x.dtype, 2)
+    _cuda(W2, "W2", x.dtype, 2)
+    if W1.shape != (d_in, ROUTER_HIDDEN) or W2.shape[0] != ROUTER_HIDDEN:
+        raise ValueError("W1 must be [d_in, 64] and W2 [64, K]")
+    K = W2.shape[1]
+    _cuda(A, "A", x.dtype, 3)
+    _cuda(B, "B", x.dtype, 3)
+    if A.shape[0] != K or A.shape[1] != d_in or B.shape[:2] != (K, A.shape[2]):
+        raise ValueError("A must be [K, d_in, r] and B [K, r, d_out], with K = W2.shape[1]")
+    r, d_out = A.shape[2], B.shape[2]
+    _cuda(y, "y", None, 2)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"y must be float32 or bfloat16, got {y.dtype}")
+    for name, t in (("b1", b1), ("b2", b2)):
+        if t is not None:
+            _cuda(t, name, torch.float32)
+    dev = x.device
+    if logits is None and want_logits:
+        logits = torch.empty(N, K, dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty(N, k, dtype=torch.int32, device=dev)
+    if w is None:
+        w = torch.empty(N, k, dtype=torch.float32, device=dev)
+    _cuda(ids, "ids", torch.int32)
+    _cuda(w, "w", torch.float32)
+    _check("molora_router_lora_apply", load_library().molora_router_lora_apply(
+        _p(x), _dtype_code(x), N, d_in, d_out, _p(W1), _p(b1), _p(W2), _p(b2), _p(A), _p(B), K, r, k, float(scale),
+        _p(logits), _p(ids), _p(w), _p(y), 1 if y.dtype == torch.bfloat16 else 0, _p(err_word), _stream(stream)))
+    return logits, ids, w
 
 
 def molora_lora_apply_masked_pass(x, A, B, adapter_of, a, y, scale, err_word=None, path="auto", stream=None):

@@ -162,6 +162,21 @@ molora_status molora_lora_apply_indirect(const void* x, molora_dtype dtype, int6
                             scale, y, y_bf16 != 0, err_word, path, stream, &table);
 }
 
+molora_status molora_router_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                       const void* W1, const float* b1, const void* W2, const float* b2,
+                                       const void* A, const void* B, int32_t K, int32_t r, int32_t k, float scale,
+                                       float* logits, int32_t* ids, float* w, void* y, int32_t y_bf16,
+                                       int32_t* err_word, cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+  if (st != MOLORA_OK) return st;
+  if (N * (int64_t)K > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0) return MOLORA_OK;
+  if (!W1 || !W2 || !w || !aligned16(W1)) return MOLORA_ERR_INVALID_ARG;
+  if (!router_dense_supported(dtype, N, d_in, d_out, K, r)) return MOLORA_ERR_UNSUPPORTED;
+  return launched(launch_router_lora_dense(x, N, d_in, d_out, W1, b1, W2, b2, A, B, K, r, k, scale, logits, ids, w, y,
+                                           y_bf16 != 0, err_word, stream));
+}
+
 molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                 const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,

@@ -288,6 +288,83 @@ __device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uin
   return row * row_bytes + ((chunk ^ f) << 4);
 }
 
+// The learned router's second stage (Table 1's 64d + 64K routing cost; Figure 2's top-k
+// weighted sum) for `rows` token rows whose 64 hidden-unit partial sums from C CTAs sit in
+// shared memory at recv[(cc * rows + rl) * stride + col0 + u]:
+//   hidden = ReLU(sum over cc in rank order + b1);  the hidden units form 8 groups of 8, each
+//   group's partial logit is an fmaf chain over its units, and the 8 group partials are added
+//   in group order, then b2;  top k by logit (strictly greater wins, so equal logits keep the
+//   lower index);  softmax renormalised over the k, shifted by the largest.
+// Called by `nthreads` threads (a multiple of 32, thread ids 0..nthreads-1): the 8 consecutive
+// lanes of a row each take a group and the row's first lane gathers the group partials by
+// shuffles into lg_s[rl * K + a] (shared scratch), then selects and writes logits (if
+// non-null), ids and w for token t_first + rl when it is below N and `ok`.  With `coef`
+// non-null it also stores each row's per-adapter weight (w_j for a selected adapter, else 0)
+// at coef[rl * K + a].  The selection runs twice (denominator, then weights), so nothing is
+// read back from global memory; the code is kept compact because it runs once per tile.
+__device__ __forceinline__ void router_rows(const float* recv, int C, int rows, int stride, int col0,
+                                            const float* w2s, const float* b1s, const float* b2s, int K, int k,
+                                            int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
+                                            float* w, float* lg_s, float* coef, int tid, int nthreads) {
+  const int lane = tid & 31;
+  for (int base = 0; base < rows * 8; base += nthreads) {
+    const int item = base + tid;
+    const int rl = item >> 3, g = item & 7;
+    const bool valid = item < rows * 8;
+    const bool lead = valid && g == 0;
+    float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+      for (int cc = 0; cc < C; ++cc) {
+        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * rows + rl) * stride + col0 + g * 8);
+        const float4 p0 = src[0], p1 = src[1];
+        h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
+        h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = fmaxf(h[i] + b1s[g * 8 + i], 0.f);
+    }
+    for (int a = 0; a < K; ++a) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(h[i], w2s[(g * 8 + i) * K + a], s);
+      float acc = s;  // group 0's partial, then groups 1..7 in order (used by the row's first lane)
+      for (int gg = 1; gg < 8; ++gg) acc += __shfl_sync(0xffffffffu, s, (lane & ~7) + gg);
+      if (lead) lg_s[rl * K + a] = acc + b2s[a];
+    }
+    if (lead) {
+      const int64_t t = t_first + rl;
+      const float* lg = lg_s + rl * K;
+      if (coef)
+        for (int a = 0; a < K; ++a) coef[rl * K + a] = 0.f;
+      if (t < N && ok) {
+        if (logits)
+          for (int a = 0; a < K; ++a) logits[t * K + a] = lg[a];
+        float m = 0.f, denom = 0.f;
+        for (int pass = 0; pass < 2; ++pass) {
+          const float inv = pass ? 1.f / denom : 0.f;
+          uint64_t used = 0;
+          for (int js = 0; js < k; ++js) {
+            int best = -1;
+            for (int a = 0; a < K; ++a)
+              if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
+            used |= 1ull << best;
+            if (js == 0) m = lg[best];
+            const float e = expf(lg[best] - m);
+            if (pass == 0) {
+              denom += e;
+            } else {
+              const float wj = e * inv;
+              ids[t * k + js] = best;
+              w[t * k + js] = wj;
+              if (coef) coef[rl * K + best] = wj;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 }  // namespace molora

@@ -41,6 +41,12 @@ bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
 cudaError_t launch_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
                               int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
                               void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream);
+// The learned router and the dense apply in one kernel: x is read once for both.
+bool router_dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r);
+cudaError_t launch_router_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* W1,
+                                     const float* b1, const void* W2, const float* b2, const void* A, const void* B,
+                                     int32_t K, int32_t r, int32_t k, float scale, float* logits, int32_t* ids,
+                                     float* w, void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream);
 
 // CUDA-core learned router (any dtype / shape).
 cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,

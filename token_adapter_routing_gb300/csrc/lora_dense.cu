@@ -12,10 +12,12 @@
 // slot, k times per token.  No dispatch is needed.
 //
 // A tile is 64 consecutive tokens, handled by a cluster of C CTAs:
-//   1. shrink, split over d_in: CTA c gathers x[t0:t0+64, c*KS:(c+1)*KS) with 16-byte
-//      cp.async, TMA-loads the K-slices of all K adapters' A, and accumulates
-//      H = x [A_0 | ... | A_{K-1}] (K*r columns, fp32) in TMEM, one tcgen05.mma per adapter
-//      and 16-element K step (M = 128: rows past 64 are unused);
+//   1. shrink, split over d_in: CTA c gathers x[t0:t0+64, c*KS:(c+1)*KS) and the K-slices
+//      of all K adapters' A with 16-byte cp.async, the latter stacked into one MN-major
+//      operand [A_0 | ... | A_{K-1}] (K*r = 64 or 128 columns), and accumulates
+//      H = x [A_0 | ... | A_{K-1}] (fp32) in TMEM with one tcgen05.mma per 16-element K step
+//      (M = 128: rows past 64 are unused; N = K*r, so x is read from shared memory once per
+//      step rather than once per adapter);
 //   2. the C partial H are summed through distributed shared memory in rank order
 //      (deterministic), each adapter's r columns are scaled by scale * c[t,a], and the
 //      result G is split into bf16 hi + lo and sent to every CTA of the cluster;
@@ -51,62 +53,95 @@ constexpr size_t kCtrlBytes = 1024;
 constexpr uint32_t kBarX = 1;
 
 struct DensePlan {
-  int C, KS, NC, KR;       // cluster size, K-slice, output columns per CTA, K*r
-  uint32_t off_a;          // phase 1: all adapters' A slices after the x tile
+  int C, KS, NC, KR, PC;   // cluster size, K-slice, output columns per CTA, K*r, pushed columns per row
+  int rounds, KSR;         // the K-slice is gathered in `rounds` rounds of KSR columns through one buffer
+  int router;              // the learned router's 64 hidden columns ride along with the shrink
+  uint32_t off_a, off_w1;  // phase 1: the stacked A rows (and W1's rows) of a round, after its x tile
   uint32_t off_g, off_b;   // phase 2: G hi/lo tiles, two B pass buffers
   uint32_t off_s;          // epilogue staging (also the receive slots, used earlier)
   uint32_t region, smem;
+  uint32_t off_rt;         // router parameters and per-row scratch, after the control block
   uint32_t g_blk;          // bytes of one 64-column block of a G tile (128 rows x 128 B)
   uint32_t b_pass;         // bytes of one B pass buffer
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Shared memory: phase 1 holds the x tile [KS/64 blocks][64 rows][128 B] (plus room for the
-// M = 128 MMA to read 64 rows past its last block) and the adapters' A slices.  Phase 2
-// (after the shrink) reuses it for the G tiles and the B pass buffers.  The staging lines
-// of the epilogue come after both; the receive slots of the cluster reduction share them,
-// because remote CTAs may push their partials while this CTA's MMAs still read phase 1,
-// and the epilogue starts only after every partial has been consumed.
-bool dense_plan(int32_t d_in, int32_t d_out, int32_t K, int32_t r, int C, size_t budget, DensePlan* s) {
-  if (d_in % (C * kKBlock) || d_out % (C * kKBlock)) return false;
+// Per-CTA scratch (fp32): the router's W2 [64 x K], b1 [64], b2 [8] and logits [RPC][K]
+// (router variant only), and the owner rows' adapter coefficients [RPC][K].
+inline size_t router_scratch_bytes(int K, int RPC) {
+  return sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + 8 + 2 * (size_t)RPC * K);
+}
+
+// Shared memory: phase 1 holds one round's x tile [KSR/64 blocks][64 rows][128 B] (plus room
+// for the M = 128 MMA to read 64 rows past its last block), its rows of the stacked A
+// operand and, with the router, of W1.  Phase 2 (after the shrink) reuses it for the G tiles
+// and the B pass buffers.  The staging lines of the epilogue come after both and share their
+// space with the receive slots of the cluster reduction: remote CTAs push their partials
+// while this CTA's MMAs may still read phase 1, and the epilogue starts only after every
+// partial has been consumed.  Two rounds halve phase 1, which is what lets the router's 64
+// extra columns (and d_in = 4096) keep two CTAs per SM.
+bool dense_plan(int32_t d_in, int32_t d_out, int32_t K, int32_t r, int C, int rounds, size_t budget, bool router,
+                DensePlan* s) {
+  if (d_in % (C * kKBlock * rounds) || d_out % (C * kKBlock)) return false;
   s->C = C;
   s->KS = d_in / C;
+  s->rounds = rounds;
+  s->KSR = s->KS / rounds;
   s->NC = d_out / C;
   s->KR = K * r;
-  if (s->KS > 512) return false;  // one gather round
-  const size_t x_bytes = (size_t)(s->KS / kKBlock) * kTileRows * 128;
-  const size_t a_bytes = (size_t)K * s->KS * r * 2;
+  s->PC = s->KR + (router ? kRouterHidden : 0);
+  s->router = router ? 1 : 0;
+  if (s->KSR > 512) return false;
+  const size_t x_bytes = (size_t)(s->KSR / kKBlock) * kTileRows * 128;
+  const size_t a_bytes = (size_t)s->KSR * s->KR * 2;
+  const size_t w1_bytes = router ? (size_t)s->KSR * kRouterHidden * 2 : 0;
   const size_t over = (size_t)(kMmaM - kTileRows) * 128;
-  const size_t phase1 = x_bytes + (a_bytes > over ? a_bytes : over);
-  const int kblocks = (s->KR + 63) / 64;  // 64-column blocks of a G tile (KR >= 64), else one narrow tile
-  s->g_blk = (uint32_t)(kMmaM * (s->KR >= 64 ? 128 : s->KR * 2));
+  const size_t phase1 = x_bytes + (a_bytes + w1_bytes > over ? a_bytes + w1_bytes : over);
+  const int kblocks = (s->KR + 63) / 64;  // 64-column blocks of a G tile
+  s->g_blk = (uint32_t)(kMmaM * 128);
   const size_t g_bytes = 2 * (size_t)kblocks * s->g_blk;
   s->b_pass = (uint32_t)((kPassW / 64) * s->KR * 128);
   const size_t phase2 = align_up(g_bytes, 1024) + 2 * (size_t)s->b_pass;
   const size_t stage = (size_t)kTileRows * (kPiece * 4 + 16);
-  const size_t recv = (size_t)kTileRows * s->KR * 4;
+  const size_t recv = (size_t)kTileRows * s->PC * 4;
   s->off_a = (uint32_t)x_bytes;
+  s->off_w1 = (uint32_t)(x_bytes + a_bytes);
   s->off_g = 0;
   s->off_b = (uint32_t)align_up(g_bytes, 1024);
   s->off_s = (uint32_t)align_up(phase1 > phase2 ? phase1 : phase2, 1024);
   s->region = (uint32_t)align_up(s->off_s + (stage > recv ? stage : recv), 1024);
-  s->smem = s->region + (uint32_t)kCtrlBytes + 1024;
+  s->off_rt = s->region + (uint32_t)kCtrlBytes;
+  s->smem = (uint32_t)(s->off_rt + align_up(router_scratch_bytes(K, kTileRows / C), 16) + 1024);
   return s->smem <= budget;
 }
 
-bool dense_choose(int32_t d_in, int32_t d_out, int32_t K, int32_t r, DensePlan* s) {
-  // K*r = 256 would need 128 KB of G tiles alone (hi and lo, M = 128 rows): it never fits
-  if (!(r == 16 || r == 32 || r == 64) || K * r > 128 || (K * r) % 16) return false;
+// Two CTAs per SM first (clusters of 8 first, one round first), else one per SM.
+bool dense_choose(int32_t d_in, int32_t d_out, int32_t K, int32_t r, bool router, DensePlan* s) {
+  // K*r = 256 would need 128 KB of G tiles alone (hi and lo, M = 128 rows): it never fits.
+  // The stacked shrink operand is made of 64-column blocks: K*r is 64 or 128.
+  if (!(r == 16 || r == 32 || r == 64) || (K * r != 64 && K * r != 128)) return false;
   for (size_t budget : {kTwoPerSm, kMaxSmem})
     for (int C : {8, 4, 2, 1})
-      if (dense_plan(d_in, d_out, K, r, C, budget, s)) return true;
+      for (int rounds : {1, 2})
+        if (dense_plan(d_in, d_out, K, r, C, rounds, budget, router, s)) return true;
   return false;
 }
 
+// The learned router's parameters and outputs, for the fused variant (router + apply).
+struct RouterIo {
+  const __nv_bfloat16* W2;  // [64 x K]
+  const float* b1;          // [64] or null
+  const float* b2;          // [K] or null
+  float* logits;            // [N x K] or null
+  int32_t* ids;             // [N x k]
+  float* w;                 // [N x k]
+};
+
 struct __align__(8) DCtrl {
-  uint64_t bar_a;        // TMA of all adapters' A slices
+  uint64_t bar_a;        // TMA of W1's slice (router variant)
   uint64_t bar_x;        // shrink MMAs done
+  uint64_t bar_round;    // shrink MMAs of a round done: its buffer may be refilled (one phase per round)
   uint64_t bar_bp[2];    // B pass buffer loaded (one phase per use)
   uint64_t bar_full[2];  // expand pass done, per TMEM buffer
   uint64_t bar_empty[2]; // epilogue drained a TMEM buffer
@@ -124,16 +159,21 @@ __device__ __forceinline__ SmemLayout layout_for_row_bytes(uint32_t row_bytes) {
 
 }  // namespace
 
+// kRouter = false: ids and w are given.  kRouter = true: the kernel also runs the learned
+// router on the same x tile (its W1 product is 64 more columns of the shrink) and writes
+// logits, ids and w before using them.
+template <bool kRouter>
 __global__ void __launch_bounds__(kThreads, 1)
     lora_dense_kernel(const __nv_bfloat16* __restrict__ x, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
                       int32_t r, int32_t k, const int32_t* __restrict__ ids, const float* __restrict__ w,
                       float scale, void* __restrict__ y, int32_t y_bf16, const DensePlan P, int32_t* err_word,
-                      const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b) {
+                      const RouterIo rio, const __nv_bfloat16* __restrict__ A,
+                      const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_w1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DCtrl* ctrl = reinterpret_cast<DCtrl*>(sm + P.region);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = P.C, KS = P.KS, NC = P.NC, KR = P.KR;
+  const int C = P.C, KS = P.KS, NC = P.NC, KR = P.KR, PC = P.PC, R = P.rounds, KSR = P.KSR;
   const int crank = (int)cluster_ctarank();
   const int64_t t0 = (int64_t)(blockIdx.x / C) * kTileRows;
   const int nvalid = (int)(N - t0 < kTileRows ? N - t0 : kTileRows);
@@ -142,15 +182,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* xs = sm;
   uint8_t* as = sm + P.off_a;
+  uint8_t* w1s = sm + P.off_w1;
   uint8_t* g_hi = sm + P.off_g;
   const int gblocks = (KR + 63) / 64;
   uint8_t* g_lo = g_hi + (size_t)gblocks * P.g_blk;
   const uint32_t g_row_bytes = KR >= 64 ? 128u : (uint32_t)KR * 2u;
   uint8_t* bs = sm + P.off_b;
   uint8_t* stage = sm + P.off_s;
-  float* recv = reinterpret_cast<float*>(sm + P.off_s);  // [C sources][64/C rows][KR], before the epilogue
+  float* recv = reinterpret_cast<float*>(sm + P.off_s);  // [C sources][64/C rows][PC], before the epilogue
   const uint32_t stage_stride = (uint32_t)kPiece * 4u + 16u;
   const int RPC = kTileRows / C;
+  // router scratch: W2 and the biases as fp32, partial logits, per-row adapter coefficients
+  float* w2s = reinterpret_cast<float*>(sm + P.off_rt);
+  float* b1s = w2s + kRouterHidden * K;
+  float* b2s = b1s + kRouterHidden;
+  float* lg_s = b2s + 8;          // [RPC][K] logits
+  float* coef_s = lg_s + RPC * K;  // [RPC][K]
 
   if (warp == 4) {
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -158,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_init(&ctrl->bar_a, 1);
       mbar_init(&ctrl->bar_x, 1);
+      mbar_init(&ctrl->bar_round, 1);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&ctrl->bar_bp[i], 1);
         mbar_init(&ctrl->bar_full[i], 1);
@@ -166,11 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctrl->bar_recv, 1);
       mbar_init(&ctrl->bar_g, 1);
       mbar_fence_init();
-      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)kTileRows * KR * 4u);
+      mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)kTileRows * PC * 4u);
       mbar_arrive_expect_tx(&ctrl->bar_g, (uint32_t)kTileRows * KR * 4u);
       ctrl->abort = 0;
-      tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b);
+      if (kRouter) tma_prefetch_desc(&map_w1);
     }
   }
   pdl_wait();
@@ -182,56 +230,105 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   cluster_arrive();  // barriers of every CTA initialised and armed
 
-  // ---- shrink
-  if (warp == 4 && lane == 0) {
-    mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)K * KS * r * 2);
-    for (int a = 0; a < K; ++a)
-      for (int kb = 0; kb < KS / kKBlock; ++kb)
-        tma_load_2d(smem_u32(as + ((size_t)a * KS + (size_t)kb * kKBlock) * r * 2), &map_a, 0,
-                    a * d_in + crank * KS + kb * kKBlock, &ctrl->bar_a);
-  }
-  if (warp < 4) {
-    const int sub = lane >> 3, chunk = lane & 7;
-    for (int kb = 0; kb < KS / kKBlock; ++kb) {
-      const uint32_t blk = smem_u32(xs + (size_t)kb * kTileRows * 128);
-      const int col = crank * KS + kb * kKBlock + chunk * 8;
-#pragma unroll 4
-      for (int it = 0; it < kTileRows / 16; ++it) {
-        const int row = it * 16 + warp * 4 + sub;
-        const int32_t tok = ctrl->tok[row];
-        const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
-        cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
+  // ---- shrink, in R rounds of KSR columns through one buffer
+  auto load_w1 = [&](int rd) {  // W1 rows of round rd: 64 x 64 boxes landing MN-major (128-byte
+                                // swizzle), one more 64-column block right after the stacked A blocks
+    mbar_arrive_expect_tx(&ctrl->bar_a, (uint32_t)KSR * kRouterHidden * 2);
+    for (int kb = 0; kb < KSR / kKBlock; ++kb)
+      tma_load_2d(smem_u32(w1s + (size_t)kb * kKBlock * 128), &map_w1, 0, crank * KS + rd * KSR + kb * kKBlock,
+                  &ctrl->bar_a);
+  };
+  if (kRouter && warp == 4 && lane == 0) load_w1(0);
+  bool shrink_ok = true;
+  for (int rd = 0; rd < R; ++rd) {
+    if (warp < 4) {
+      if (rd > 0 && !mbar_wait(&ctrl->bar_round, (uint32_t)(rd - 1) & 1u)) {  // the buffer is free again
+        ctrl->abort = 1;
+        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
       }
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-  named_barrier(kBarX, kThreads);  // the x tile is in shared memory
-  if (warp == 4 && lane == 0) {
-    bool ok = mbar_wait(&ctrl->bar_a, 0);
-    tc_fence_after();
-    if (ok) {
-      const uint32_t atom = 8u * r * 2u;
-      const SmemLayout swz = layout_for_row_bytes((uint32_t)r * 2u);
-      const uint32_t idesc = idesc_bf16_f32(kMmaM, r, false, true);
-      for (int kb = 0; kb < KS / kKBlock; ++kb)
-        for (int ks = 0; ks < kKBlock / 16; ++ks) {
-          // 128 MMA rows from the block's start: the tile's 64 rows, then 64 unused rows
-          const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileRows * 128 + ks * 32), 16, 1024,
-                                        kSwizzle128B);
-          const int krow = kb * kKBlock + ks * 16;
-          for (int a = 0; a < K; ++a) {
-            const uint64_t db = smem_desc(smem_u32(as + ((size_t)a * KS + krow) * r * 2), atom, atom, swz);
-            umma_f16(tmem + (uint32_t)(a * r), da, db, idesc, (kb | ks) != 0);
-          }
+      const int sub = lane >> 3, chunk = lane & 7;
+      for (int kb = 0; kb < KSR / kKBlock; ++kb) {
+        const uint32_t blk = smem_u32(xs + (size_t)kb * kTileRows * 128);
+        const int col = crank * KS + rd * KSR + kb * kKBlock + chunk * 8;
+#pragma unroll 4
+        for (int it = 0; it < kTileRows / 16; ++it) {
+          const int row = it * 16 + warp * 4 + sub;
+          const int32_t tok = ctrl->tok[row];
+          const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
+          cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
         }
-      umma_commit(&ctrl->bar_x);
-    } else {
-      ctrl->abort = 1;
-      report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
-      mbar_arrive(&ctrl->bar_x);
+      }
+      // every adapter's rows of this round, stacked as one MN-major [KSR x K*r] operand:
+      // 64-column blocks of KSR rows x 128 B with the 128-byte swizzle (column a*r + j is A_a[., j])
+      const int cpr = r / 8;  // 16-byte chunks per adapter row
+      const int per_a = KSR * cpr;
+      for (int q = tid; q < K * per_a; q += kEpilogueThreads) {
+        const int a = q / per_a, rem = q - a * per_a, i = rem / cpr, c = rem - i * cpr;
+        const int n = a * r + c * 8;
+        cp_async_16(smem_u32(as + (size_t)(n / 64) * KSR * 128 + sw128_offset(i, (n % 64) / 8)),
+                    A + ((int64_t)a * d_in + crank * KS + rd * KSR + i) * r + c * 8, 16u);
+      }
+      cp_async_commit();
+      if (rd == 0 && !kRouter) {
+        // the owner rows' coefficients sum_j [ids[t,j] == a] w[t,j], while the gather is in flight
+        for (int q = tid; q < RPC * K; q += kEpilogueThreads) {
+          const int rl = q / K, a = q - rl * K;
+          const int64_t t = t0 + crank * RPC + rl;
+          float c = 0.f;
+          if (t < N) {
+            for (int j = 0; j < k; ++j) {
+              const int32_t id = ids[t * k + j];
+              if (id == a) c += w ? w[t * k + j] : 1.f;
+              if ((id < 0 || id >= K) && a == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
+            }
+          }
+          coef_s[q] = c;
+        }
+      }
+      if (rd == 0 && kRouter) {  // the router's second layer, while the gather is in flight
+        for (int i = tid; i < kRouterHidden * K; i += kEpilogueThreads) w2s[i] = __bfloat162float(rio.W2[i]);
+        if (tid < kRouterHidden) b1s[tid] = rio.b1 ? rio.b1[tid] : 0.f;
+        if (tid < K) b2s[tid] = rio.b2 ? rio.b2[tid] : 0.f;
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    named_barrier(kBarX, kThreads);  // round rd's x, A (and the coefficients or W2) are in shared memory
+    if (warp == 4 && lane == 0) {
+      if (shrink_ok && kRouter) shrink_ok = mbar_wait(&ctrl->bar_a, (uint32_t)rd & 1u);
+      shrink_ok = shrink_ok && !ctrl->abort;
+      tc_fence_after();
+      if (shrink_ok) {
+        // one MMA per 16-row K step over all adapters at once (and the router's W1): the x
+        // tile is read once per step, not once per adapter.  TMEM columns [0, K*r) take x A_a
+        // for every adapter in order, [K*r, K*r + 64) the router's hidden partials.
+        const uint32_t idesc = idesc_bf16_f32(kMmaM, (uint32_t)PC, false, true);
+        for (int kb = 0; kb < KSR / kKBlock; ++kb)
+          for (int ks = 0; ks < kKBlock / 16; ++ks) {
+            // 128 MMA rows from the block's start: the tile's 64 rows, then 64 unused rows
+            const uint64_t da = smem_desc(smem_u32(xs + (size_t)kb * kTileRows * 128 + ks * 32), 16, 1024,
+                                          kSwizzle128B);
+            const uint64_t db = smem_desc(smem_u32(as + (size_t)kb * kKBlock * 128 + ks * 2048),
+                                          (uint32_t)KSR * 128u, 1024, kSwizzle128B);
+            umma_f16(tmem, da, db, idesc, (rd | kb | ks) != 0);
+          }
+      }
+      if (rd + 1 < R) {
+        // this round's MMAs release the buffer; the last round's completion is bar_x
+        if (shrink_ok) umma_commit(&ctrl->bar_round);
+        else mbar_arrive(&ctrl->bar_round);
+        if (kRouter && shrink_ok) {
+          shrink_ok = mbar_wait(&ctrl->bar_round, (uint32_t)rd & 1u);
+          if (shrink_ok) load_w1(rd + 1);
+        }
+      } else if (shrink_ok) {
+        umma_commit(&ctrl->bar_x);
+      } else {
+        ctrl->abort = 1;
+        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+        mbar_arrive(&ctrl->bar_x);
+      }
     }
   }
   const int npass = (NC + kPassW - 1) / kPassW;
@@ -269,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 2) {  // rows 0..63
     const int row = tid;
     const uint32_t owner = (uint32_t)(row / RPC);
-    const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * KR), owner);
+    const uint32_t dst = dsmem_addr(smem_u32(recv + ((size_t)crank * RPC + (row % RPC)) * PC), owner);
     const uint32_t dst_bar = dsmem_addr(smem_u32(&ctrl->bar_recv), owner);
     float v[16];
-    for (int c0 = 0; c0 < KR; c0 += 16) {
+    for (int c0 = 0; c0 < PC; c0 += 16) {
       if (have_h)
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
       else
@@ -293,25 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctrl->abort = 1;
       report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
     }
+    if (kRouter) {
+      // the learned router for the owner's rows: hidden units from the C partials,
+      // logits, top k and softmax; logits, ids and w go out, the coefficients to scratch
+      router_rows(recv, C, RPC, PC, KR, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have_h, rio.logits,
+                  rio.ids, rio.w, lg_s, coef_s, tid, kEpilogueThreads);
+      named_barrier(2, kEpilogueThreads);  // coefficients ready
+    }
     // owner: rows [crank*RPC, (crank+1)*RPC) of the tile; each item is 8 columns of one row
     const int groups = KR / 8;
     for (int item = tid; item < RPC * groups; item += kEpilogueThreads) {
       const int rl = item / groups, c0 = (item % groups) * 8;
       const int trow = crank * RPC + rl;
       const int a = c0 / r;
-      float coef = 0.f;
-      const int64_t t = t0 + trow;
-      if (t < N) {
-        for (int j = 0; j < k; ++j) {
-          const int32_t id = ids[t * k + j];
-          if (id == a) coef += w ? w[t * k + j] : 1.f;
-          if ((id < 0 || id >= K) && a == 0 && crank == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
-        }
-      }
-      coef *= scale;
+      const float coef = coef_s[rl * K + a] * scale;
       float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int cc = 0; cc < C; ++cc) {
-        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * RPC + rl) * KR + c0);
+        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * RPC + rl) * PC + c0);
         const float4 p0 = src[0], p1 = src[1];
         h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
         h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
@@ -472,7 +567,13 @@ bool dense_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
   (void)N;
   DensePlan s;
-  return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, &s) && dense_encoder() != nullptr;
+  return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, false, &s) && dense_encoder() != nullptr;
+}
+
+bool router_dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
+  (void)N;
+  DensePlan s;
+  return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, true, &s) && dense_encoder() != nullptr;
 }
 
 // Where the dense path beat the grouped one on GB300 (top-2, r = 16, L2 flushed): with a plan
@@ -480,36 +581,67 @@ bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
 // One CTA per SM (d_in = 4096 at K*r = 64) leaves too few clusters resident, and small batches
 // pay for the extra adapters: the grouped path won all of those points.
 bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
-  if (dtype != MOLORA_BF16 || N < 2048 || !(r == 16 || r == 32 || r == 64) || K * r > 128) return false;
+  if (dtype != MOLORA_BF16 || N < 2048 || !(r == 16 || r == 32 || r == 64) || (K * r != 64 && K * r != 128))
+    return false;
   DensePlan s;
   for (int C : {8, 4, 2, 1})
-    if (dense_plan(d_in, d_out, K, r, C, kTwoPerSm, &s)) return dense_encoder() != nullptr;
+    if (dense_plan(d_in, d_out, K, r, C, 1, kTwoPerSm, false, &s)) return dense_encoder() != nullptr;
   return false;
 }
 
-cudaError_t launch_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
-                              int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
-                              void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
+                         int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale, void* y,
+                         bool y_bf16, int32_t* err_word, const void* W1, const RouterIo& rio, cudaStream_t stream) {
+  const bool router = W1 != nullptr;
   DensePlan s;
-  if (!dense_choose(d_in, d_out, K, r, &s)) return cudaErrorNotSupported;
-  CUtensorMap map_a, map_b;
-  const CUtensorMapSwizzle swa =
-      r == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!dense_map(&map_a, A, (uint64_t)K * d_in, (uint64_t)r, (uint32_t)r, kKBlock, swa)) return cudaErrorInvalidValue;
+  if (!dense_choose(d_in, d_out, K, r, router, &s)) return cudaErrorNotSupported;
+  CUtensorMap map_b, map_w1;
   // B seen as [K*r x d_out]: a box is all K*r rows (every adapter) by 64 columns
   if (!dense_map(&map_b, B, (uint64_t)K * r, (uint64_t)d_out, 64, (uint32_t)(K * r), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (router) {
+    // W1 [d_in x 64]: boxes of 64 rows x 64 columns (128 B rows, 128-byte swizzle)
+    if (!dense_map(&map_w1, W1, (uint64_t)d_in, kRouterHidden, kRouterHidden, kKBlock, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
+    std::memset(&map_w1, 0, sizeof(map_w1));
+  }
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(lora_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    attr_err = cudaFuncSetAttribute(lora_dense_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(lora_dense_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kMaxSmem);
     if (attr_err != cudaSuccess) cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles = (N + kTileRows - 1) / kTileRows;
-  return launch_kernel(lora_dense_kernel, dim3((unsigned)(tiles * s.C)), dim3(kThreads), s.smem, stream, s.C,
-                       static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K, r, k, ids, w, scale, y,
-                       (int32_t)(y_bf16 ? 1 : 0), s, err_word, map_a, map_b);
+  return launch_kernel(router ? lora_dense_kernel<true> : lora_dense_kernel<false>, dim3((unsigned)(tiles * s.C)),
+                       dim3(kThreads), s.smem, stream, s.C, static_cast<const __nv_bfloat16*>(x), N, d_in, d_out, K,
+                       r, k, ids, w, scale, y, (int32_t)(y_bf16 ? 1 : 0), s, err_word, rio,
+                       static_cast<const __nv_bfloat16*>(A), map_b, map_w1);
+}
+
+}  // namespace
+
+cudaError_t launch_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
+                              int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
+                              void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream) {
+  const RouterIo none = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  return launch_dense(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, err_word, nullptr, none, stream);
+}
+
+cudaError_t launch_router_lora_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* W1,
+                                     const float* b1, const void* W2, const float* b2, const void* A, const void* B,
+                                     int32_t K, int32_t r, int32_t k, float scale, float* logits, int32_t* ids,
+                                     float* w, void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream) {
+  const RouterIo rio = {static_cast<const __nv_bfloat16*>(W2), b1, b2, logits, ids, w};
+  return launch_dense(x, N, d_in, d_out, A, B, K, r, nullptr, nullptr, k, scale, y, y_bf16, err_word, W1, rio,
+                      stream);
 }
 
 }  // namespace molora

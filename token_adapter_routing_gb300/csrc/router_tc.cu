@@ -10,8 +10,9 @@
 // with st.async (counted by the owner's mbarrier), and the owner sums the C partials in rank
 // order (deterministic).  The owner's 128 threads then split each token's 64 hidden units
 // into 8 groups: ReLU, partial logits over the group's 8 units, and a fixed-order sum of the
-// 8 group partials; one thread per token selects the top k (strictly greater wins, so equal
-// logits keep the lower index) and renormalises the softmax over the k.
+// 8 group partials (combined by warp shuffles); one thread per token selects the top k
+// (strictly greater wins, so equal logits keep the lower index) and renormalises the softmax
+// over the k (router_rows in common.cuh, shared with the fused router + apply kernel).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -26,7 +27,6 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kKBlock = 64;
 constexpr int kThreads = 160;
-constexpr int kGroups = 8;  // hidden units per token split into 8 groups of 8
 constexpr uint32_t kTmemCols = 64;
 constexpr size_t kMaxSmem = 227 * 1024;
 constexpr size_t kTwoPerSm = 113 * 1024;
@@ -47,8 +47,8 @@ bool plan(int32_t d_in, int32_t K, int C, size_t budget, RouterShape* s) {
     s->XR = XR;
     s->off_w1 = (size_t)XR * kTileM * 2;
     const size_t phase1 = s->off_w1 + (size_t)XR * kRouterHidden * 2;
-    // partial logits of the owner's rows reuse the phase-1 space (x and W1 are consumed by then)
-    const size_t plog = (size_t)(kTileM / C) * kGroups * K * 4;
+    // the logits of the owner's rows reuse the phase-1 space (x and W1 are consumed by then)
+    const size_t plog = (size_t)(kTileM / C) * K * 4;
     // receive slots: other CTAs may push while this CTA's tensor core still reads x
     s->off_recv = align_up(phase1 > plog ? phase1 : plog, 1024);
     s->off_w2 = s->off_recv + (size_t)kTileM * kRouterHidden * 4;
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   RCtrl* ctrl = reinterpret_cast<RCtrl*>(sm + region);
   uint8_t* xs = sm;
   uint8_t* w1s = sm + off_w1;
-  float* plog = reinterpret_cast<float*>(sm);  // [RPC rows][8 groups][K], after the MMA
+  float* plog = reinterpret_cast<float*>(sm);  // [RPC rows][K] logits, after the MMA
   float* recv = reinterpret_cast<float*>(sm + off_recv);  // [C sources][RPC rows][64]
   float* w2s = reinterpret_cast<float*>(sm + off_w2);
   float* b1s = w2s + kRouterHidden * K;
@@ -194,58 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     const bool got = mbar_wait(&ctrl->bar_recv, 0);
-    // owner: hidden unit group (row, g) -> ReLU -> partial logits over the group's 8 units
-    for (int item = tid; item < RPC * kGroups; item += kTileM) {
-      const int rl = item / kGroups, g = item % kGroups;
-      float h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = 0.f;
-      for (int cc = 0; cc < C; ++cc) {
-        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * RPC + rl) * kRouterHidden + g * 8);
-        const float4 p0 = src[0], p1 = src[1];
-        h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
-        h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = fmaxf(h[i] + b1s[g * 8 + i], 0.f);
-      float* dstp = plog + ((size_t)rl * kGroups + g) * K;
-      for (int a = 0; a < K; ++a) {
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s = fmaf(h[i], w2s[(g * 8 + i) * K + a], s);
-        dstp[a] = s;
-      }
-    }
-    named_barrier(1, kTileM);  // partial logits of the owner's rows are in shared memory
-    if (tid < RPC) {
-      const int rl = tid;
-      const int64_t t = t0 + crank * RPC + rl;
-      if (t < N && got && have) {
-        float* lg = plog + (size_t)rl * kGroups * K;  // group 0's slot collects the sum
-        for (int a = 0; a < K; ++a) {
-          float s = lg[a];
-          for (int g = 1; g < kGroups; ++g) s += lg[g * K + a];
-          s += b2s[a];
-          lg[a] = s;
-          if (logits) logits[t * K + a] = s;
-        }
-        uint64_t used = 0;
-        float m = 0.f, denom = 0.f;
-        for (int js = 0; js < k; ++js) {
-          int best = -1;
-          for (int a = 0; a < K; ++a)
-            if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
-          used |= 1ull << best;
-          if (js == 0) m = lg[best];
-          const float e = expf(lg[best] - m);
-          ids[t * k + js] = best;
-          w[t * k + js] = e;
-          denom += e;
-        }
-        const float inv = 1.f / denom;
-        for (int js = 0; js < k; ++js) w[t * k + js] *= inv;
-      }
-    }
+    // owner: ReLU, logits, top k and softmax for this CTA's rows (plog holds the logit rows)
+    router_rows(recv, C, RPC, kRouterHidden, 0, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have, logits, ids,
+                w, plog, nullptr, tid, kTileM);
   }
   __syncwarp();
   __syncthreads();
