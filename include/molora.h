@@ -154,6 +154,30 @@ MOLORA_API molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t
                                           int32_t* perm, int32_t* err_word, cudaStream_t stream);
 
 /*
+ * molora_route_vocab_lora_apply -- the whole vocabulary-routed step: molora_route_vocab_dispatch
+ * followed by molora_lora_apply on its outputs (k = 1, weights 1), with the same results:
+ *
+ *   adapter, counts, offsets, perm   as molora_route_vocab_dispatch(tok, N, starts, K)
+ *   y[t,:] += scale * (x[t,:] A_{adapter[t]}) B_{adapter[t]}   for every routed token
+ *
+ * Two kernels, enqueued back to back on `stream`: the routing + dispatch kernel, then the
+ * apply on the path molora_lora_apply would choose.  (Routing inside the apply, every CTA
+ * routing all N tokens for its own tile, measured slower on GB300 at 2048 tokens: the
+ * redundant routing costs more than the launch it saves.)
+ *
+ * tok int32 [N];  starts int32 [K+1];  x, A, B, r, d_in, d_out, scale as molora_lora_apply;
+ * y fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1) [N x d_out], updated in place;
+ * adapter int32 [N], counts int32 [K], offsets int32 [K+1], perm int32 [N]: outputs, all
+ * required.  Error bits as the two calls.
+ */
+MOLORA_API molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64_t N, const int32_t* starts,
+                                            int32_t K, const void* x, molora_dtype dtype, int32_t d_in,
+                                            int32_t d_out, const void* A, const void* B, int32_t r,
+                                            float scale, void* y, int32_t y_bf16, int32_t* adapter,
+                                            int32_t* counts, int32_t* offsets, int32_t* perm,
+                                            int32_t* err_word, cudaStream_t stream);
+
+/*
  * molora_lora_apply -- batched per-token LoRA apply over the hot set (Figure 2; Table 10
  * shapes; Figure 4 hot set):
  *

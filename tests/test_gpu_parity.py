@@ -412,6 +412,78 @@ def test_apply_dense_bf16y(m):
     assert_bf16y_close(y, y0b, y_ref, 2)
 
 
+# ------------------------------------------------------------------------- the whole vocabulary-routed step
+
+@pytest.mark.parametrize("name,kw,outside", [
+    ("modality4", {}, False),
+    ("modality4", {"N": 333, "d_in": 1024, "d_out": 2048, "r": 32}, True),  # tokens in no range
+    ("modality4", {"N": 8193, "d_in": 512, "d_out": 512}, True),
+    ("decode_sweep", {"N": 100, "K": 16}, False),                           # the scalar path
+    ("modality4", {"dist": "95-2-2-1"}, False),
+])
+def test_route_vocab_lora_apply_step(m, name, kw, outside):
+    wl = workloads.make(name, **kw)
+    starts = wl.starts.clone()
+    if outside:  # shrink the last range so that some tokens fall outside every range
+        starts[-1] = starts[-2] + (starts[-1] - starts[-2]) // 2
+    tok, st = dev(wl.tok), dev(starts)
+    x, A, B = dev(wl.x), dev(wl.A), dev(wl.B)
+    y1, y2 = dev(wl.y0).clone(), dev(wl.y0).clone()
+    e1, e2 = err_word(), err_word()
+    adapter, counts, offsets, perm = m.molora_route_vocab_lora_apply(tok, st, x, A, B, y1, wl.scale, err_word=e1)
+    a2, c2, o2, p2 = m.molora_route_vocab_dispatch(tok, st, err_word=e2)
+    m.molora_lora_apply(x, A, B, a2, y2, wl.scale, counts=c2, offsets=o2, perm=p2, err_word=e2)
+    torch.cuda.synchronize()
+    ref_a, n_out = oracle.route_vocab(wl.tok, starts)
+    rc, ro, rp, _ = oracle.dispatch(ref_a, wl.K)
+    assert torch.equal(adapter.cpu(), ref_a)
+    assert torch.equal(counts.cpu(), rc) and torch.equal(offsets.cpu(), ro) and torch.equal(perm.cpu(), rp)
+    assert int(e1.item()) == int(e2.item())
+    assert (n_out > 0) == outside
+    if outside:
+        assert int(e1.item()) == m.DEV_TOKEN_OUTSIDE_RANGES | m.DEV_BAD_ADAPTER_ID
+    else:
+        assert int(e1.item()) == 0
+    # the same kernels on the same inputs: the step equals the two calls bit for bit
+    assert torch.equal(y1.cpu(), y2.cpu())
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ref_a, wl.y0, wl.scale)  # skips tokens in no range
+    assert_apply_close(y1, y_ref)
+
+
+def test_route_vocab_lora_apply_step_bf16y_graph_and_empty(m):
+    wl = workloads.make("modality4", N=1500, d_in=1024, d_out=1536)
+    tok, st, x, A, B = dev(wl.tok), dev(wl.starts), dev(wl.x), dev(wl.A), dev(wl.B)
+    y0b = wl.y0.to(torch.bfloat16)
+    yb = dev(y0b).clone()
+    m.molora_route_vocab_lora_apply(tok, st, x, A, B, yb, wl.scale)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl), y0b.float(), wl.scale)
+    assert_bf16y_close(yb, y0b, y_ref, 2)
+    # captured once, replayed: the same result each time
+    yg = dev(wl.y0).clone()
+    outs = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (wl.N, wl.K, wl.K + 1, wl.N)]
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            m.molora_route_vocab_lora_apply(tok, st, x, A, B, yg, wl.scale, *outs)
+    results = []
+    for rep in range(3):
+        yg.copy_(dev(wl.y0))
+        graph.replay()
+        torch.cuda.synchronize()
+        results.append(yg.cpu().clone())
+    assert torch.equal(results[0], results[1]) and torch.equal(results[0], results[2])
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, outs[0]), wl.y0, wl.scale)
+    assert_apply_close(results[0], y_ref)
+    # N = 0 writes the empty histogram
+    counts = torch.full((wl.K,), 7, dtype=torch.int32, device="cuda")
+    offsets = torch.full((wl.K + 1,), 7, dtype=torch.int32, device="cuda")
+    m.molora_route_vocab_lora_apply(tok[:0], st, x[:0], A, B, yg[:0], wl.scale, counts=counts, offsets=offsets)
+    torch.cuda.synchronize()
+    assert int(counts.abs().sum()) == 0 and int(offsets.abs().sum()) == 0
+
+
 # ------------------------------------------------------------------------- indirect layout
 
 def separate_adapters(wl):

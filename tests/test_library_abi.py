@@ -138,4 +138,14 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert fused(dtype=0) == UNSUPPORTED and fused(K=16, r=16) == UNSUPPORTED and fused(r=8) == UNSUPPORTED
     assert lib.molora_router_lora_apply(None, 1, 0, 512, 512, None, None, None, None, None, None, 4, 16, 2, 2.0,
                                         None, None, None, None, 0, None, None) == 0
+    # the whole vocabulary-routed step: null outputs, bad K, odd y
+    lib.molora_route_vocab_lora_apply.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P, P,
+                                                  P, P]
+
+    def step(K=4, starts=fake, counts=fake, perm=fake, y=fake):
+        return lib.molora_route_vocab_lora_apply(fake, 64, starts, K, fake, 1, 512, 512, fake, fake, 16, 2.0, y, 0,
+                                                 fake, counts, fake, perm, None, None)
+
+    assert step(starts=None) == INVALID and step(counts=None) == INVALID and step(perm=None) == INVALID
+    assert step(K=0) == INVALID and step(K=65) == INVALID and step(y=odd) == INVALID
     assert lib.molora_status_string(1) == b"invalid argument"

@@ -43,7 +43,7 @@ MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-            "molora_lora_apply", "molora_router_lora_apply",
+            "molora_lora_apply", "molora_router_lora_apply", "molora_route_vocab_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect", "molora_lora_apply_masked_pass", "molora_select_path",
             "molora_status_string", "molora_version", "molora_selftest_bounded_wait")
 
@@ -82,6 +82,8 @@ def load_library():
                                                P, S, P]
     lib.molora_router_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32, F, P, P, P, P,
                                              I32, P, P]
+    lib.molora_route_vocab_lora_apply.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P, P,
+                                                  P, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
     lib.molora_status_string.argtypes = [S]
@@ -261,6 +263,43 @@ def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None,
         _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(ids), _p(w), k, _p(counts), _p(offsets),
         _p(perm), float(scale), _p(y), _p(err_word), PATHS[path], _stream(stream)))
     return y
+
+
+def molora_route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter=None, counts=None, offsets=None,
+                                  perm=None, err_word=None, stream=None):
+    """The whole vocabulary-routed step in one call: routing, dispatch and the apply (k = 1).
+    Returns (adapter, counts, offsets, perm); y (fp32 or bf16) is updated in place."""
+    _cuda(tok, "tok", torch.int32, 1)
+    _cuda(starts, "starts", torch.int32, 1)
+    N, K = tok.numel(), starts.numel() - 1
+    _cuda(x, "x", None, 2)
+    if x.shape[0] != N:
+        raise ValueError("x must have one row per token")
+    d_in = x.shape[1]
+    _cuda(A, "A", x.dtype, 3)
+    _cuda(B, "B", x.dtype, 3)
+    if A.shape[0] != K or A.shape[1] != d_in or B.shape[:2] != (K, A.shape[2]):
+        raise ValueError("A must be [K, d_in, r] and B [K, r, d_out], with K = len(starts) - 1")
+    r, d_out = A.shape[2], B.shape[2]
+    _cuda(y, "y", None, 2)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"y must be float32 or bfloat16, got {y.dtype}")
+    dev = tok.device
+    if adapter is None:
+        adapter = torch.empty(N, dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty(K, dtype=torch.int32, device=dev)
+    if offsets is None:
+        offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
+    if perm is None:
+        perm = torch.empty(N, dtype=torch.int32, device=dev)
+    for name, t in (("adapter", adapter), ("counts", counts), ("offsets", offsets), ("perm", perm)):
+        _cuda(t, name, torch.int32)
+    _check("molora_route_vocab_lora_apply", load_library().molora_route_vocab_lora_apply(
+        _p(tok), N, _p(starts), K, _p(x), _dtype_code(x), d_in, d_out, _p(A), _p(B), r, float(scale), _p(y),
+        1 if y.dtype == torch.bfloat16 else 0, _p(adapter), _p(counts), _p(offsets), _p(perm), _p(err_word),
+        _stream(stream)))
+    return adapter, counts, offsets, perm
 
 
 def molora_router_lora_apply(x, W1, W2, A, B, k, y, scale, b1=None, b2=None, logits=None, ids=None, w=None,

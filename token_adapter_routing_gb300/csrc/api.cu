@@ -120,6 +120,23 @@ molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t N, const i
   return launched(launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, stream));
 }
 
+molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                            const void* x, molora_dtype dtype, int32_t d_in, int32_t d_out,
+                                            const void* A, const void* B, int32_t r, float scale, void* y,
+                                            int32_t y_bf16, int32_t* adapter, int32_t* counts, int32_t* offsets,
+                                            int32_t* perm, int32_t* err_word, cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, tok, 1, y);
+  if (st != MOLORA_OK) return st;
+  if (!starts || !counts || !offsets || (N > 0 && (!adapter || !perm))) return MOLORA_ERR_INVALID_ARG;
+  if (N == 0)  // the empty histogram, as molora_route_vocab_dispatch writes it
+    return launched(launch_route_vocab_dispatch(tok, 0, starts, K, adapter, counts, offsets, perm, err_word, stream));
+  const molora_path path = molora_select_path(dtype, N, d_in, d_out, K, r, 1);
+  if (launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, stream) != cudaSuccess)
+    return MOLORA_ERR_CUDA;
+  return apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, adapter, nullptr, 1, counts, offsets, perm, scale, y,
+                    y_bf16 != 0, err_word, path, stream);
+}
+
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
                                int32_t k) {
   if (k >= 2 && dense_preferred(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;

@@ -576,16 +576,19 @@ bool router_dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t
   return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, true, &s) && dense_encoder() != nullptr;
 }
 
-// Where the dense path beat the grouped one on GB300 (top-2, r = 16, L2 flushed): with a plan
-// of two CTAs per SM and at least a few thousand tokens (2048 -> 6144 at N = 4096: 64 vs 82 us).
-// One CTA per SM (d_in = 4096 at K*r = 64) leaves too few clusters resident, and small batches
-// pay for the extra adapters: the grouped path won all of those points.
+// Where the dense path beat the scalar and grouped ones on GB300 (top-2, r = 16, warm and L2
+// flushed alike): with a plan of two CTAs per SM (one or two gather rounds) from 512 tokens --
+// 4096 -> 4096 at K = 4: 18.6 vs 19.4 us at 512 and 23.8 vs 32.9 us at 2048 tokens; 2048 -> 6144
+// at K = 4: 18.2 vs 21.3 us at 512 and 49 vs 71 us at 4096.  A one-CTA-per-SM plan (K*r = 128
+// at d_in = 4096) leaves too few clusters resident, and small batches pay for the extra
+// adapters: the scalar or grouped path won all of those points.
 bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
-  if (dtype != MOLORA_BF16 || N < 2048 || !(r == 16 || r == 32 || r == 64) || (K * r != 64 && K * r != 128))
+  if (dtype != MOLORA_BF16 || N < 512 || !(r == 16 || r == 32 || r == 64) || (K * r != 64 && K * r != 128))
     return false;
   DensePlan s;
   for (int C : {8, 4, 2, 1})
-    if (dense_plan(d_in, d_out, K, r, C, 1, kTwoPerSm, false, &s)) return dense_encoder() != nullptr;
+    for (int rounds : {1, 2})
+      if (dense_plan(d_in, d_out, K, r, C, rounds, kTwoPerSm, false, &s)) return dense_encoder() != nullptr;
   return false;
 }
 
