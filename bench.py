@@ -846,9 +846,12 @@ def run_mode(args):
                 m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm)
             ms = _replay_ms(_graph(fn, stream), stream, args.replays)
             p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
+            r_ms = _replay_ms(_graph(lambda: m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False),
+                                     stream), stream, min(args.replays, 200))
             emit({"mode": "topk", "workload": "N=8192, d=4096, K=8, r=64, router d->64->K", "k": k,
                   "replays": args.replays, "p50_ms": round(p50, 5), "p99_ms": round(p99, 5),
-                  "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1), "l2": "not flushed (back-to-back replays)"})
+                  "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1), "router_alone_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
+                  "l2": "not flushed (back-to-back replays)"})
     elif args.mode == "router":
         wl = workloads.make("topk_mlp")
         x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),
