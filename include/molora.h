@@ -68,7 +68,7 @@ typedef enum {
   MOLORA_PATH_SCALAR = 1,  /* CUDA-core, token-major, one CTA per token (the memory-bound regime) */
   MOLORA_PATH_GROUPED = 2, /* grouped tcgen05 shrink + expand over the dispatch permutation */
   MOLORA_PATH_DENSE = 3    /* tcgen05 over all K adapters per token, weight 0 for the unselected
-                              (K*r <= 128, bf16); needs no dispatch; one y update per token */
+                              (K*r = 64 or 128, bf16); needs no dispatch; one y update per token */
 } molora_path;
 
 /* Device-side error bits OR-ed into *err_word. */
@@ -258,9 +258,10 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
 /*
  * molora_router_lora_apply -- the learned router and the top-k apply in one pass over x
  * (Table 1: routing cost O(64d + 64K) on top of the apply; Figure 2: top-k adapters combined
- * by a weighted sum).  It computes exactly what molora_router_topk followed by
- * molora_lora_apply computes, in one kernel that reads each x row once for both: the router's
- * x W1 is 64 more columns of the apply's shrink x [A_0 | ... | A_{K-1}].
+ * by a weighted sum).  Its results equal, bit for bit, those of molora_router_topk followed
+ * by molora_lora_apply on the dense path (MOLORA_PATH_DENSE), computed in one kernel that
+ * reads each x row once for both: the router's x W1 is 64 more columns of the apply's shrink
+ * x [A_0 | ... | A_{K-1}].
  *
  *   logits, ids, w   as molora_router_topk (same hidden width 64, same top-k and softmax rule)
  *   y[t,:] += scale * sum_j w[t,j] * (x[t,:] A_{ids[t,j]}) B_{ids[t,j]}
@@ -270,8 +271,8 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
  * logits fp32 [N x K] output or NULL;  ids int32 [N x k] and w fp32 [N x k] outputs;
  * y fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1) [N x d_out], updated in place.
  * Every y element receives one addition, so results are reproducible for any k.
- * Supported: dtype MOLORA_BF16, r in {16, 32, 64}, K*r <= 128 (the stacked ranks of the
- * hot set), d_in and d_out multiples of 64 that split evenly over the kernel's cluster;
+ * Supported: dtype MOLORA_BF16, r in {16, 32, 64}, K*r = 64 or 128 (the stacked ranks of
+ * the hot set), d_in and d_out multiples of 64 that split evenly over the kernel's cluster;
  * other shapes return MOLORA_ERR_UNSUPPORTED (use the two calls).  x, W1, A, B and y must be
  * 16-byte aligned.
  */

@@ -34,7 +34,7 @@ cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int
                                const float* w, int32_t k, float scale, void* y, bool y_bf16, int32_t mask_adapter,
                                int32_t* err_word, cudaStream_t stream, const AdapterTable* table = nullptr);
 
-// Token-major tcgen05 apply over all K adapters (K*r <= 128; weight 0 for the unselected).
+// Token-major tcgen05 apply over all K adapters (K*r = 64 or 128; weight 0 for the unselected).
 bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r);
 // True where AUTO takes the dense path (measured faster than the grouped one).
 bool dense_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r);
