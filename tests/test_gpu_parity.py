@@ -544,7 +544,7 @@ def test_apply_indirect_topk_and_bf16y(m, path):
     assert_bf16y_close(yb, y0b, yb_ref, 1 if path == "scalar" else 1 + k, parts)
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS + ["dense"])
 def test_apply_degenerate_cases(m, path):
     wl = workloads.make("modality4", N=300, d_in=512, d_out=512)
     g = torch.Generator().manual_seed(5)
@@ -568,6 +568,22 @@ def test_apply_degenerate_cases(m, path):
     m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(idsK), y, wl.scale, w=dev(wK), counts=cK, offsets=oK,
                         perm=pK, path=path)
     y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, idsK, wl.y0, wl.scale, wK)
+    assert_apply_close(y, y_ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_apply_single_adapter_is_plain_lora(m, path):
+    # K = 1, k = 1: every token takes the one adapter, y = y0 + scale * (x A) B, a ragged N
+    wl = workloads.make("modality4", N=777, d_in=1024, d_out=1536, K=1)
+    ids = torch.zeros(wl.N, dtype=torch.int32)
+    e = err_word()
+    counts, offsets, perm = m.molora_dispatch(dev(ids), 1, err_word=e)
+    y = dev(wl.y0).clone()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), dev(ids), y, wl.scale, counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path=path)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, wl.y0, wl.scale)
     assert_apply_close(y, y_ref)
 
 
