@@ -68,3 +68,17 @@ def test_reference_arm_other_ranks_print_nothing(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_algorithmic_bytes_of_the_benchmark_apply():
+    # x read once (2048 x 4096 bf16), y read and written once (fp32), the four adapters'
+    # A and B read once, the ids and the permutation read once, the K+1 offsets
+    import workloads
+    wl = workloads.make("modality4")
+    x = 2048 * 4096 * 2
+    y = 2 * 2048 * 4096 * 4
+    ab = 4 * (4096 * 16 + 16 * 4096) * 2
+    idx = 2 * 2048 * 4 + 5 * 4
+    assert bench.algorithmic_bytes(wl, 4) == x + y + ab + idx == 84_951_060
+    # an adapter the batch does not touch costs nothing
+    assert bench.algorithmic_bytes(wl, 3) == x + y + 3 * (4096 * 16 + 16 * 4096) * 2 + idx
