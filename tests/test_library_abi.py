@@ -149,3 +149,31 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert step(starts=None) == INVALID and step(counts=None) == INVALID and step(perm=None) == INVALID
     assert step(K=0) == INVALID and step(K=65) == INVALID and step(y=odd) == INVALID
     assert lib.molora_status_string(1) == b"invalid argument"
+
+
+def test_binding_has_no_cpu_fallback():
+    import torch
+    # every entry point refuses host tensors outright: the product path is the CUDA library
+    import token_adapter_routing_gb300 as m
+    x = torch.zeros(8, 64, dtype=torch.bfloat16)
+    A = torch.zeros(4, 64, 16, dtype=torch.bfloat16)
+    B = torch.zeros(4, 16, 64, dtype=torch.bfloat16)
+    W1 = torch.zeros(64, 64, dtype=torch.bfloat16)
+    W2 = torch.zeros(64, 4, dtype=torch.bfloat16)
+    ids = torch.zeros(8, 1, dtype=torch.int32)
+    tok = torch.zeros(8, dtype=torch.int32)
+    starts = torch.tensor([0, 10, 20, 30, 40], dtype=torch.int32)
+    y = torch.zeros(8, 64)
+    calls = [
+        lambda: m.molora_route_vocab(tok, starts),
+        lambda: m.molora_router_topk(x, W1, W2, 2),
+        lambda: m.molora_dispatch(ids, 4),
+        lambda: m.molora_route_vocab_dispatch(tok, starts),
+        lambda: m.molora_lora_apply(x, A, B, ids, y, 2.0),
+        lambda: m.molora_route_vocab_lora_apply(tok, starts, x, A, B, y, 2.0),
+        lambda: m.molora_router_lora_apply(x, W1, W2, A, B, 2, y, 2.0),
+        lambda: m.molora_lora_apply_masked_pass(x, A, B, tok, 0, y, 2.0),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
