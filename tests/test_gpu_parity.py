@@ -928,3 +928,30 @@ def test_bounded_wait_reports_timeout_and_context_survives(m):
     assert err == 0
     y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
     assert_apply_close(y, y_ref)
+
+
+# ------------------------------------------------------------------------- clusters of 4
+
+@pytest.mark.parametrize("path", ["grouped", "dense", "fused"])
+def test_four_cta_clusters(m, path):
+    # d_in = 768 and d_out = 1280 do not split over 8 CTAs of 64-column blocks: the plans
+    # fall back to clusters of 4 (16 rows per owner CTA in the dense kernel)
+    if path == "grouped":
+        wl = workloads.make("modality4", N=421, d_in=768, d_out=1280)
+        adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, path)
+        assert e == 0
+        y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
+        assert_apply_close(y, y_ref)
+        return
+    wl = workloads.make("topk_mlp", N=421, d_in=768, d_out=1280, k=2)
+    x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
+    y = dev(wl.y0).clone()
+    e = err_word()
+    if path == "dense":
+        logits, ids, w = m.molora_router_topk(x, W1, W2, 2)
+        m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, err_word=e, path="dense")
+    else:
+        logits, ids, w = m.molora_router_lora_apply(x, W1, W2, A, B, 2, y, wl.scale, err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    check_learned_apply(wl, 2, logits, ids, w, y)
