@@ -930,20 +930,22 @@ def test_bounded_wait_reports_timeout_and_context_survives(m):
     assert_apply_close(y, y_ref)
 
 
-# ------------------------------------------------------------------------- clusters of 4
+# ------------------------------------------------------------------------- clusters of 4, 2 and 1
 
 @pytest.mark.parametrize("path", ["grouped", "dense", "fused"])
-def test_four_cta_clusters(m, path):
-    # d_in = 768 and d_out = 1280 do not split over 8 CTAs of 64-column blocks: the plans
-    # fall back to clusters of 4 (16 rows per owner CTA in the dense kernel)
+@pytest.mark.parametrize("d_in,d_out", [(768, 1280), (384, 384), (192, 320)])
+def test_smaller_clusters(m, path, d_in, d_out):
+    # shapes that do not split over 8 CTAs of 64-column blocks: the plans fall back to
+    # clusters of 4 (768 -> 1280), 2 (384 -> 384) and 1 (192 -> 320); in the dense kernel an
+    # owner CTA then holds 16, 32 or all 64 rows of its tile
     if path == "grouped":
-        wl = workloads.make("modality4", N=421, d_in=768, d_out=1280)
+        wl = workloads.make("modality4", N=421, d_in=d_in, d_out=d_out)
         adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, path)
         assert e == 0
         y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
         assert_apply_close(y, y_ref)
         return
-    wl = workloads.make("topk_mlp", N=421, d_in=768, d_out=1280, k=2)
+    wl = workloads.make("topk_mlp", N=421, d_in=d_in, d_out=d_out, k=2)
     x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
     y = dev(wl.y0).clone()
     e = err_word()
