@@ -5,7 +5,7 @@
 //   y[t,:] += scale * sum_a c[t,a] (x[t,:] A_a) B_a,   c[t,a] = sum_j [ids[t,j] == a] w[t,j]
 //
 // which is the pages' sum written over all K adapters, with weight zero for the ones a
-// token did not select.  When K*r is small (the hot set's ranks stacked: at most 128
+// token did not select.  When K*r is small (the hot set's ranks stacked: 64 or 128
 // columns) this evaluates every adapter for every token on the tensor cores instead of
 // grouping slots by adapter, and in exchange reads each token's x row once and adds into
 // each y row once, whatever k is -- the grouped path reads x and reduces into y once per
@@ -17,7 +17,9 @@
 //      operand [A_0 | ... | A_{K-1}] (K*r = 64 or 128 columns), and accumulates
 //      H = x [A_0 | ... | A_{K-1}] (fp32) in TMEM with one tcgen05.mma per 16-element K step
 //      (M = 128: rows past 64 are unused; N = K*r, so x is read from shared memory once per
-//      step rather than once per adapter);
+//      step rather than once per adapter).  The K-slice comes in one round, or in two through
+//      one buffer where one round would not fit two CTAs per SM; the tile's coefficients
+//      c[t,a] are read while the gather is in flight;
 //   2. the C partial H are summed through distributed shared memory in rank order
 //      (deterministic), each adapter's r columns are scaled by scale * c[t,a], and the
 //      result G is split into bf16 hi + lo and sent to every CTA of the cluster;
@@ -27,6 +29,10 @@
 //   4. epilogue: D goes TMEM -> registers -> shared memory -> one bulk fp32 (or bf16) add
 //      per row segment into y, performed by the TMA unit in L2.  Every y element receives
 //      one addition, so results are reproducible for any k.
+// The router variant (kRouter) adds the learned router's W1 as one more 64-column block of
+// the stacked shrink operand, so one pass over x feeds both; the owner CTA of each row runs
+// the router's second stage (ReLU, logits, top k, softmax) on the reduced hidden partials and
+// uses the resulting weights as c[t,a].
 #include <cudaTypedefs.h>
 
 #include <cstring>
