@@ -838,6 +838,7 @@ def run_mode(args):
                     row["faster"] = "grouped" if row["grouped_us_warm"] < row["scalar_us_warm"] else "scalar"
                     emit(row)
     elif args.mode == "topk":
+        peak = measured_peaks()[0].get("hbm_gbs")
         for k in (1, 2, 3, 4):
             wl = workloads.make("topk_scaling", k=k)
             x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),
@@ -847,19 +848,33 @@ def run_mode(args):
             counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
             offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
             perm = torch.empty(wl.N * k, dtype=torch.int32, device=dev)
+            need = m.molora_workspace_bytes(wl.N, wl.d_in, wl.d_out, wl.K, wl.r, k, router=True)
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
-            def fn():
+            def fused():  # router + stacked apply: x read once, one y update per token
+                m.molora_router_lora_apply(x, W1, W2, A, B, k, y, wl.scale, ids=ids, w=w, want_logits=False, ws=ws)
+
+            def grouped():  # router -> dispatch -> grouped apply (k gathers and k reductions per token)
                 m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False)
                 m.molora_dispatch(ids, wl.K, counts=counts, offsets=offsets, perm=perm)
-                m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm)
-            ms = _replay_ms(_graph(fn, stream), stream, args.replays)
-            p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
+                m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, counts=counts, offsets=offsets, perm=perm,
+                                    path="grouped")
+            # algorithmic bytes: x once, y read + written, every adapter's A and B, W1, ids and w
+            nbytes = (wl.N * wl.d_in * 2 + 2 * wl.N * wl.d_out * 4 + wl.K * (wl.d_in * wl.r + wl.r * wl.d_out) * 2
+                      + wl.d_in * 64 * 2 + wl.N * 2 * k * 4)
+            res = {}
+            for name, fn, reps in (("fused_stacked", fused, args.replays), ("grouped", grouped, min(args.replays, 200))):
+                ms = _replay_ms(_graph(fn, stream), stream, reps)
+                p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
+                res[name] = {"p50_ms": round(p50, 5), "p99_ms": round(p99, 5), "replays": reps,
+                             "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1),
+                             "GBps_p50": round(nbytes / (p50 * 1e-3) / 1e9, 1),
+                             "frac_of_measured_hbm": round(nbytes / (p50 * 1e-3) / 1e9 / peak, 3) if peak else None}
             r_ms = _replay_ms(_graph(lambda: m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False),
                                      stream), stream, min(args.replays, 200))
             emit({"mode": "topk", "workload": "N=8192, d=4096, K=8, r=64, router d->64->K", "k": k,
-                  "replays": args.replays, "p50_ms": round(p50, 5), "p99_ms": round(p99, 5),
-                  "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1), "router_alone_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
-                  "l2": "not flushed (back-to-back replays)"})
+                  "algorithmic_bytes": nbytes, **res, "router_alone_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
+                  "l2": "not flushed (back-to-back replays; 344 MB of inputs and outputs exceed the L2)"})
     elif args.mode == "router":
         wl = workloads.make("topk_mlp")
         x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),

@@ -14,6 +14,16 @@
  *   - Tables 3 and 7: the per-sequence alternative runs K masked passes (K*N token-work
  *     against N for per-token routing).
  *
+ * Workspace (ws, ws_bytes), for the calls that take it (Table 1's shared dispatch
+ * infrastructure needs none; only MOLORA_PATH_STACKED does):
+ *   - ws_bytes == NULL: no workspace.  AUTO chooses among the paths that need none, and an
+ *     explicit MOLORA_PATH_STACKED returns MOLORA_ERR_INVALID_ARG.
+ *   - ws == NULL, ws_bytes != NULL: a query.  *ws_bytes is set to the bytes the call would
+ *     need (0 if its path needs none); nothing is launched.
+ *   - ws != NULL: a caller-owned device buffer of *ws_bytes bytes, 256-byte aligned, at least
+ *     the queried size (else MOLORA_ERR_INVALID_ARG).  The call overwrites it; it must not be
+ *     shared with work that may run concurrently.  Its contents after the call are unspecified.
+ *
  * Conventions for every call:
  *   - All array pointers are DEVICE pointers owned by the caller (for example torch tensors).
  *     The library never allocates, frees or synchronises inside a call: each call only
@@ -67,8 +77,12 @@ typedef enum {
   MOLORA_PATH_AUTO = 0,
   MOLORA_PATH_SCALAR = 1,  /* CUDA-core, token-major, one CTA per token (the memory-bound regime) */
   MOLORA_PATH_GROUPED = 2, /* grouped tcgen05 shrink + expand over the dispatch permutation */
-  MOLORA_PATH_DENSE = 3    /* tcgen05 over all K adapters per token, weight 0 for the unselected
+  MOLORA_PATH_DENSE = 3,   /* tcgen05 over all K adapters per token, weight 0 for the unselected
                               (K*r = 64 or 128, bf16); needs no dispatch; one y update per token */
+  MOLORA_PATH_STACKED = 4  /* the same sum as DENSE for a stacked rank K*r up to 1024 (bf16, fp32 y,
+                              d_in a multiple of 64): a shrink kernel writes scale * c[t,a] (x A_a) for
+                              every adapter to a caller workspace, then a persistent tcgen05 GEMM adds
+                              it times [B_0; ...; B_{K-1}] into y; no dispatch; one y update per token */
 } molora_path;
 
 /* Device-side error bits OR-ed into *err_word. */
@@ -194,28 +208,32 @@ MOLORA_API molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64
  *                         path; the scalar path reads ids directly and ignores them)
  * y       fp32 [N x d_out], updated in place (read-modify-write)
  *
+ * ws, ws_bytes  workspace (see the convention above); the stacked path needs
+ *               2 * roundup256(N * K * r * 2) bytes, every other path none
+ *
  * Accumulation is fp32 (tensor cores or FMA); x, A, B are read as given.  The grouped path
  * needs bf16 and r >= 16; anything else runs on the scalar path.  With k > 1 the grouped
  * path adds each slot's contribution to y with an fp32 reduction in L2, so the order of the
- * k additions (and therefore the last bits of y) may vary from run to run; with k = 1 and
- * on the scalar path every element of y is written exactly once and results are
- * reproducible bit for bit.
+ * k additions (and therefore the last bits of y) may vary from run to run; with k = 1, and
+ * on the scalar, dense and stacked paths for any k, every element of y receives one
+ * addition and results are reproducible bit for bit.
  */
 MOLORA_API molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
                                 int32_t d_out, const void* A, const void* B, int32_t K, int32_t r,
                                 const int32_t* ids, const float* w, int32_t k,
                                 const int32_t* counts, const int32_t* offsets,
-                                const int32_t* perm, float scale, float* y, int32_t* err_word,
-                                cudaStream_t stream);
+                                const int32_t* perm, float scale, float* y, void* ws,
+                                size_t* ws_bytes, int32_t* err_word, cudaStream_t stream);
 
 /* molora_lora_apply with an explicit kernel family (used to measure the crossover).
- * MOLORA_PATH_GROUPED on an unsupported shape returns MOLORA_ERR_UNSUPPORTED. */
+ * A path that does not support the shape returns MOLORA_ERR_UNSUPPORTED. */
 MOLORA_API molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
                                    int32_t d_out, const void* A, const void* B, int32_t K,
                                    int32_t r, const int32_t* ids, const float* w, int32_t k,
                                    const int32_t* counts, const int32_t* offsets,
-                                   const int32_t* perm, float scale, float* y, int32_t* err_word,
-                                   molora_path path, cudaStream_t stream);
+                                   const int32_t* perm, float scale, float* y, void* ws,
+                                   size_t* ws_bytes, int32_t* err_word, molora_path path,
+                                   cudaStream_t stream);
 
 /*
  * molora_lora_apply_bf16y -- molora_lora_apply_ex with y held in bf16 (the output dtype a
@@ -270,17 +288,27 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
  * b2 fp32 [K] or NULL;  A [K x d_in x r] and B [K x r x d_out] bf16 slabs;  1 <= k <= K;
  * logits fp32 [N x K] output or NULL;  ids int32 [N x k] and w fp32 [N x k] outputs;
  * y fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1) [N x d_out], updated in place.
+ * ws, ws_bytes: workspace (see the convention above).
  * Every y element receives one addition, so results are reproducible for any k.
- * Supported: dtype MOLORA_BF16, r in {16, 32, 64}, K*r = 64 or 128 (the stacked ranks of
- * the hot set), d_in and d_out multiples of 64 that split evenly over the kernel's cluster;
- * other shapes return MOLORA_ERR_UNSUPPORTED (use the two calls).  x, W1, A, B and y must be
- * 16-byte aligned.
+ * Two kernel families:
+ *   - one kernel, K*r = 64 or 128, y fp32 or bf16, d_in and d_out multiples of 64 that split
+ *     evenly over its cluster; logits, ids, w and y equal molora_router_topk followed by the
+ *     dense molora_lora_apply bit for bit.  Used without a workspace (ws_bytes == NULL);
+ *   - the stacked pair (the shrink with the router, then the expand GEMM), K*r up to 1024,
+ *     fp32 y, d_in a multiple of 64.  Its router sums the 64 hidden units in order for each
+ *     logit, so its logits may differ from molora_router_topk's in the last bits.  Used
+ *     whenever a buffer is passed (ws != NULL) and it applies.
+ * A query (ws == NULL, ws_bytes != NULL) returns the stacked pair's size where it applies and
+ * the one kernel does not or is measured slower, else 0.
+ * Other shapes return MOLORA_ERR_UNSUPPORTED (use the separate calls).  dtype must be
+ * MOLORA_BF16; x, W1, A, B and y must be 16-byte aligned.
  */
 MOLORA_API molora_status molora_router_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
                                        int32_t d_out, const void* W1, const float* b1, const void* W2,
                                        const float* b2, const void* A, const void* B, int32_t K, int32_t r,
                                        int32_t k, float scale, float* logits, int32_t* ids, float* w,
-                                       void* y, int32_t y_bf16, int32_t* err_word, cudaStream_t stream);
+                                       void* y, int32_t y_bf16, void* ws, size_t* ws_bytes,
+                                       int32_t* err_word, cudaStream_t stream);
 
 /*
  * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:
@@ -299,7 +327,8 @@ MOLORA_API molora_status molora_lora_apply_masked_pass(const void* x, molora_dty
                                             float* y, int32_t* err_word, molora_path path,
                                             cudaStream_t stream);
 
-/* The kernel family molora_lora_apply would choose for this shape (never AUTO). */
+/* The kernel family molora_lora_apply would choose for this shape when given a workspace
+ * (never AUTO; without one, a STACKED choice becomes the best path that needs none). */
 MOLORA_API molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                int32_t K, int32_t r, int32_t k);
 

@@ -56,7 +56,8 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     P, I64, I32, F, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_int
     lib.molora_route_vocab.argtypes = [P, I64, P, I32, P, P, P]
     lib.molora_dispatch.argtypes = [P, I64, I32, I32, P, P, P, P, P]
-    lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, S, P]
+    lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P, P, S,
+                                         P]
     lib.molora_router_topk.argtypes = [P, S, I64, I32, P, P, P, P, I32, I32, P, P, P, P]
     lib.molora_status_string.restype = ctypes.c_char_p
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
@@ -81,9 +82,10 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_route_vocab_dispatch(fake, 8, fake, 4, fake, fake, None, fake, None, None) == INVALID
     assert lib.molora_route_vocab_dispatch(fake, -1, fake, 4, fake, fake, fake, fake, None, None) == INVALID
 
-    def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0):
+    def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0,
+              ws=None, ws_bytes=None):
         return lib.molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, None, k, fake, fake, fake,
-                                        2.0, y, None, path, None)
+                                        2.0, y, ws, ws_bytes, None, path, None)
 
     assert apply(r=12) == INVALID
     assert apply(K=0) == INVALID and apply(K=65) == INVALID
@@ -92,7 +94,16 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert apply(x=None) == INVALID and apply(y=None) == INVALID and apply(ids=None) == INVALID
     assert apply(x=odd) == INVALID and apply(A=odd) == INVALID and apply(B=odd) == INVALID and apply(y=odd) == INVALID
     assert apply(N=-1) == INVALID and apply(d_in=0) == INVALID
-    assert apply(path=9) == INVALID
+    assert apply(path=9) == INVALID and apply(path=-1) == INVALID
+    # the stacked path needs a workspace: without ws_bytes it is an invalid request, and an
+    # empty batch is a no-op on every path
+    assert apply(path=4) == INVALID
+    assert apply(N=0, path=4) == 0
+    # a query looks at sizes only: bad sizes are still rejected, null pointers are not
+    size = ctypes.c_size_t(12345)
+    assert apply(x=None, A=None, B=None, ids=None, y=None, ws_bytes=ctypes.byref(size)) == 0
+    assert size.value == 0  # no workspace path without the driver's tensor-map encoder
+    assert apply(K=0, ws_bytes=ctypes.byref(size)) == INVALID and apply(r=12, ws_bytes=ctypes.byref(size)) == INVALID
     # the grouped tensor-core path needs bf16 and r >= 16
     assert apply(dtype=0, path=2) == UNSUPPORTED
     assert apply(r=8, path=2) == UNSUPPORTED
@@ -127,17 +138,17 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_router_topk(fake, 1, 8, 64, fake, None, fake, None, 4, 1, None, None, fake, None) == INVALID
     # router + apply in one kernel: bad k, null or unaligned W1, null w; fp32 and K*r > 128 unsupported
     lib.molora_router_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, P, P, P, P, I32, I32, I32, F, P, P, P, P,
-                                             I32, P, P]
+                                             I32, P, P, P, P]
 
     def fused(dtype=1, K=4, r=16, k=2, W1=fake, w=fake, y=fake):
         return lib.molora_router_lora_apply(fake, dtype, 64, 512, 512, W1, None, fake, None, fake, fake, K, r, k,
-                                            2.0, None, fake, w, y, 0, None, None)
+                                            2.0, None, fake, w, y, 0, None, None, None, None)
 
     assert fused(k=5) == INVALID and fused(k=0) == INVALID and fused(W1=None) == INVALID
     assert fused(W1=odd) == INVALID and fused(w=None) == INVALID and fused(y=odd) == INVALID
     assert fused(dtype=0) == UNSUPPORTED and fused(K=16, r=16) == UNSUPPORTED and fused(r=8) == UNSUPPORTED
     assert lib.molora_router_lora_apply(None, 1, 0, 512, 512, None, None, None, None, None, None, 4, 16, 2, 2.0,
-                                        None, None, None, None, 0, None, None) == 0
+                                        None, None, None, None, 0, None, None, None, None) == 0
     # the whole vocabulary-routed step: null outputs, bad K, odd y
     lib.molora_route_vocab_lora_apply.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P, P,
                                                   P, P]
@@ -177,3 +188,68 @@ def test_binding_has_no_cpu_fallback():
     for call in calls:
         with pytest.raises(ValueError, match="CUDA tensor"):
             call()
+
+
+def test_binding_rejects_mis_sized_tensors_before_any_launch():
+    """The Python binding checks every tensor's size against N, d_out, K and k before it looks
+    at devices (so these CPU tensors fail on their sizes, with the argument named), and a
+    correctly sized CPU tensor fails only for not being on a GPU: nothing reaches the library."""
+    import torch
+    import token_adapter_routing_gb300 as m
+    N, d_in, d_out, K, r, k = 8, 64, 32, 4, 16, 2
+    x = torch.zeros(N, d_in, dtype=torch.bfloat16)
+    A = torch.zeros(K, d_in, r, dtype=torch.bfloat16)
+    B = torch.zeros(K, r, d_out, dtype=torch.bfloat16)
+    ids = torch.zeros(N, k, dtype=torch.int32)
+    w = torch.zeros(N, k)
+    y = torch.zeros(N, d_out)
+    counts = torch.zeros(K, dtype=torch.int32)
+    offsets = torch.zeros(K + 1, dtype=torch.int32)
+    perm = torch.zeros(N * k, dtype=torch.int32)
+    ok = dict(w=w, counts=counts, offsets=offsets, perm=perm)
+
+    def apply(**kw):
+        args = dict(ok)
+        args.update(kw)
+        yy = args.pop("y", y)
+        ii = args.pop("ids", ids)
+        return m.molora_lora_apply(x, A, B, ii, yy, 2.0, **args)
+
+    with pytest.raises(ValueError, match="y must be"):
+        apply(y=torch.zeros(N, d_out + 1))
+    with pytest.raises(ValueError, match="y must be"):
+        apply(y=torch.zeros(N + 1, d_out))
+    with pytest.raises(ValueError, match="ids must be"):
+        apply(ids=torch.zeros(N + 1, k, dtype=torch.int32))
+    with pytest.raises(ValueError, match="w must"):
+        apply(w=torch.zeros(N, k + 1))
+    with pytest.raises(ValueError, match="counts must"):
+        apply(counts=torch.zeros(K + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="offsets must"):
+        apply(offsets=torch.zeros(K, dtype=torch.int32))
+    with pytest.raises(ValueError, match="perm must"):
+        apply(perm=torch.zeros(N, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        apply()
+    with pytest.raises(ValueError, match="perm must"):
+        m.molora_dispatch(ids, K, perm=torch.zeros(N * k - 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="offsets must"):
+        m.molora_dispatch(ids, K, offsets=torch.zeros(K + 2, dtype=torch.int32))
+    W1 = torch.zeros(d_in, 64, dtype=torch.bfloat16)
+    W2 = torch.zeros(64, K, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="logits must"):
+        m.molora_router_topk(x, W1, W2, k, logits=torch.zeros(N, K + 1))
+    with pytest.raises(ValueError, match="ids must"):
+        m.molora_router_topk(x, W1, W2, k, ids=torch.zeros(N, k + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="y must be"):
+        m.molora_router_lora_apply(x, W1, W2, A, B, k, torch.zeros(N, d_out - 1), 2.0)
+    with pytest.raises(ValueError, match="w must"):
+        m.molora_router_lora_apply(x, W1, W2, A, B, k, y, 2.0, w=torch.zeros(N, k + 1))
+    tok = torch.zeros(N, dtype=torch.int32)
+    starts = torch.arange(K + 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="perm must"):
+        m.molora_route_vocab_dispatch(tok, starts, perm=torch.zeros(N + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="adapter must"):
+        m.molora_route_vocab(tok, starts, adapter=torch.zeros(N - 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="adapter_of must"):
+        m.molora_lora_apply_masked_pass(x, A, B, torch.zeros(N + 1, dtype=torch.int32), 0, y, 2.0)

@@ -37,16 +37,44 @@ static int64_t crossover_tokens(int32_t K) {
   return 4096;
 }
 
-static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
-                                      const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
-                                      int32_t k, const void* y) {
+static molora_status check_apply_sizes(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
+                                       int32_t r, int32_t k) {
   if (!valid_dtype(dtype) || N < 0 || d_in < 1 || d_out < 1 || K < 1 || K > kMaxAdapters || k < 1 || k > K)
     return MOLORA_ERR_INVALID_ARG;
   if (!(r == 8 || r == 16 || r == 32 || r == 64)) return MOLORA_ERR_INVALID_ARG;
   if (N > INT32_MAX || N * (int64_t)k > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
-  if (N == 0) return MOLORA_OK;
+  return MOLORA_OK;
+}
+
+static molora_status check_apply_args(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                      const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                                      int32_t k, const void* y) {
+  const molora_status st = check_apply_sizes(dtype, N, d_in, d_out, K, r, k);
+  if (st != MOLORA_OK || N == 0) return st;
   if (!x || !A || !B || !ids || !y) return MOLORA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(y)) return MOLORA_ERR_INVALID_ARG;
+  return MOLORA_OK;
+}
+
+// The best path that needs no workspace (AUTO without one, or with the adapter table of the
+// indirect layout, which only the scalar and grouped kernels read).
+static molora_path select_without_ws(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K,
+                                     int32_t r, int32_t k, bool table) {
+  if (!table && k >= 2 && dense_preferred(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
+  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
+  return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
+}
+
+// Workspace convention (include/molora.h): ws_bytes == NULL -> none; ws == NULL -> query;
+// else a buffer of *ws_bytes bytes.  `need` is what the chosen path needs.
+static molora_status check_ws(void* ws, size_t* ws_bytes, size_t need, bool* query) {
+  *query = ws_bytes != nullptr && ws == nullptr;
+  if (*query) {
+    *ws_bytes = need;
+    return MOLORA_OK;
+  }
+  if (need == 0) return MOLORA_OK;
+  if (!ws || !ws_bytes || *ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOLORA_ERR_INVALID_ARG;
   return MOLORA_OK;
 }
 
@@ -54,13 +82,35 @@ static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, in
                                 const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
                                 float scale, void* y, bool y_bf16, int32_t* err_word, molora_path path,
-                                cudaStream_t stream, const AdapterTable* table = nullptr) {
-  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
-  if (st != MOLORA_OK || N == 0) return st;
+                                cudaStream_t stream, const AdapterTable* table = nullptr, void* ws = nullptr,
+                                size_t* ws_bytes = nullptr) {
+  const bool have_ws = ws_bytes != nullptr;
+  const bool query = have_ws && ws == nullptr;  // sizes only: no pointer is looked at
+  const molora_status st = query ? check_apply_sizes(dtype, N, d_in, d_out, K, r, k)
+                                 : check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+  if (st != MOLORA_OK) return st;
   if (path == MOLORA_PATH_AUTO) {
     path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+    if (path == MOLORA_PATH_STACKED && (!have_ws || table || y_bf16 || !stacked_supported(dtype, N, d_in, d_out, K, r, false)))
+      path = select_without_ws(dtype, N, d_in, d_out, K, r, k, table != nullptr);
     if (path == MOLORA_PATH_DENSE && table) path = MOLORA_PATH_GROUPED;  // the dense path reads the slabs
   }
+  if (path == MOLORA_PATH_STACKED) {
+    if (!have_ws) return N == 0 ? MOLORA_OK : MOLORA_ERR_INVALID_ARG;
+    if (table || y_bf16 || !stacked_supported(dtype, N, d_in, d_out, K, r, false)) return MOLORA_ERR_UNSUPPORTED;
+    bool is_query = false;
+    const molora_status ws_st = check_ws(ws, ws_bytes, stacked_workspace_bytes(N, K, r), &is_query);
+    if (ws_st != MOLORA_OK || is_query || N == 0) return ws_st;
+    return launched(launch_lora_stacked(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, static_cast<float*>(y), ws,
+                                        err_word, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                        stream));
+  }
+  if (path < MOLORA_PATH_AUTO || path > MOLORA_PATH_STACKED) return MOLORA_ERR_INVALID_ARG;
+  if (query) {  // the other paths need no workspace
+    *ws_bytes = 0;
+    return MOLORA_OK;
+  }
+  if (N == 0) return MOLORA_OK;
   if (path == MOLORA_PATH_SCALAR)
     return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, y_bf16, -1,
                                        err_word, stream, table));
@@ -130,7 +180,7 @@ molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64_t N, const
   if (!starts || !counts || !offsets || (N > 0 && (!adapter || !perm))) return MOLORA_ERR_INVALID_ARG;
   if (N == 0)  // the empty histogram, as molora_route_vocab_dispatch writes it
     return launched(launch_route_vocab_dispatch(tok, 0, starts, K, adapter, counts, offsets, perm, err_word, stream));
-  const molora_path path = molora_select_path(dtype, N, d_in, d_out, K, r, 1);
+  const molora_path path = select_without_ws(dtype, N, d_in, d_out, K, r, 1, false);
   if (launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, stream) != cudaSuccess)
     return MOLORA_ERR_CUDA;
   return apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, adapter, nullptr, 1, counts, offsets, perm, scale, y,
@@ -139,18 +189,17 @@ molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64_t N, const
 
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
                                int32_t k) {
-  if (k >= 2 && dense_preferred(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
-  if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
-  return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
+  if (stacked_preferred(dtype, N, d_in, d_out, K, r, k, false)) return MOLORA_PATH_STACKED;
+  return select_without_ws(dtype, N, d_in, d_out, K, r, k, false);
 }
 
 molora_status molora_lora_apply_ex(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                    const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
                                    const float* w, int32_t k, const int32_t* counts, const int32_t* offsets,
-                                   const int32_t* perm, float scale, float* y, int32_t* err_word, molora_path path,
-                                   cudaStream_t stream) {
+                                   const int32_t* perm, float scale, float* y, void* ws, size_t* ws_bytes,
+                                   int32_t* err_word, molora_path path, cudaStream_t stream) {
   return molora::apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, false,
-                            err_word, path, stream);
+                            err_word, path, stream, nullptr, ws, ws_bytes);
 }
 
 molora_status molora_lora_apply_bf16y(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
@@ -182,14 +231,33 @@ molora_status molora_lora_apply_indirect(const void* x, molora_dtype dtype, int6
 molora_status molora_router_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                        const void* W1, const float* b1, const void* W2, const float* b2,
                                        const void* A, const void* B, int32_t K, int32_t r, int32_t k, float scale,
-                                       float* logits, int32_t* ids, float* w, void* y, int32_t y_bf16,
-                                       int32_t* err_word, cudaStream_t stream) {
-  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+                                       float* logits, int32_t* ids, float* w, void* y, int32_t y_bf16, void* ws,
+                                       size_t* ws_bytes, int32_t* err_word, cudaStream_t stream) {
+  const bool query = ws_bytes != nullptr && ws == nullptr;  // sizes only: no pointer is looked at
+  const molora_status st = query ? check_apply_sizes(dtype, N, d_in, d_out, K, r, k)
+                                 : check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
   if (st != MOLORA_OK) return st;
   if (N * (int64_t)K > INT32_MAX) return MOLORA_ERR_INVALID_ARG;
+  if (!query && N > 0 && (!W1 || !W2 || !w || !aligned16(W1))) return MOLORA_ERR_INVALID_ARG;
+  // A query sizes the preferred family: the stacked pair where it applies and either wins or is
+  // the only one.  A call given a buffer runs the stacked pair wherever it applies.
+  const bool one_kernel = router_dense_supported(dtype, N, d_in, d_out, K, r);
+  const bool stacked_ok = y_bf16 == 0 && stacked_supported(dtype, N, d_in, d_out, K, r, true);
+  const bool stacked = stacked_ok && ws_bytes != nullptr &&
+                       (query ? !one_kernel || stacked_preferred(dtype, N, d_in, d_out, K, r, k, true) : true);
+  if (stacked) {
+    bool is_query = false;
+    const molora_status ws_st = check_ws(ws, ws_bytes, stacked_workspace_bytes(N, K, r), &is_query);
+    if (ws_st != MOLORA_OK || is_query || N == 0) return ws_st;
+    return launched(launch_lora_stacked(x, N, d_in, d_out, A, B, K, r, nullptr, nullptr, k, scale,
+                                        static_cast<float*>(y), ws, err_word, W1, b1, W2, b2, logits, ids, w, stream));
+  }
+  if (query) {  // the one-kernel path needs no workspace
+    *ws_bytes = 0;
+    return one_kernel || N == 0 ? MOLORA_OK : MOLORA_ERR_UNSUPPORTED;
+  }
   if (N == 0) return MOLORA_OK;
-  if (!W1 || !W2 || !w || !aligned16(W1)) return MOLORA_ERR_INVALID_ARG;
-  if (!router_dense_supported(dtype, N, d_in, d_out, K, r)) return MOLORA_ERR_UNSUPPORTED;
+  if (!one_kernel) return MOLORA_ERR_UNSUPPORTED;
   return launched(launch_router_lora_dense(x, N, d_in, d_out, W1, b1, W2, b2, A, B, K, r, k, scale, logits, ids, w, y,
                                            y_bf16 != 0, err_word, stream));
 }
@@ -197,9 +265,10 @@ molora_status molora_router_lora_apply(const void* x, molora_dtype dtype, int64_
 molora_status molora_lora_apply(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
                                 const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                 int32_t k, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
-                                float scale, float* y, int32_t* err_word, cudaStream_t stream) {
-  return molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y,
-                              err_word, MOLORA_PATH_AUTO, stream);
+                                float scale, float* y, void* ws, size_t* ws_bytes, int32_t* err_word,
+                                cudaStream_t stream) {
+  return molora_lora_apply_ex(x, dtype, N, d_in, d_out, A, B, K, r, ids, w, k, counts, offsets, perm, scale, y, ws,
+                              ws_bytes, err_word, MOLORA_PATH_AUTO, stream);
 }
 
 molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,

@@ -75,6 +75,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// As mbar_wait, but also gives up as soon as *abort is set by another thread of the CTA, and
+// sets *abort itself when the time limit runs out, so that one failed wait ends every other
+// role's waits promptly instead of each running out its own limit.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ cp.async (16 B, L2 only)
 // src_bytes < 16 zero-fills the rest of the 16 destination bytes (0 = pure zero fill).
 __device__ __forceinline__ void cp_async_16(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
@@ -132,6 +149,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* ma
       "[%4];" ::"r"(sdst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
+}
+// smem box -> global through a tensor map, each element ADDED to the destination (the
+// element type of the map: fp32 add for a FLOAT32 map); rows and columns outside the tensor
+// are skipped.  Completes as a bulk group of the issuing thread.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t ssrc, int32_t c0, int32_t c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(ssrc)
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -48,6 +48,22 @@ cudaError_t launch_router_lora_dense(const void* x, int64_t N, int32_t d_in, int
                                      int32_t K, int32_t r, int32_t k, float scale, float* logits, int32_t* ids,
                                      float* w, void* y, bool y_bf16, int32_t* err_word, cudaStream_t stream);
 
+// Stacked two-kernel tcgen05 apply (K*r up to 1024): shrink (optionally with the learned
+// router) into a workspace of stacked_workspace_bytes, then a persistent expand GEMM into y.
+bool stacked_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
+                       bool router);
+// True where AUTO takes the stacked path (measured faster than the paths needing no workspace).
+bool stacked_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
+                       int32_t k, bool router);
+size_t stacked_workspace_bytes(int64_t N, int32_t K, int32_t r);
+// W1 == nullptr: ids and w are given.  Otherwise the router (W1, b1, W2, b2) runs in the shrink
+// kernel and writes logits (if non-null), ids_out and w_out.
+cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
+                                int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
+                                float* y, void* ws, int32_t* err_word, const void* W1, const float* b1,
+                                const void* W2, const float* b2, float* logits, int32_t* ids_out, float* w_out,
+                                cudaStream_t stream);
+
 // CUDA-core learned router (any dtype / shape).
 cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
                                  const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,

@@ -1,0 +1,772 @@
+// lora_stacked.cu -- the top-k LoRA apply of "MoLoRA: Composable Specialization via
+// Per-Token Adapter Routing" for a large stacked rank K*r (up to 1024 columns), token-major,
+// in two tcgen05 kernels around a workspace (Figure 2: a token's output is the weighted sum
+// over its top-k adapters; Table 10's shapes; Table 16: the cost of raising k):
+//
+//   y[t,:] += sum_a G[t, a*r:(a+1)*r] B_a,   G[t, a*r + j] = scale * c[t,a] * (x[t,:] A_a)[j],
+//   c[t,a] = sum_j [ids[t,j] == a] w[t,j]   (zero for the adapters a token did not select)
+//
+// i.e. the pages' sum written over all K adapters.  It costs K/k times the tensor work of
+// grouping slots by adapter, and in exchange x is read once per token and every y element
+// receives exactly one addition whatever k is, so the result is reproducible run to run.
+//
+// stacked_shrink_kernel: a 128-token tile is split over C CTAs by columns of the stacked
+//   operand [A_0 | ... | A_{K-1}] (CTA c: adapters [c*K/C, (c+1)*K/C)).  A TMA producer warp
+//   streams the tile's x K-blocks and the matching A rows through a ring of stages, one
+//   thread issues tcgen05.mma (M = 128, N = the CTA's K*r/C columns) into TMEM.  With the
+//   learned router (kRouter), W1's 64 columns ride along, 64/C per CTA, as a second MMA per
+//   K step; the CTAs of a tile exchange their ReLU'd hidden units through distributed shared
+//   memory, and every CTA evaluates the router's second stage for all 128 rows in the same
+//   order (so all agree on ids and weights) and keeps the coefficients of its own adapters.
+//   The epilogue scales each adapter's r columns by scale * c[t,a] and writes G as two bf16
+//   terms G_hi + G_lo (relative error 2^-17) to the workspace.
+// stacked_expand_kernel: a persistent tcgen05 GEMM y[N x d_out] += [G_hi | G_lo] B over
+//   tiles of 128 rows x BN columns: a TMA producer warp fills a ring of (G_hi, G_lo, B)
+//   K-blocks, one thread issues the MMAs into one of two TMEM accumulators, and four epilogue
+//   warps drain the other: TMEM -> registers -> a swizzled staging box -> a TMA tensor
+//   reduce-add into y (the fp32 addition happens in L2).  Each CTA prefetches the y rows of
+//   its next tile into L2 while it works on the current one.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace molora {
+
+namespace {
+
+constexpr int kRows = 128;      // tile rows = TMEM lanes = MMA M
+constexpr int kKBlock = 64;     // K elements per stage (one 128-byte swizzle row of bf16)
+constexpr int kEpiThreads = 128;
+constexpr int kThreads = kEpiThreads + 64;  // + TMA producer warp (4) + MMA warp (5)
+constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kSmemSlack = 1024;         // alignment of the dynamic smem base to 1024 B
+constexpr int kMaxStages = 6;
+constexpr int kHidStride = kRouterHidden + 4;  // floats per row of hidden units: conflict-free float4 rows
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------------------
+// shrink plan
+struct ShrinkPlan {
+  int C;                 // CTAs per tile (split of the stacked columns)
+  int KC;                // adapters per CTA
+  int NA;                // KC * r: adapter columns per CTA (MMA N, <= 256)
+  int NH;                // router hidden columns per CTA (64 / C; 0 without the router)
+  int S;                 // stages in the ring
+  uint32_t stage_bytes;  // x block, then the KC adapter blocks, then the W1 block
+  uint32_t off_a, off_w1;
+  uint32_t off_recv;     // router: all 64 hidden units of the 128 rows, fp32 [128][kHidStride]
+  uint32_t off_par;      // router: W2 fp32 [64][K], b1 [64], b2 [K]; then coef fp32 [128][KC]
+  uint32_t off_coef;
+  uint32_t off_ctrl;
+  uint32_t tmem_cols;
+  uint32_t smem;
+};
+
+bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s) {
+  if (K % C) return false;
+  s->C = C;
+  s->KC = K / C;
+  s->NA = s->KC * r;
+  s->NH = router ? kRouterHidden / C : 0;
+  if (s->NA > 256 || s->NA % 16 || (router && s->NH < 16)) return false;
+  s->off_a = (uint32_t)(kRows * kKBlock * 2);
+  s->off_w1 = s->off_a + (uint32_t)(s->NA * kKBlock * 2);
+  s->stage_bytes = (uint32_t)align_up(s->off_w1 + (size_t)s->NH * kKBlock * 2, 1024);
+  const size_t recv = router ? (size_t)kRows * kHidStride * 4 : 0;
+  const size_t par = router ? sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + K) : 0;
+  const size_t coef = sizeof(float) * (size_t)kRows * s->KC;
+  const size_t ctrl = 256 + 16 * kMaxStages;
+  const uint32_t cols = (uint32_t)(s->NA + s->NH);
+  s->tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+  for (int S = kMaxStages; S >= 2; --S) {
+    const size_t base = (size_t)S * s->stage_bytes;
+    const size_t off_recv = base;
+    const size_t off_par = off_recv + recv;
+    const size_t off_coef = align_up(off_par + par, 16);
+    const size_t off_ctrl = align_up(off_coef + coef, 64);
+    size_t total = off_ctrl + ctrl + kSmemSlack;
+    // all 512 TMEM columns: keep the CTA alone on its SM, so an allocation never waits
+    if (s->tmem_cols > 256 && total < 116 * 1024) total = 116 * 1024;
+    if (total <= kMaxSmem) {
+      s->S = S;
+      s->off_recv = (uint32_t)off_recv;
+      s->off_par = (uint32_t)off_par;
+      s->off_coef = (uint32_t)off_coef;
+      s->off_ctrl = (uint32_t)off_ctrl;
+      s->smem = (uint32_t)total;
+      return true;
+    }
+  }
+  return false;
+}
+
+// The fewest column splits that fit (a CTA's MMA covers at most 256 columns), then more while
+// the grid still fits the SMs twice over: a tile's CTAs run side by side.
+bool shrink_choose(int64_t N, int32_t K, int32_t r, bool router, ShrinkPlan* s) {
+  const int64_t tiles = (N + kRows - 1) / kRows;
+  bool found = false;
+  for (int C : {1, 2, 4}) {
+    ShrinkPlan t;
+    if (!shrink_layout(K, r, C, router, &t)) continue;
+    if (!found) {
+      *s = t;
+      found = true;
+    } else if (tiles * C <= (int64_t)num_sms()) {
+      *s = t;
+    }
+  }
+  return found;
+}
+
+// ---------------------------------------------------------------------------------------------
+// expand plan
+struct ExpandPlan {
+  int BN;                // output columns per tile (MMA N; two TMEM accumulators of BN columns)
+  int S;                 // stages in the ring
+  int nkb;               // K-blocks per tile: ceil(KR / 64)
+  uint32_t stage_bytes;  // G_hi block, G_lo block, BN/64 B boxes
+  uint32_t off_glo, off_b;
+  uint32_t off_stage;    // epilogue staging: 4 warps x 2 buffers x [32 rows x 128 B]
+  uint32_t off_ctrl;
+  uint32_t smem;
+};
+
+bool expand_layout(int32_t KR, int BN, ExpandPlan* s) {
+  s->BN = BN;
+  s->nkb = (KR + kKBlock - 1) / kKBlock;
+  s->off_glo = (uint32_t)(kRows * kKBlock * 2);
+  s->off_b = 2 * s->off_glo;
+  s->stage_bytes = s->off_b + (uint32_t)(BN * kKBlock * 2);
+  const size_t staging = 4 * 2 * 32 * 128;
+  const size_t ctrl = 256 + 16 * kMaxStages;
+  for (int S = kMaxStages; S >= 2; --S) {
+    const size_t off_stage = (size_t)S * s->stage_bytes;
+    const size_t off_ctrl = off_stage + staging;
+    const size_t total = off_ctrl + ctrl + kSmemSlack;
+    if (total <= kMaxSmem) {
+      s->S = S;
+      s->off_stage = (uint32_t)off_stage;
+      s->off_ctrl = (uint32_t)off_ctrl;
+      s->smem = (uint32_t)total;
+      return true;
+    }
+  }
+  return false;
+}
+
+bool expand_choose(int32_t KR, int32_t d_out, ExpandPlan* s) {
+  // 256-column tiles halve the re-reads of G; narrow outputs take 128
+  for (int BN : {256, 128})
+    if ((BN == 128 || d_out >= 256) && expand_layout(KR, BN, s)) return true;
+  return false;
+}
+
+struct __align__(8) SCtrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t mma_done;
+  uint64_t recv;
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int32_t abort;
+};
+
+__device__ __forceinline__ SmemLayout swizzle_for_row_bytes(uint32_t row_bytes) {
+  return row_bytes == 32 ? kSwizzle32B : (row_bytes == 64 ? kSwizzle64B : kSwizzle128B);
+}
+
+}  // namespace
+
+// The learned router's parameters and outputs for the fused variant.
+struct StackRouterIo {
+  const __nv_bfloat16* W2;  // [64 x K]
+  const float* b1;          // [64] or null
+  const float* b2;          // [K] or null
+  float* logits;            // [N x K] or null
+  int32_t* ids;             // [N x k]
+  float* w;                 // [N x k]
+};
+
+template <bool kRouter>
+__global__ void __launch_bounds__(kThreads, 1)
+    stacked_shrink_kernel(int64_t N, int32_t d_in, int32_t K, int32_t r, int32_t k, const int32_t* __restrict__ ids,
+                          const float* __restrict__ w, float scale, __nv_bfloat16* __restrict__ g_hi,
+                          __nv_bfloat16* __restrict__ g_lo, int32_t* err_word, const StackRouterIo rio,
+                          const ShrinkPlan P, const __grid_constant__ CUtensorMap map_x,
+                          const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w1) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SCtrl* ctrl = reinterpret_cast<SCtrl*>(sm + P.off_ctrl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = P.C, KC = P.KC, NA = P.NA, NH = P.NH, S = P.S;
+  const int crank = (int)(blockIdx.x % (unsigned)C);  // == %cluster_ctarank for the router's clusters of C
+  const bool exchange = kRouter && C > 1;
+  const int64_t t0 = (int64_t)(blockIdx.x / (unsigned)C) * kRows;
+  const int a0 = crank * KC;
+  const int KR = K * r;
+  const int nkb = d_in / kKBlock;
+  float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [128][kHidStride] hidden units (router)
+  float* w2s = reinterpret_cast<float*>(sm + P.off_par);    // [64][K]
+  float* b1s = w2s + kRouterHidden * K;
+  float* b2s = b1s + kRouterHidden;
+  float* coef = reinterpret_cast<float*>(sm + P.off_coef);  // [128][KC]
+  volatile int32_t* abort = &ctrl->abort;
+
+  if (warp == 5) {
+    tmem_alloc(&ctrl->tmem_base, P.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    mbar_init(&ctrl->mma_done, 1);
+    mbar_init(&ctrl->recv, 1);
+    ctrl->abort = 0;
+    mbar_fence_init();
+    // the other CTAs' hidden units of all 128 rows
+    if (exchange) mbar_arrive_expect_tx(&ctrl->recv, (uint32_t)kRows * (uint32_t)(kRouterHidden - NH) * 4u);
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_a);
+    if (kRouter) tma_prefetch_desc(&map_w1);
+  }
+  pdl_wait();  // x, ids and w may come from the previous kernel
+  pdl_launch_dependents();
+  if (warp < 4) {
+    if (kRouter) {
+      for (int i = tid; i < kRouterHidden * K; i += kEpiThreads) w2s[i] = __bfloat162float(rio.W2[i]);
+      if (tid < kRouterHidden) b1s[tid] = rio.b1 ? rio.b1[tid] : 0.f;
+      for (int i = tid; i < K; i += kEpiThreads) b2s[i] = rio.b2 ? rio.b2[i] : 0.f;
+    } else {
+      // this row's coefficient for each of the CTA's adapters: sum of the weights of the
+      // slots that chose it (invalid ids are skipped and reported once per tile)
+      const int64_t t = t0 + tid;
+      for (int j = 0; j < KC; ++j) coef[tid * KC + j] = 0.f;
+      if (t < N) {
+        for (int j = 0; j < k; ++j) {
+          const int32_t id = ids[t * k + j];
+          if (id >= a0 && id < a0 + KC) coef[tid * KC + (id - a0)] += w ? w[t * k + j] : 1.f;
+          if ((id < 0 || id >= K) && crank == 0) report(err_word, MOLORA_DEV_BAD_ADAPTER_ID);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+  if (exchange) cluster_arrive();  // every CTA's receive barrier is armed before any remote store
+
+  if (warp == 4) {
+    // ---- TMA producer: x K-block, the CTA's adapter rows of it, W1's columns of it
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)(kRows + NA + NH) * kKBlock * 2u;
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb, ++issued) {
+        const int s = kb % S, use = kb / S;
+        if (use > 0 && !mbar_wait_or_abort(&ctrl->empty[s], (uint32_t)(use - 1) & 1u, abort)) break;
+        uint8_t* st = sm + (size_t)s * P.stage_bytes;
+        mbar_arrive_expect_tx(&ctrl->full[s], bytes);
+        tma_load_2d(smem_u32(st), &map_x, kb * kKBlock, (int32_t)t0, &ctrl->full[s]);
+        for (int j = 0; j < KC; ++j)
+          tma_load_2d(smem_u32(st + P.off_a + (size_t)j * kKBlock * r * 2), &map_a, 0,
+                      (a0 + j) * d_in + kb * kKBlock, &ctrl->full[s]);
+        if (kRouter) tma_load_2d(smem_u32(st + P.off_w1), &map_w1, crank * NH, kb * kKBlock, &ctrl->full[s]);
+      }
+      // nothing may land in shared memory after the CTA has left: wait for the last loads
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = (issued - 1 - s) / S;  // last use of stage s
+        mbar_wait(&ctrl->full[s], (uint32_t)last & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_a = idesc_bf16_f32(kRows, (uint32_t)NA, false, true);
+      const uint32_t idesc_h = idesc_bf16_f32(kRows, (uint32_t)(NH > 0 ? NH : 16), false, true);
+      const SmemLayout swa = swizzle_for_row_bytes((uint32_t)r * 2u);
+      const SmemLayout swh = swizzle_for_row_bytes((uint32_t)NH * 2u);
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % S;
+        ok = mbar_wait_or_abort(&ctrl->full[s], (uint32_t)(kb / S) & 1u, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t* st = sm + (size_t)s * P.stage_bytes;
+        for (int ks = 0; ks < kKBlock / 16; ++ks) {
+          const uint64_t dx = smem_desc(smem_u32(st + ks * 32), 16, 1024, kSwizzle128B);
+          // the CTA's adapters stacked along N: one box of 64 rows x r per adapter
+          const uint64_t da = smem_desc(smem_u32(st + P.off_a + (size_t)ks * 16 * r * 2), (uint32_t)kKBlock * r * 2,
+                                        8u * r * 2, swa);
+          umma_f16(tmem, dx, da, idesc_a, (kb | ks) != 0);
+          if (kRouter) {
+            const uint64_t dh =
+                smem_desc(smem_u32(st + P.off_w1 + (size_t)ks * 16 * NH * 2), (uint32_t)kKBlock * NH * 2, 8u * NH * 2, swh);
+            umma_f16(tmem + (uint32_t)NA, dx, dh, idesc_h, (kb | ks) != 0);
+          }
+        }
+        umma_commit(&ctrl->empty[s]);  // the stage is free once these MMAs have read it
+      }
+      if (ok) {
+        umma_commit(&ctrl->mma_done);
+      } else {
+        report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+        umma_commit(&ctrl->mma_done);  // still arrives once every MMA issued above has finished
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- epilogue (warps 0-3, one token row per thread)
+  const int row = tid;
+  const int64_t t = t0 + row;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  bool have = false;
+  if (warp < 4) {
+    // warp-uniform: every lane of a warp must take the same branch around tcgen05.ld (.aligned)
+    have = __all_sync(0xffffffffu, mbar_wait_or_abort(&ctrl->mma_done, 0, abort) && !*abort);
+    tc_fence_after();
+    if (kRouter) {
+      // this CTA's hidden units: ReLU(x W1 + b1), kept locally and sent to the tile's other CTAs
+      for (int c0 = 0; c0 < NH; c0 += 16) {
+        float v[16];
+        if (have)
+          tmem_ld16(lane_base + (uint32_t)(NA + c0), v);
+        else
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        const int u0 = crank * NH + c0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i] + b1s[u0 + i], 0.f);
+        float* dst = recv + (size_t)row * kHidStride + u0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  }
+  if (exchange) {
+    __syncwarp();
+    cluster_wait();  // every CTA's barriers are armed
+    if (warp < 4) {
+      const uint32_t src = smem_u32(recv + (size_t)row * kHidStride + crank * NH);
+      for (int d = 1; d < C; ++d) {
+        const uint32_t peer = (uint32_t)((crank + d) % C);
+        const uint32_t dst = dsmem_addr(src, peer);
+        const uint32_t bar = dsmem_addr(smem_u32(&ctrl->recv), peer);
+        for (int c = 0; c < NH; c += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(recv + (size_t)row * kHidStride + crank * NH + c);
+          st_async_v4(dst + (uint32_t)c * 4u,
+                      make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w)),
+                      bar);
+        }
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctrl->recv, 0))) {
+        have = false;
+        if (lane == 0) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+      }
+    }
+  }
+  if (warp < 4) {
+    if (kRouter) {
+      // the router's second stage for this row, in the same order in every CTA of the tile:
+      // logit[a] = b2[a] + sum over u = 0..63 of hidden[u] W2[u,a]; top k by logit (strictly
+      // greater wins, so equal logits keep the lower index); softmax over the k, shifted by
+      // the largest.  The logits are parked in this CTA's (now idle) first stage.
+      float* lg = reinterpret_cast<float*>(sm) + (size_t)row * K;
+      float hid[kRouterHidden];
+#pragma unroll
+      for (int i = 0; i < kRouterHidden / 4; ++i) {
+        const float4 v = reinterpret_cast<const float4*>(recv + (size_t)row * kHidStride)[i];
+        hid[4 * i] = v.x, hid[4 * i + 1] = v.y, hid[4 * i + 2] = v.z, hid[4 * i + 3] = v.w;
+      }
+      for (int a = 0; a < K; ++a) {
+        float s = 0.f;
+#pragma unroll
+        for (int u = 0; u < kRouterHidden; ++u) s = fmaf(hid[u], w2s[u * K + a], s);
+        lg[a] = s + b2s[a];
+      }
+      for (int j = 0; j < KC; ++j) coef[row * KC + j] = 0.f;
+      const bool writer = crank == 0 && t < N && have;
+      if (writer && rio.logits)
+        for (int a = 0; a < K; ++a) rio.logits[t * K + a] = lg[a];
+      float m = 0.f, denom = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        const float inv = pass ? 1.f / denom : 0.f;
+        uint64_t used = 0;
+        for (int js = 0; js < k; ++js) {
+          int best = -1;
+          for (int a = 0; a < K; ++a)
+            if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
+          used |= 1ull << best;
+          if (js == 0) m = lg[best];
+          const float e = expf(lg[best] - m);
+          if (pass == 0) {
+            denom += e;
+          } else {
+            const float wj = e * inv;
+            if (writer) {
+              rio.ids[t * k + js] = best;
+              rio.w[t * k + js] = wj;
+            }
+            if (best >= a0 && best < a0 + KC) coef[row * KC + (best - a0)] = wj;
+          }
+        }
+      }
+    }
+    // G = scale * c[t,a] * (x A_a), split into bf16 hi + lo, to the workspace rows.  Every lane
+    // of the warp loads TMEM (a warp-collective instruction); rows past N store nothing.
+    if (have) {
+      for (int j = 0; j < KC; ++j) {
+        const float cf = scale * coef[row * KC + j];
+        const int64_t base = t * KR + (int64_t)(a0 + j) * r;
+        for (int c0 = 0; c0 < r; c0 += 16) {
+          float v[16];
+          tmem_ld16(lane_base + (uint32_t)(j * r + c0), v);
+          if (t >= N) continue;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float g0 = cf * v[2 * i], g1 = cf * v[2 * i + 1];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(g0), h1 = __float2bfloat16_rn(g1);
+            const __nv_bfloat16 l0 = __float2bfloat16_rn(g0 - __bfloat162float(h0));
+            const __nv_bfloat16 l1 = __float2bfloat16_rn(g1 - __bfloat162float(h1));
+            hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+            lo[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+          }
+          uint4* dh = reinterpret_cast<uint4*>(g_hi + base + c0);
+          uint4* dl = reinterpret_cast<uint4*>(g_lo + base + c0);
+          dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (exchange) {
+    cluster_arrive();
+    cluster_wait();  // no CTA leaves while a peer may still store into its shared memory
+  }
+  if (warp == 5) {
+    if (lane == 0) mbar_wait(&ctrl->mma_done, 0);  // (already complete unless a wait gave up)
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, P.tmem_cols);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    stacked_expand_kernel(int64_t N, int32_t d_out, float* __restrict__ y, int32_t* err_word, const ExpandPlan P,
+                          const __grid_constant__ CUtensorMap map_ghi, const __grid_constant__ CUtensorMap map_glo,
+                          const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_y) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SCtrl* ctrl = reinterpret_cast<SCtrl*>(sm + P.off_ctrl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BN = P.BN, S = P.S, nkb = P.nkb;
+  const int64_t m_tiles = (N + kRows - 1) / kRows;
+  const int n_tiles = (d_out + BN - 1) / BN;
+  const int64_t tiles = m_tiles * n_tiles;
+  volatile int32_t* abort = &ctrl->abort;
+  // this thread's row segment of a tile, prefetched into L2 one tile ahead
+  auto prefetch_y = [&](int64_t tile) {
+    if (tile >= tiles) return;
+    const int64_t m = tile / n_tiles;
+    const int n = (int)(tile % n_tiles);
+    const int64_t t = m * kRows + tid;
+    const int cols = min(BN, d_out - n * BN);
+    if (t < N && cols > 0) prefetch_l2_bulk(y + t * d_out + (int64_t)n * BN, (uint32_t)cols * 4u);
+  };
+
+  if (warp == 5) {
+    tmem_alloc(&ctrl->tmem_base, 2u * (uint32_t)BN);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctrl->tfull[b], 1);
+      mbar_init(&ctrl->tempty[b], kEpiThreads);
+    }
+    mbar_init(&ctrl->mma_done, 1);
+    ctrl->abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&map_ghi);
+    tma_prefetch_desc(&map_glo);
+    tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_y);
+  }
+  // y is not written by the kernel this one may overlap; a prefetch only moves lines into L2
+  if (warp < 4) prefetch_y(blockIdx.x);
+  pdl_wait();  // G comes from the previous kernel
+  pdl_launch_dependents();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 4) {
+    // ---- TMA producer: per tile, nkb K-blocks of G_hi, G_lo and B
+    if (lane == 0) {
+      const uint32_t bytes = P.stage_bytes;
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int32_t m0 = (int32_t)((tile / n_tiles) * kRows);
+        const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = (int)(it % S);
+          const int64_t use = it / S;
+          if (use > 0 && !mbar_wait_or_abort(&ctrl->empty[s], (uint32_t)(use - 1) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = sm + (size_t)s * P.stage_bytes;
+          mbar_arrive_expect_tx(&ctrl->full[s], bytes);
+          tma_load_2d(smem_u32(st), &map_ghi, kb * kKBlock, m0, &ctrl->full[s]);
+          tma_load_2d(smem_u32(st + P.off_glo), &map_glo, kb * kKBlock, m0, &ctrl->full[s]);
+          for (int q = 0; q < BN / 64; ++q)
+            tma_load_2d(smem_u32(st + P.off_b + (size_t)q * kKBlock * 128), &map_b, n0 + q * 64, kb * kKBlock,
+                        &ctrl->full[s]);
+        }
+      }
+      // nothing may land in shared memory after the CTA has left
+      const int64_t issued = it;
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int64_t last = (issued - 1 - s) / S;
+        mbar_wait(&ctrl->full[s], (uint32_t)last & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---- MMA issuer: D[buf] = G_hi B + G_lo B over the tile's K-blocks
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kRows, (uint32_t)BN, false, true);
+      int64_t it = 0, tc = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tc) {
+        const int buf = (int)(tc & 1);
+        const int64_t use = tc >> 1;
+        if (use > 0 && !mbar_wait_or_abort(&ctrl->tempty[buf], (uint32_t)(use - 1) & 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = (int)(it % S);
+          if (!mbar_wait_or_abort(&ctrl->full[s], (uint32_t)(it / S) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* st = sm + (size_t)s * P.stage_bytes;
+          for (int ks = 0; ks < kKBlock / 16; ++ks) {
+            // B: BN/64 boxes of [64 K-rows x 128 B], MN-major; 16 K-rows per step
+            const uint64_t db = smem_desc(smem_u32(st + P.off_b + ks * 2048), kKBlock * 128, 1024, kSwizzle128B);
+            const uint64_t dh = smem_desc(smem_u32(st + ks * 32), 16, 1024, kSwizzle128B);
+            const uint64_t dl = smem_desc(smem_u32(st + P.off_glo + ks * 32), 16, 1024, kSwizzle128B);
+            umma_f16(d, dh, db, idesc, (kb | ks) != 0);
+            umma_f16(d, dl, db, idesc, 1);
+          }
+          umma_commit(&ctrl->empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&ctrl->tfull[buf]);
+      }
+      if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+      // TMEM is freed below only once every MMA issued here has completed
+      umma_commit(&ctrl->mma_done);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: TMEM -> registers -> swizzled [32 rows x 32 cols] box -> TMA reduce-add into y
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    uint8_t* stg = sm + P.off_stage + (size_t)warp * 2 * 4096;
+    int sb = 0;
+    int64_t tc = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tc) {
+      const int buf = (int)(tc & 1);
+      prefetch_y(tile + gridDim.x);
+      // warp-uniform, since the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&ctrl->tfull[buf], (uint32_t)(tc >> 1) & 1u, abort))) break;
+      tc_fence_after();
+      const int32_t m0 = (int32_t)((tile / n_tiles) * kRows) + warp * 32;
+      const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
+      for (int c = 0; c < BN / 32; ++c) {
+        // boxes that start past the last row or column hold nothing of y: skipped outright
+        // (warp-uniform), so that the two staging buffers strictly alternate between issued
+        // reductions and the wait below always covers the buffer about to be rewritten
+        if (m0 >= N || n0 + c * 32 >= d_out) continue;
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)(buf * BN + c * 32), v);
+        uint8_t* box = stg + (size_t)sb * 4096;
+        if (lane == 0) bulk_wait_read<1>();  // the reduction issued from this buffer last time has read it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(box + sw128_offset((uint32_t)lane, (uint32_t)i)) =
+              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&map_y, smem_u32(box), n0 + c * 32, m0);
+          bulk_commit();
+        }
+        sb ^= 1;
+      }
+      tc_fence_before();
+      mbar_arrive(&ctrl->tempty[buf]);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 5) {
+    mbar_wait(&ctrl->mma_done, 0);
+    tc_fence_after();
+    tmem_dealloc(tmem, 2u * (uint32_t)BN);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 stacked_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major [rows x cols] array of `esize`-byte elements.
+bool stacked_map(CUtensorMap* m, CUtensorMapDataType type, uint32_t esize, const void* base, uint64_t rows,
+                 uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = stacked_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, type, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle swizzle_for(uint32_t row_bytes) {
+  return row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                         : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+size_t g_bytes(int64_t N, int32_t KR) { return align_up((size_t)N * (size_t)KR * 2u, 256); }
+
+}  // namespace
+
+bool stacked_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
+                       bool router) {
+  if (dtype != MOLORA_BF16 || !(r == 16 || r == 32 || r == 64) || d_in % kKBlock || d_out % 8) return false;
+  ShrinkPlan sp;
+  ExpandPlan ep;
+  return shrink_choose(N, K, r, router, &sp) && expand_choose(K * r, d_out, &ep) && stacked_encoder() != nullptr;
+}
+
+size_t stacked_workspace_bytes(int64_t N, int32_t K, int32_t r) { return 2 * g_bytes(N, K * r); }
+
+// Where AUTO takes the stacked pair: a stacked rank of at least 256 columns (beyond the one-kernel
+// dense path) over at least 1024 tokens, the top-k scaling regime.
+bool stacked_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, int32_t k,
+                       bool router) {
+  (void)k;
+  return K * r >= 256 && N >= 1024 && stacked_supported(dtype, N, d_in, d_out, K, r, router);
+}
+
+cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
+                                int32_t K, int32_t r, const int32_t* ids, const float* w, int32_t k, float scale,
+                                float* y, void* ws, int32_t* err_word, const void* W1, const float* b1,
+                                const void* W2, const float* b2, float* logits, int32_t* ids_out, float* w_out,
+                                cudaStream_t stream) {
+  const bool router = W1 != nullptr;
+  const int32_t KR = K * r;
+  ShrinkPlan sp;
+  ExpandPlan ep;
+  if (!shrink_choose(N, K, r, router, &sp) || !expand_choose(KR, d_out, &ep)) return cudaErrorNotSupported;
+  __nv_bfloat16* g_hi = static_cast<__nv_bfloat16*>(ws);
+  __nv_bfloat16* g_lo = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + g_bytes(N, KR));
+  CUtensorMap map_x, map_a, map_w1, map_ghi, map_glo, map_b, map_y;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // x [N x d_in]: boxes of 128 rows x 64 columns (K-major, 128-byte swizzle)
+  if (!stacked_map(&map_x, BF, 2, x, (uint64_t)N, (uint64_t)d_in, kKBlock, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // A seen as [K*d_in x r]: boxes of 64 rows of one adapter, swizzle matching r (MN-major)
+  if (!stacked_map(&map_a, BF, 2, A, (uint64_t)K * d_in, (uint64_t)r, (uint32_t)r, kKBlock, swizzle_for((uint32_t)r * 2)))
+    return cudaErrorInvalidValue;
+  if (router) {
+    // W1 [d_in x 64]: boxes of 64 rows x the CTA's 64/C columns
+    if (!stacked_map(&map_w1, BF, 2, W1, (uint64_t)d_in, kRouterHidden, (uint32_t)sp.NH, kKBlock,
+                     swizzle_for((uint32_t)sp.NH * 2)))
+      return cudaErrorInvalidValue;
+  } else {
+    std::memset(&map_w1, 0, sizeof(map_w1));
+  }
+  // G_hi, G_lo [N x K*r]: boxes of 128 rows x 64 columns (K-major); columns past K*r read as 0
+  if (!stacked_map(&map_ghi, BF, 2, g_hi, (uint64_t)N, (uint64_t)KR, kKBlock, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !stacked_map(&map_glo, BF, 2, g_lo, (uint64_t)N, (uint64_t)KR, kKBlock, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // B seen as [K*r x d_out]: boxes of 64 rows x 64 columns (MN-major); rows past K*r read as 0
+  if (!stacked_map(&map_b, BF, 2, B, (uint64_t)KR, (uint64_t)d_out, 64, kKBlock, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // y [N x d_out] fp32: reduce boxes of 32 rows x 32 columns (128-byte swizzle)
+  if (!stacked_map(&map_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, (uint64_t)N, (uint64_t)d_out, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(stacked_shrink_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(stacked_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(stacked_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kMaxSmem);
+    if (attr_err != cudaSuccess) cudaGetLastError();
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+
+  const StackRouterIo rio = {static_cast<const __nv_bfloat16*>(W2), b1, b2, logits, ids_out, w_out};
+  const int64_t tiles = (N + kRows - 1) / kRows;
+  // the router variant exchanges hidden units within a tile's CTAs: a cluster of C
+  const int cluster = router && sp.C > 1 ? sp.C : 0;
+  cudaError_t e = launch_kernel(router ? stacked_shrink_kernel<true> : stacked_shrink_kernel<false>,
+                                dim3((unsigned)(tiles * sp.C)), dim3(kThreads), sp.smem, stream, cluster, N, d_in, K,
+                                r, k, ids, w, scale, g_hi, g_lo, err_word, rio, sp, map_x, map_a, map_w1);
+  if (e != cudaSuccess) return e;
+  const int64_t exp_tiles = tiles * ((d_out + ep.BN - 1) / ep.BN);
+  const int grid = (int)(exp_tiles < num_sms() ? exp_tiles : num_sms());
+  return launch_kernel(stacked_expand_kernel, dim3((unsigned)grid), dim3(kThreads), ep.smem, stream, 0, N, d_out, y,
+                       err_word, ep, map_ghi, map_glo, map_b, map_y);
+}
+
+}  // namespace molora
