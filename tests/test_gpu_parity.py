@@ -857,10 +857,15 @@ def test_router_apply_fused_empty_and_unsupported(m):
     y = dev(wl.y0)[:0]
     m.molora_router_lora_apply(x[:0], W1, W2, A, B, 2, y, wl.scale)  # N = 0: nothing launched
     wl16 = workloads.make("topk_mlp", N=64, d_in=512, d_out=512, K=16, r=16, k=2)  # K*r = 256
+    x16, W1_16, W2_16, A16, B16 = dev(wl16.x), dev(wl16.W1), dev(wl16.W2), dev(wl16.A), dev(wl16.B)
+    # beyond the one-kernel family: refused without a workspace ...
     with pytest.raises(m.MoloraError):
-        m.molora_router_lora_apply(dev(wl16.x), dev(wl16.W1), dev(wl16.W2), dev(wl16.A), dev(wl16.B), 2,
-                                   dev(wl16.y0), wl16.scale)
+        m.molora_router_lora_apply(x16, W1_16, W2_16, A16, B16, 2, dev(wl16.y0), wl16.scale, use_ws=False)
+    # ... and run by the stacked pair when one may be used
+    y16 = dev(wl16.y0).clone()
+    logits, ids, w = m.molora_router_lora_apply(x16, W1_16, W2_16, A16, B16, 2, y16, wl16.scale)
     torch.cuda.synchronize()
+    check_learned_apply(wl16, 2, logits, ids, w, y16)
 
 
 # ------------------------------------------------------------------------- full-size workloads
