@@ -64,7 +64,9 @@ typedef enum {
   MOLORA_OK = 0,
   MOLORA_ERR_INVALID_ARG = 1,
   MOLORA_ERR_UNSUPPORTED = 2,
-  MOLORA_ERR_CUDA = 3
+  MOLORA_ERR_CUDA = 3,
+  MOLORA_ERR_SCRATCH_TOO_SMALL = 4  /* molora_lora_apply_static_ws: the problem needs more than
+                                       its fixed scratch holds */
 } molora_status;
 
 typedef enum { MOLORA_F32 = 0, MOLORA_BF16 = 1 } molora_dtype;
@@ -309,6 +311,38 @@ MOLORA_API molora_status molora_router_lora_apply(const void* x, molora_dtype dt
                                        int32_t k, float scale, float* logits, int32_t* ids, float* w,
                                        void* y, int32_t y_bf16, void* ws, size_t* ws_bytes,
                                        int32_t* err_word, cudaStream_t stream);
+
+/*
+ * molora_lora_apply_static_ws -- molora_lora_apply on the stacked path (MOLORA_PATH_STACKED)
+ * for callers that cannot allocate device memory.  The paper has no counterpart: this is a
+ * convenience of this library.
+ *
+ * Who needs it: code that runs where cudaMalloc is not an option -- a process whose device
+ * memory is entirely reserved by another allocator (a serving framework's pool), a latency
+ * path that may not call cudaMalloc or cudaFree because they can synchronise the device, or a
+ * caller that holds only raw pointers and a stream and has no allocator at all.  Instead of a
+ * caller-provided workspace it uses a fixed scratch buffer compiled into the library (a
+ * file-scope device array of MOLORA_STATIC_SCRATCH_BYTES, held by every GPU that loads the
+ * library until the process exits).  The call itself allocates nothing.
+ *
+ * Arguments and results: those of molora_lora_apply (y fp32, bf16 x/A/B, d_in a multiple of
+ * 64); the results equal molora_lora_apply_ex with MOLORA_PATH_STACKED.
+ * Limit: 2 * roundup256(N * K * r * 2) <= MOLORA_STATIC_SCRATCH_BYTES (N * K * r up to 4M,
+ * e.g. N = 8192 tokens at K*r = 512); larger problems return MOLORA_ERR_SCRATCH_TOO_SMALL
+ * before anything is launched.  Shapes the stacked path does not support return
+ * MOLORA_ERR_UNSUPPORTED.
+ * Sharing: every call on a device uses the same buffer, which keeps the last call's contents
+ * (nothing in it needs to start at zero).  Calls whose work can overlap on the GPU -- on
+ * different streams, or from several threads -- race on it and must be serialised by the
+ * caller.
+ * Set-up: the first call on each device looks up the buffer's device address (with that
+ * device current); make that first call before any stream capture begins.
+ */
+#define MOLORA_STATIC_SCRATCH_BYTES (16u << 20)
+MOLORA_API molora_status molora_lora_apply_static_ws(const void* x, molora_dtype dtype, int64_t N, int32_t d_in,
+                                          int32_t d_out, const void* A, const void* B, int32_t K, int32_t r,
+                                          const int32_t* ids, const float* w, int32_t k, float scale,
+                                          float* y, int32_t* err_word, cudaStream_t stream);
 
 /*
  * molora_lora_apply_masked_pass -- one pass of the per-sequence baseline (Tables 3 and 7:

@@ -27,13 +27,14 @@ from . import build as _build
 __all__ = [
     "molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
     "molora_lora_apply", "molora_lora_apply_masked_pass", "molora_route_vocab_lora_apply",
-    "molora_router_lora_apply", "molora_select_path", "molora_workspace_bytes",
+    "molora_router_lora_apply", "molora_select_path", "molora_workspace_bytes", "molora_lora_apply_static_ws",
     "molora_selftest_bounded_wait", "library_path", "load_library",
     "MoloraError", "PATHS", "DEV_TOKEN_OUTSIDE_RANGES", "DEV_BAD_RANGES", "DEV_BAD_ADAPTER_ID",
     "DEV_BAD_PERMUTATION", "DEV_WAIT_TIMEOUT", "MAX_ADAPTERS", "ROUTER_HIDDEN",
 ]
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_SCRATCH_TOO_SMALL = 0, 1, 2, 3, 4
+STATIC_SCRATCH_BYTES = 16 << 20
 F32, BF16 = 0, 1
 PATHS = {"auto": 0, "scalar": 1, "grouped": 2, "dense": 3, "stacked": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
@@ -49,7 +50,7 @@ EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molo
             "molora_lora_apply", "molora_router_lora_apply", "molora_route_vocab_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
             "molora_lora_apply_masked_pass", "molora_select_path", "molora_status_string", "molora_version",
-            "molora_selftest_bounded_wait")
+            "molora_selftest_bounded_wait", "molora_lora_apply_static_ws")
 
 
 class MoloraError(RuntimeError):
@@ -90,6 +91,7 @@ def load_library():
     lib.molora_route_vocab_lora_apply.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P, P,
                                                   P, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
+    lib.molora_lora_apply_static_ws.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, F, P, P, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
     lib.molora_status_string.argtypes = [S]
     lib.molora_status_string.restype = ctypes.c_char_p
@@ -98,7 +100,8 @@ def load_library():
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
                  "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
                  "molora_router_lora_apply", "molora_route_vocab_lora_apply", "molora_lora_apply_masked_pass",
-                 "molora_select_path", "molora_version", "molora_selftest_bounded_wait"):
+                 "molora_select_path", "molora_version", "molora_selftest_bounded_wait",
+                 "molora_lora_apply_static_ws"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -504,6 +507,36 @@ def molora_router_lora_apply(x, W1, W2, A, B, k, y, scale, b1=None, b2=None, log
     else:
         _check("molora_router_lora_apply", call(None, None))
     return logits, ids, w
+
+
+def molora_lora_apply_static_ws(x, A, B, ids, y, scale, w=None, err_word=None, stream=None):
+    """The stacked apply for callers that cannot allocate device memory: the workspace is a
+    fixed scratch buffer inside the library (STATIC_SCRATCH_BYTES; N*K*r up to 4M), shared by
+    every call on the device -- calls that may overlap on the GPU must be serialised.  The
+    first call on a device looks the buffer up; make it before capturing a CUDA graph.
+    Same results as molora_lora_apply(..., path="stacked"); y (fp32) is updated in place."""
+    if x.dim() != 2 or A.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [N, d_in], A [K, d_in, r] and B [K, r, d_out]")
+    N, d_in = x.shape
+    K, _, r = A.shape
+    d_out = B.shape[2]
+    if A.shape[1] != d_in or tuple(B.shape[:2]) != (K, r):
+        raise ValueError("A must be [K, d_in, r] and B [K, r, d_out]")
+    k = _slots(ids, N)
+    if y.dim() != 2 or tuple(y.shape) != (N, d_out):
+        raise ValueError(f"y must be [N, d_out] = {(N, d_out)}, got {tuple(y.shape)}")
+    _need(w, "w", N * k, rows=N)
+    _cuda(x, "x", None, 2)
+    dev = x.device
+    _cuda(A, "A", x.dtype, 3, device=dev)
+    _cuda(B, "B", x.dtype, 3, device=dev)
+    _cuda(ids, "ids", torch.int32, device=dev)
+    _cuda(y, "y", torch.float32, 2, device=dev)
+    _sized(w, "w", N * k, torch.float32, dev)
+    _check("molora_lora_apply_static_ws", load_library().molora_lora_apply_static_ws(
+        _p(x), _dtype_code(x), N, d_in, d_out, _p(A), _p(B), K, r, _p(ids), _p(w), k, float(scale), _p(y),
+        _p(_err_word(err_word, dev)), _stream(stream, dev)))
+    return y
 
 
 def molora_lora_apply_masked_pass(x, A, B, adapter_of, a, y, scale, err_word=None, path="auto", stream=None):

@@ -289,6 +289,22 @@ molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, i
                                       nullptr, scale, y, false, a, err_word, stream));
 }
 
+molora_status molora_lora_apply_static_ws(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out,
+                                          const void* A, const void* B, int32_t K, int32_t r, const int32_t* ids,
+                                          const float* w, int32_t k, float scale, float* y, int32_t* err_word,
+                                          cudaStream_t stream) {
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
+  if (st != MOLORA_OK || N == 0) return st;
+  if (!stacked_supported(dtype, N, d_in, d_out, K, r, false)) return MOLORA_ERR_UNSUPPORTED;
+  const size_t need = stacked_workspace_bytes(N, K, r);
+  if (need > stacked_static_scratch_bytes() || stacked_static_scratch_bytes() != MOLORA_STATIC_SCRATCH_BYTES)
+    return MOLORA_ERR_SCRATCH_TOO_SMALL;
+  void* scratch = nullptr;
+  if (stacked_static_scratch(&scratch) != cudaSuccess) return MOLORA_ERR_CUDA;
+  return launched(launch_lora_stacked(x, N, d_in, d_out, A, B, K, r, ids, w, k, scale, y, scratch, err_word, nullptr,
+                                      nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, stream));
+}
+
 const char* molora_status_string(molora_status status) {
   switch (status) {
     case MOLORA_OK:
@@ -299,6 +315,8 @@ const char* molora_status_string(molora_status status) {
       return "unsupported shape for this path";
     case MOLORA_ERR_CUDA:
       return "CUDA launch error";
+    case MOLORA_ERR_SCRATCH_TOO_SMALL:
+      return "problem too large for the fixed scratch buffer (N * K * r too large)";
   }
   return "unknown status";
 }

@@ -64,6 +64,11 @@ cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t 
                                 const void* W2, const float* b2, float* logits, int32_t* ids_out, float* w_out,
                                 cudaStream_t stream);
 
+// The fixed scratch of molora_lora_apply_static_ws: its size, and its device address on the
+// current device (looked up on the first call per device).
+size_t stacked_static_scratch_bytes();
+cudaError_t stacked_static_scratch(void** ptr);
+
 // CUDA-core learned router (any dtype / shape).
 cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
                                  const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,

@@ -769,4 +769,45 @@ cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t 
                        err_word, ep, map_ghi, map_glo, map_b, map_y);
 }
 
+
+// ---------------------------------------------------------------------------------------------
+// Fixed scratch for molora_lora_apply_static_ws: a caller that cannot allocate device memory
+// (see include/molora.h) gets the stacked path's workspace from this file-scope array instead.
+// Every GPU that loads the library holds it until the process exits.  All calls on a device
+// share it, so calls that may run at the same time on the GPU (different streams, or graphs
+// replayed concurrently) race on it; nothing in it has to start at zero, because the shrink
+// writes every row of G that the expand reads (rows past N come from the tensor map's
+// out-of-bounds zero fill, not from memory).
+namespace {
+constexpr size_t kStaticScratchBytes = 16u << 20;
+constexpr int kMaxDevices = 64;
+}  // namespace
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+size_t stacked_static_scratch_bytes() { return kStaticScratchBytes; }
+
+// The device address of g_static_scratch on the current device.  In host code the array's
+// name only stands for the device symbol, so the address is looked up once per device (with
+// that device current) and cached; the first call on a device does this.
+cudaError_t stacked_static_scratch(void** ptr) {
+  static void* addr[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace molora
