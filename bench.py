@@ -65,10 +65,13 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "topk", "router", "perseq", "skew",
-                                      "bf16y", "indirect", "split"],
+                                      "bf16y", "indirect", "split", "kernels"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
+    p.add_argument("--topk-k", default="1,2,3,4", help="--mode topk: comma-separated k values")
+    p.add_argument("--topk-arms", default="fused_stacked,grouped,router",
+                   help="--mode topk: which of fused_stacked, grouped, router to time")
     return p.parse_args(argv)
 
 
@@ -306,6 +309,9 @@ def run_ours(args, rank, world, local):
     traffic = load_profiled_traffic(args.path)
     if traffic is not None:
         roof["traffic"] = traffic
+        roof["traffic_source"] = ("ncu, profiles/lora_grouped_kernel_modality4.md: dram__bytes_read.sum + "
+                                  "dram__bytes_write.sum per launch, steady state (--cache-control none, "
+                                  "back-to-back launches of this command), mean of three launches")
 
     e2e = None
     if not args.no_e2e:
@@ -412,8 +418,10 @@ def run_e2e(m, wl, dev, args, world):
 
 
 def load_profiled_traffic(path):
-    """DRAM bytes (read + write) per apply launch from the committed ncu summary of the
-    grouped kernel on this workload (a line `dram_bytes_per_launch: <int>`), or None."""
+    """DRAM bytes per apply launch from the committed ncu summary of the grouped kernel on
+    this workload (a line `dram_bytes_per_launch: <int>`): read + write, measured in steady
+    state over back-to-back launches with the caches left alone (so the y write-back the
+    launch causes is counted).  None for the scalar path."""
     fn = os.path.join(ROOT, "profiles", "lora_grouped_kernel_modality4.md")
     if path == "scalar" or not os.path.exists(fn):
         return None
@@ -839,7 +847,8 @@ def run_mode(args):
                     emit(row)
     elif args.mode == "topk":
         peak = measured_peaks()[0].get("hbm_gbs")
-        for k in (1, 2, 3, 4):
+        arms = set(args.topk_arms.split(","))
+        for k in (int(v) for v in args.topk_k.split(",")):
             wl = workloads.make("topk_scaling", k=k)
             x, W1, W2, A, B, y = (wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev), wl.A.to(dev), wl.B.to(dev),
                                   wl.y0.to(dev))
@@ -864,16 +873,24 @@ def run_mode(args):
                       + wl.d_in * 64 * 2 + wl.N * 2 * k * 4)
             res = {}
             for name, fn, reps in (("fused_stacked", fused, args.replays), ("grouped", grouped, min(args.replays, 200))):
-                ms = _replay_ms(_graph(fn, stream), stream, reps)
+                if name not in arms:
+                    continue
+                g_arm = _graph(fn, stream)
+                clocks = ClockSampler(0)
+                clocks.start()
+                ms = _replay_ms(g_arm, stream, reps)
+                clk = clocks.stop()
                 p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
-                res[name] = {"p50_ms": round(p50, 5), "p99_ms": round(p99, 5), "replays": reps,
+                res[name] = {"p50_ms": round(p50, 5), "p99_ms": round(p99, 5), "replays": reps, "clocks": clk,
                              "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1),
                              "GBps_p50": round(nbytes / (p50 * 1e-3) / 1e9, 1),
                              "frac_of_measured_hbm": round(nbytes / (p50 * 1e-3) / 1e9 / peak, 3) if peak else None}
-            r_ms = _replay_ms(_graph(lambda: m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False),
-                                     stream), stream, min(args.replays, 200))
+            if "router" in arms:
+                r_ms = _replay_ms(_graph(lambda: m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False),
+                                         stream), stream, min(args.replays, 200))
+                res["router_alone_us_p50"] = round(_pct(r_ms, 0.5) * 1e3, 2)
             emit({"mode": "topk", "workload": "N=8192, d=4096, K=8, r=64, router d->64->K", "k": k,
-                  "algorithmic_bytes": nbytes, **res, "router_alone_us_p50": round(_pct(r_ms, 0.5) * 1e3, 2),
+                  "algorithmic_bytes": nbytes, **res,
                   "l2": "not flushed (back-to-back replays; 344 MB of inputs and outputs exceed the L2)"})
     elif args.mode == "router":
         wl = workloads.make("topk_mlp")
@@ -898,12 +915,31 @@ def run_mode(args):
             m.molora_lora_apply(x, A, B, ids, y, wl.scale, w=w, path="dense")
 
         def path_fused():  # router and dense apply in one kernel: x is read once
-            m.molora_router_lora_apply(x, W1, W2, A, B, wl.k, y, wl.scale, logits=logits, ids=ids, w=w)
+            m.molora_router_lora_apply(x, W1, W2, A, B, wl.k, y, wl.scale, logits=logits, ids=ids, w=w, use_ws=False)
+
+        ws = torch.empty(max(256, m.molora_workspace_bytes(wl.N, wl.d_in, wl.d_out, wl.K, wl.r, wl.k, path="stacked")),
+                         dtype=torch.uint8, device=dev)
+
+        def path_stacked():  # router in the stacked shrink, then the expand GEMM: x read once
+            m.molora_router_lora_apply(x, W1, W2, A, B, wl.k, y, wl.scale, logits=logits, ids=ids, w=w, ws=ws)
 
         r_ms = _replay_ms(g_router, stream, 100, flush)
         res = {}
-        for name, fn in (("grouped", path_grouped), ("dense", path_dense), ("fused", path_fused)):
+        for name, fn in (("grouped", path_grouped), ("dense", path_dense), ("fused", path_fused),
+                         ("fused_stacked", path_stacked)):
             res[f"path_{name}_us_p50"] = round(_pct(_replay_ms(_graph(fn, stream), stream, 100, flush), 0.5) * 1e3, 2)
+        # the two one-pass paths back to back (no flush), 200 replays: p50, p99 and the fraction of
+        # measured HBM for x once, y read + written, A, B, W1, logits, ids and w
+        nbytes = (wl.N * wl.d_in * 2 + 2 * wl.N * wl.d_out * 4 + wl.K * (wl.d_in * wl.r + wl.r * wl.d_out) * 2
+                  + wl.d_in * 64 * 2 + wl.N * (wl.K + 2 * wl.k) * 4)
+        peak = measured_peaks()[0].get("hbm_gbs")
+        for name, fn in (("fused", path_fused), ("fused_stacked", path_stacked)):
+            ms = _replay_ms(_graph(fn, stream), stream, 200)
+            p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
+            res[f"b2b_{name}"] = {"p50_us": round(p50 * 1e3, 2), "p99_us": round(p99 * 1e3, 2),
+                                  "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1),
+                                  "frac_of_measured_hbm": round(nbytes / (p50 * 1e-3) / 1e9 / peak, 3) if peak else None}
+        res["algorithmic_bytes"] = nbytes
         path_grouped()  # ids, w, counts, offsets and perm for the apply-only graphs
         torch.cuda.synchronize()
         for name in ("grouped", "dense"):
@@ -920,6 +956,36 @@ def run_mode(args):
               **res, "auto_path": auto, "path_us_p50": best,
               "fused_tokens_per_s": round(wl.N / (res["path_fused_us_p50"] * 1e-6), 1),
               "path_tokens_per_s": round(wl.N / (best * 1e-6), 1), "l2": "flushed between replays"})
+    elif args.mode == "kernels":
+        # single-kernel invocations at the shapes where AUTO uses them, for per-kernel rooflines
+        # and ncu captures: the scalar apply at decode batches (d = 4096, r = 16, K = 16 hot-set
+        # adapters, top-1 uniform) and the CUDA-core router on fp32 x (the learned-router shape)
+        peak = measured_peaks()[0].get("hbm_gbs")
+        for b in (160, 512):
+            wl = workloads.make("decode_sweep", N=b, K=16)
+            x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+            adapter = m.molora_route_vocab(wl.tok.to(dev), wl.starts.to(dev))
+            torch.cuda.synchronize()
+            used = int((torch.bincount(adapter.cpu().long(), minlength=wl.K) > 0).sum().item())
+            us = _loop_us(lambda: m.molora_lora_apply(x, A, B, adapter, y, wl.scale, path="scalar"), stream)
+            nbytes = b * wl.d_in * 2 + 2 * b * wl.d_out * 4 + used * (wl.d_in * wl.r + wl.r * wl.d_out) * 2 + b * 4
+            emit({"mode": "kernels", "kernel": "lora_scalar_kernel",
+                  "workload": f"batch {b}, d_in=d_out=4096, K=16 hot-set adapters ({used} touched), r=16, top-1",
+                  "us_per_call": round(us, 3), "algorithmic_bytes": nbytes,
+                  "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                  "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 3) if peak else None,
+                  "timing": "50 calls back to back in one CUDA graph (the hot set stays in L2)"})
+        wl = workloads.make("topk_mlp", dtype=torch.float32)
+        x, W1, W2 = wl.x.to(dev), wl.W1.to(dev), wl.W2.to(dev)
+        ids = torch.empty(wl.N, wl.k, dtype=torch.int32, device=dev)
+        w = torch.empty(wl.N, wl.k, dtype=torch.float32, device=dev)
+        us = _loop_us(lambda: m.molora_router_topk(x, W1, W2, wl.k, ids=ids, w=w, want_logits=False), stream, n=20)
+        nbytes = wl.N * wl.d_in * 4 + wl.d_in * 64 * 4 + 64 * wl.K * 4 + wl.N * 2 * wl.k * 4
+        emit({"mode": "kernels", "kernel": "router_scalar_kernel",
+              "workload": "fp32 x, N=4096, d_in=2048 -> 64 -> K=4, top-2", "us_per_call": round(us, 3),
+              "algorithmic_bytes": nbytes, "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+              "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 3) if peak else None,
+              "timing": "20 calls back to back in one CUDA graph (x is 33.6 MB: L2-resident)"})
     elif args.mode == "perseq":
         wl = workloads.make(WORKLOAD)
         tok, starts = wl.tok.to(dev), wl.starts.to(dev)

@@ -516,6 +516,24 @@ def test_apply_indirect_equals_slab(m, path, name, kw):
     assert_apply_close(y_ind, y_ref)
 
 
+def test_apply_indirect_auto_never_takes_the_dense_path(m):
+    # k = 2 at a shape where AUTO prefers the dense path for slabs: with the indirect layout it
+    # must choose among the kernels that read the adapter table, and still match the oracle
+    wl = workloads.make("modality4", N=2048, d_in=4096, d_out=4096)
+    assert m.molora_select_path(wl.dtype, wl.N, wl.d_in, wl.d_out, wl.K, wl.r, 2) == "dense"
+    ids, w = random_topk(wl.N, wl.K, 2, seed=77)
+    A_list, B_list = separate_adapters(wl)
+    counts, offsets, perm = m.molora_dispatch(dev(ids), wl.K)
+    y = dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(wl.x), A_list, B_list, dev(ids), y, wl.scale, w=dev(w), counts=counts, offsets=offsets,
+                        perm=perm, err_word=e, path="auto")
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, ids, wl.y0, wl.scale, w)
+    assert_apply_close(y, y_ref)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_apply_indirect_topk_and_bf16y(m, path):
     k = 2

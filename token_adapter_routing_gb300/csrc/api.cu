@@ -90,10 +90,14 @@ static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, in
                                  : check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, ids, k, y);
   if (st != MOLORA_OK) return st;
   if (path == MOLORA_PATH_AUTO) {
-    path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
-    if (path == MOLORA_PATH_STACKED && (!have_ws || table || y_bf16 || !stacked_supported(dtype, N, d_in, d_out, K, r, false)))
-      path = select_without_ws(dtype, N, d_in, d_out, K, r, k, table != nullptr);
-    if (path == MOLORA_PATH_DENSE && table) path = MOLORA_PATH_GROUPED;  // the dense path reads the slabs
+    if (table) {
+      // the adapter table is read by the scalar and grouped kernels only: choose between them
+      path = select_without_ws(dtype, N, d_in, d_out, K, r, k, true);
+    } else {
+      path = molora_select_path(dtype, N, d_in, d_out, K, r, k);
+      if (path == MOLORA_PATH_STACKED && (!have_ws || y_bf16 || !stacked_supported(dtype, N, d_in, d_out, K, r, false)))
+        path = select_without_ws(dtype, N, d_in, d_out, K, r, k, false);
+    }
   }
   if (path == MOLORA_PATH_STACKED) {
     if (!have_ws) return N == 0 ? MOLORA_OK : MOLORA_ERR_INVALID_ARG;

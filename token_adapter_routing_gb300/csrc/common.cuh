@@ -140,6 +140,19 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// bulk_wait_read<n> for a run-time n in 0..7 (larger values wait as for 7).
+__device__ __forceinline__ void bulk_wait_read_upto(int n) {
+  switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    default: bulk_wait_read<7>(); break;
+  }
+}
 
 // ------------------------------------------------------------------ TMA (tensor maps)
 __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* map, int32_t c0, int32_t c1,
@@ -157,6 +170,12 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(c0), "r"(c1), "r"(ssrc)
+               : "memory");
+}
+// Asks L2 to fetch one box of a tensor map (no shared memory involved, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
                : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

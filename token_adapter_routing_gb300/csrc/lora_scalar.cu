@@ -246,45 +246,89 @@ cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int
 }
 
 // ---------------------------------------------------------------------------------------
-// CUDA-core router: 8 tokens per CTA so each W1 element is read once per 8 tokens.  Four
-// thread groups split d_in; thread j of a group accumulates hidden unit j.  Then the 64 x K
-// second layer, and one thread per token selects the top k (strictly greater wins, so equal
-// logits keep the lower index) and renormalises the softmax over the selected k.
-constexpr int kRouterTok = 8;
+// CUDA-core router (fp32 x, or shapes the tensor-core router does not take).  A CTA owns 16
+// tokens and all 64 hidden units: d_in is walked in chunks of 64, each chunk of x [16 x 64]
+// and W1 [64 x 64] staged in shared memory (two buffers; the next chunk's global loads are in
+// flight in registers while the current one is multiplied), and thread (q, u) accumulates
+// token q's hidden units 4u..4u+3 in order over d_in.  Then ReLU, the 64 x K second layer, and
+// one thread per token selects the top k (strictly greater wins, so equal logits keep the
+// lower index) and renormalises the softmax over the selected k.
+constexpr int kRouterTok = 16;
+constexpr int kRouterChunk = 64;
+constexpr int kRouterThreads = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRouterThreads)
     router_scalar_kernel(const T* __restrict__ x, int64_t N, int32_t d_in, const T* __restrict__ W1,
                          const float* __restrict__ b1, const T* __restrict__ W2, const float* __restrict__ b2,
                          int32_t K, int32_t k, float* __restrict__ logits, int32_t* __restrict__ ids,
                          float* __restrict__ w) {
-  __shared__ float part[4][kRouterTok][kRouterHidden];
-  __shared__ float hid[kRouterTok][kRouterHidden];
-  __shared__ float lg[kRouterTok][kMaxAdapters];
+  __shared__ float xs[2][kRouterTok][kRouterChunk + 1];
+  __shared__ __align__(16) float ws[2][kRouterChunk][kRouterHidden];
+  // after the main loop the W1 buffers hold the hidden units and the logits
+  float(*hid)[kRouterHidden + 1] = reinterpret_cast<float(*)[kRouterHidden + 1]>(&ws[0][0][0]);
+  float(*lg)[kMaxAdapters] = reinterpret_cast<float(*)[kMaxAdapters]>(&ws[1][0][0]);
+  static_assert(kRouterTok * (kRouterHidden + 1) <= kRouterChunk * kRouterHidden, "hidden units fit a W1 buffer");
+  static_assert(kRouterTok * kMaxAdapters <= kRouterChunk * kRouterHidden, "logits fit a W1 buffer");
+  constexpr int kXPer = kRouterTok * kRouterChunk / kRouterThreads;     // 4 x elements per thread
+  constexpr int kWPer = kRouterChunk * kRouterHidden / kRouterThreads;  // 16 W1 elements per thread
   const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
-  const int j = threadIdx.x & 63, grp = threadIdx.x >> 6;
+  const int tid = threadIdx.x, tq = tid >> 4, tu = tid & 15;
   pdl_wait();
   pdl_launch_dependents();
-  float acc[kRouterTok];
+  float rx[kXPer], rw[kWPer];
+  auto gload = [&](int c) {  // chunk c of x and W1 into registers (zero past the ends)
+    const int i0 = c * kRouterChunk;
 #pragma unroll
-  for (int q = 0; q < kRouterTok; ++q) acc[q] = 0.f;
-  for (int32_t i = grp; i < d_in; i += 4) {
-    const float wv = to_f(W1[(int64_t)i * kRouterHidden + j]);
+    for (int e = 0; e < kXPer; ++e) {
+      const int idx = tid + e * kRouterThreads, q = idx / kRouterChunk, ii = idx % kRouterChunk;
+      rx[e] = (t0 + q < N && i0 + ii < d_in) ? to_f(x[(t0 + q) * d_in + i0 + ii]) : 0.f;
+    }
 #pragma unroll
-    for (int q = 0; q < kRouterTok; ++q)
-      if (t0 + q < N) acc[q] = fmaf(to_f(x[(t0 + q) * d_in + i]), wv, acc[q]);
+    for (int e = 0; e < kWPer; ++e) {
+      const int idx = tid + e * kRouterThreads, ii = idx / kRouterHidden, u = idx % kRouterHidden;
+      rw[e] = i0 + ii < d_in ? to_f(W1[(int64_t)(i0 + ii) * kRouterHidden + u]) : 0.f;
+    }
+  };
+  auto sstore = [&](int b) {
+#pragma unroll
+    for (int e = 0; e < kXPer; ++e) {
+      const int idx = tid + e * kRouterThreads;
+      xs[b][idx / kRouterChunk][idx % kRouterChunk] = rx[e];
+    }
+#pragma unroll
+    for (int e = 0; e < kWPer; ++e) {
+      const int idx = tid + e * kRouterThreads;
+      ws[b][idx / kRouterHidden][idx % kRouterHidden] = rw[e];
+    }
+  };
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int nch = (d_in + kRouterChunk - 1) / kRouterChunk;
+  gload(0);
+  sstore(0);
+  __syncthreads();
+  for (int c = 0; c < nch; ++c) {
+    const int b = c & 1;
+    if (c + 1 < nch) gload(c + 1);
+#pragma unroll 8
+    for (int ii = 0; ii < kRouterChunk; ++ii) {
+      const float a = xs[b][tq][ii];
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[b][ii][4 * tu]);
+      acc[0] = fmaf(a, wv.x, acc[0]);
+      acc[1] = fmaf(a, wv.y, acc[1]);
+      acc[2] = fmaf(a, wv.z, acc[2]);
+      acc[3] = fmaf(a, wv.w, acc[3]);
+    }
+    if (c + 1 < nch) sstore(b ^ 1);  // buffer b^1 was last read before the previous barrier
+    __syncthreads();
   }
 #pragma unroll
-  for (int q = 0; q < kRouterTok; ++q) part[grp][q][j] = acc[q];
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < kRouterTok * kRouterHidden; idx += blockDim.x) {
-    const int q = idx / kRouterHidden, jj = idx % kRouterHidden;
-    float h = part[0][q][jj] + part[1][q][jj] + part[2][q][jj] + part[3][q][jj];
-    if (b1) h += b1[jj];
-    hid[q][jj] = h > 0.f ? h : 0.f;
+  for (int j = 0; j < 4; ++j) {
+    const float h = acc[j] + (b1 ? b1[4 * tu + j] : 0.f);
+    hid[tq][4 * tu + j] = h > 0.f ? h : 0.f;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < kRouterTok * K; idx += blockDim.x) {
+  for (int idx = tid; idx < kRouterTok * K; idx += kRouterThreads) {
     const int q = idx / K, a = idx % K;
     float s = 0.f;
     for (int jj = 0; jj < kRouterHidden; ++jj) s = fmaf(hid[q][jj], to_f(W2[jj * K + a]), s);
@@ -293,8 +337,8 @@ __global__ void __launch_bounds__(256)
     if (logits && t0 + q < N) logits[(t0 + q) * K + a] = s;
   }
   __syncthreads();
-  if (threadIdx.x < kRouterTok && t0 + threadIdx.x < N) {
-    const int q = threadIdx.x;
+  if (tid < kRouterTok && t0 + tid < N) {
+    const int q = tid;
     const int64_t t = t0 + q;
     uint64_t used = 0;
     float m = 0.f, denom = 0.f;
@@ -319,10 +363,10 @@ cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, i
                                  float* logits, int32_t* ids, float* w, cudaStream_t stream) {
   const unsigned grid = (unsigned)((N + kRouterTok - 1) / kRouterTok);
   if (dtype == MOLORA_BF16)
-    return launch_kernel(router_scalar_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, 0,
+    return launch_kernel(router_scalar_kernel<__nv_bfloat16>, dim3(grid), dim3(kRouterThreads), 0, stream, 0,
                          static_cast<const __nv_bfloat16*>(x), N, d_in, static_cast<const __nv_bfloat16*>(W1), b1,
                          static_cast<const __nv_bfloat16*>(W2), b2, K, k, logits, ids, w);
-  return launch_kernel(router_scalar_kernel<float>, dim3(grid), dim3(256), 0, stream, 0, static_cast<const float*>(x),
+  return launch_kernel(router_scalar_kernel<float>, dim3(grid), dim3(kRouterThreads), 0, stream, 0, static_cast<const float*>(x),
                        N, d_in, static_cast<const float*>(W1), b1, static_cast<const float*>(W2), b2, K, k, logits, ids,
                        w);
 }

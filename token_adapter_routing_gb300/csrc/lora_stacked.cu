@@ -30,6 +30,9 @@
 
 #include <cstring>
 #include <mutex>
+#ifdef MOLORA_TUNING_ENV
+#include <cstdlib>
+#endif
 
 #include "common.cuh"
 #include "kernels.h"
@@ -57,9 +60,12 @@ struct ShrinkPlan {
   int NA;                // KC * r: adapter columns per CTA (MMA N, <= 256)
   int NH;                // router hidden columns per CTA (64 / C; 0 without the router)
   int S;                 // stages in the ring
+  int PF;                // x K-blocks prefetched into L2 ahead of the TMA loads (0: none)
   uint32_t stage_bytes;  // x block, then the KC adapter blocks, then the W1 block
   uint32_t off_a, off_w1;
-  uint32_t off_recv;     // router: all 64 hidden units of the 128 rows, fp32 [128][kHidStride]
+  uint32_t off_recv;     // router: all 64 hidden units of the 128 rows, fp32 [128][kHidStride], in
+                         // the stage ring (free once every MMA of the tile's CTAs is done)
+  uint32_t off_lg;       // router: the rows' logits fp32 [128][K], after them in the ring
   uint32_t off_par;      // router: W2 fp32 [64][K], b1 [64], b2 [K]; then coef fp32 [128][KC]
   uint32_t off_coef;
   uint32_t off_ctrl;
@@ -67,7 +73,7 @@ struct ShrinkPlan {
   uint32_t smem;
 };
 
-bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s) {
+bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s, int max_stages = kMaxStages) {
   if (K % C) return false;
   s->C = C;
   s->KC = K / C;
@@ -78,15 +84,19 @@ bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s) {
   s->off_w1 = s->off_a + (uint32_t)(s->NA * kKBlock * 2);
   s->stage_bytes = (uint32_t)align_up(s->off_w1 + (size_t)s->NH * kKBlock * 2, 1024);
   const size_t recv = router ? (size_t)kRows * kHidStride * 4 : 0;
+  const size_t lg = router ? (size_t)kRows * K * 4 : 0;
   const size_t par = router ? sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + K) : 0;
   const size_t coef = sizeof(float) * (size_t)kRows * s->KC;
   const size_t ctrl = 256 + 16 * kMaxStages;
   const uint32_t cols = (uint32_t)(s->NA + s->NH);
   s->tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
-  for (int S = kMaxStages; S >= 2; --S) {
+  s->PF = 8;
+  s->off_recv = 0;
+  s->off_lg = (uint32_t)recv;
+  for (int S = max_stages; S >= 2; --S) {
     const size_t base = (size_t)S * s->stage_bytes;
-    const size_t off_recv = base;
-    const size_t off_par = off_recv + recv;
+    if (base < recv + lg) break;  // the router's rows live in the ring after the MMAs
+    const size_t off_par = base;
     const size_t off_coef = align_up(off_par + par, 16);
     const size_t off_ctrl = align_up(off_coef + coef, 64);
     size_t total = off_ctrl + ctrl + kSmemSlack;
@@ -94,7 +104,6 @@ bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s) {
     if (s->tmem_cols > 256 && total < 116 * 1024) total = 116 * 1024;
     if (total <= kMaxSmem) {
       s->S = S;
-      s->off_recv = (uint32_t)off_recv;
       s->off_par = (uint32_t)off_par;
       s->off_coef = (uint32_t)off_coef;
       s->off_ctrl = (uint32_t)off_ctrl;
@@ -109,10 +118,14 @@ bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s) {
 // the grid still fits the SMs twice over: a tile's CTAs run side by side.
 bool shrink_choose(int64_t N, int32_t K, int32_t r, bool router, ShrinkPlan* s) {
   const int64_t tiles = (N + kRows - 1) / kRows;
+  int max_stages = kMaxStages;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_SHR_S")) max_stages = atoi(e);
+#endif
   bool found = false;
   for (int C : {1, 2, 4}) {
     ShrinkPlan t;
-    if (!shrink_layout(K, r, C, router, &t)) continue;
+    if (!shrink_layout(K, r, C, router, &t, max_stages)) continue;
     if (!found) {
       *s = t;
       found = true;
@@ -120,6 +133,9 @@ bool shrink_choose(int64_t N, int32_t K, int32_t r, bool router, ShrinkPlan* s) 
       *s = t;
     }
   }
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_SHR_PF")) s->PF = atoi(e);
+#endif
   return found;
 }
 
@@ -129,22 +145,24 @@ struct ExpandPlan {
   int BN;                // output columns per tile (MMA N; two TMEM accumulators of BN columns)
   int S;                 // stages in the ring
   int nkb;               // K-blocks per tile: ceil(KR / 64)
+  int nstg;              // epilogue staging buffers per warp (reductions in flight per warp)
   uint32_t stage_bytes;  // G_hi block, G_lo block, BN/64 B boxes
   uint32_t off_glo, off_b;
-  uint32_t off_stage;    // epilogue staging: 4 warps x 2 buffers x [32 rows x 128 B]
+  uint32_t off_stage;    // epilogue staging: 4 warps x nstg buffers x [32 rows x 128 B]
   uint32_t off_ctrl;
   uint32_t smem;
 };
 
-bool expand_layout(int32_t KR, int BN, ExpandPlan* s) {
+bool expand_layout(int32_t KR, int BN, int nstg, int max_stages, ExpandPlan* s) {
   s->BN = BN;
   s->nkb = (KR + kKBlock - 1) / kKBlock;
+  s->nstg = nstg;
   s->off_glo = (uint32_t)(kRows * kKBlock * 2);
   s->off_b = 2 * s->off_glo;
   s->stage_bytes = s->off_b + (uint32_t)(BN * kKBlock * 2);
-  const size_t staging = 4 * 2 * 32 * 128;
+  const size_t staging = (size_t)4 * nstg * 32 * 128;
   const size_t ctrl = 256 + 16 * kMaxStages;
-  for (int S = kMaxStages; S >= 2; --S) {
+  for (int S = max_stages; S >= 2; --S) {
     const size_t off_stage = (size_t)S * s->stage_bytes;
     const size_t off_ctrl = off_stage + staging;
     const size_t total = off_ctrl + ctrl + kSmemSlack;
@@ -159,10 +177,23 @@ bool expand_layout(int32_t KR, int BN, ExpandPlan* s) {
   return false;
 }
 
+// 256-column tiles halve the re-reads of G (narrow outputs take 128).  Measured on GB300 (top-k
+// scaling workload, N = 8192, K*r = 512): three operand stages of 64 KB with two staging
+// buffers per epilogue warp beat two stages with four or six buffers (121 vs 129 us for the
+// router + apply), and 128-column tiles lose (136-146 us).
 bool expand_choose(int32_t KR, int32_t d_out, ExpandPlan* s) {
-  // 256-column tiles halve the re-reads of G; narrow outputs take 128
-  for (int BN : {256, 128})
-    if ((BN == 128 || d_out >= 256) && expand_layout(KR, BN, s)) return true;
+  int only_bn = 0, nstg = 2, max_stages = kMaxStages;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_EXP_BN")) only_bn = atoi(e);
+  if (const char* e = getenv("MOLORA_EXP_NSTG")) nstg = atoi(e);
+  if (const char* e = getenv("MOLORA_EXP_S")) max_stages = atoi(e);
+#endif
+  for (int BN : {256, 128}) {
+    if (only_bn && BN != only_bn) continue;
+    if (BN == 256 && d_out < 256) continue;
+    for (int n = nstg; n >= 2; n -= 2)
+      if (expand_layout(KR, BN, n, max_stages, s)) return true;
+  }
   return false;
 }
 
@@ -211,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int a0 = crank * KC;
   const int KR = K * r;
   const int nkb = d_in / kKBlock;
-  float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [128][kHidStride] hidden units (router)
+  float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [128][kHidStride] hidden units (router), in the ring
   float* w2s = reinterpret_cast<float*>(sm + P.off_par);    // [64][K]
   float* b1s = w2s + kRouterHidden * K;
   float* b2s = b1s + kRouterHidden;
@@ -267,9 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- TMA producer: x K-block, the CTA's adapter rows of it, W1's columns of it
     if (lane == 0) {
       const uint32_t bytes = (uint32_t)(kRows + NA + NH) * kKBlock * 2u;
+      // x streams from DRAM once per tile: the tile's first CTA asks L2 for its K-blocks PF
+      // stages ahead of the loads, so the loads see L2 latency, not DRAM latency
+      const bool prefetcher = crank == 0 && P.PF > 0;
+      if (prefetcher)
+        for (int kb = 0; kb < P.PF && kb < nkb; ++kb) tma_prefetch_l2_2d(&map_x, kb * kKBlock, (int32_t)t0);
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb, ++issued) {
         const int s = kb % S, use = kb / S;
+        if (prefetcher && kb + P.PF < nkb) tma_prefetch_l2_2d(&map_x, (kb + P.PF) * kKBlock, (int32_t)t0);
         if (use > 0 && !mbar_wait_or_abort(&ctrl->empty[s], (uint32_t)(use - 1) & 1u, abort)) break;
         uint8_t* st = sm + (size_t)s * P.stage_bytes;
         mbar_arrive_expect_tx(&ctrl->full[s], bytes);
@@ -329,32 +366,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t t = t0 + row;
   const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   bool have = false;
+  float hid_own[kRouterHidden];  // this CTA's hidden units of the row (the first NH are used)
   if (warp < 4) {
     // warp-uniform: every lane of a warp must take the same branch around tcgen05.ld (.aligned)
     have = __all_sync(0xffffffffu, mbar_wait_or_abort(&ctrl->mma_done, 0, abort) && !*abort);
     tc_fence_after();
     if (kRouter) {
-      // this CTA's hidden units: ReLU(x W1 + b1), kept locally and sent to the tile's other CTAs
-      for (int c0 = 0; c0 < NH; c0 += 16) {
-        float v[16];
-        if (have)
-          tmem_ld16(lane_base + (uint32_t)(NA + c0), v);
-        else
+      // this CTA's hidden units, ReLU(x W1 + b1), held in registers until the ring is free
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        const int u0 = crank * NH + c0;
+      for (int c0 = 0; c0 < kRouterHidden; c0 += 16) {
+        if (c0 < NH) {
+          float v[16];
+          if (have)
+            tmem_ld16(lane_base + (uint32_t)(NA + c0), v);
+          else
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i] + b1s[u0 + i], 0.f);
-        float* dst = recv + (size_t)row * kHidStride + u0;
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 16; ++i) hid_own[c0 + i] = fmaxf(v[i] + b1s[crank * NH + c0 + i], 0.f);
+        }
       }
     }
   }
   if (exchange) {
     __syncwarp();
     cluster_wait();  // every CTA's barriers are armed
+    // the receive rows live in the stage ring: nobody writes them until every CTA of the tile
+    // has finished its MMAs (its epilogue warps arrive here only after its mma_done)
+    cluster_arrive();
+    cluster_wait();
+  }
+  if (kRouter && warp < 4) {
+    float* dst = recv + (size_t)row * kHidStride + crank * NH;
+#pragma unroll
+    for (int c0 = 0; c0 < kRouterHidden; c0 += 4)
+      if (c0 < NH)
+        reinterpret_cast<float4*>(dst)[c0 / 4] = make_float4(hid_own[c0], hid_own[c0 + 1], hid_own[c0 + 2], hid_own[c0 + 3]);
+  }
+  if (exchange) {
     if (warp < 4) {
       const uint32_t src = smem_u32(recv + (size_t)row * kHidStride + crank * NH);
       for (int d = 1; d < C; ++d) {
@@ -379,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the router's second stage for this row, in the same order in every CTA of the tile:
       // logit[a] = b2[a] + sum over u = 0..63 of hidden[u] W2[u,a]; top k by logit (strictly
       // greater wins, so equal logits keep the lower index); softmax over the k, shifted by
-      // the largest.  The logits are parked in this CTA's (now idle) first stage.
-      float* lg = reinterpret_cast<float*>(sm) + (size_t)row * K;
+      // the largest.  The logits are parked in the (now idle) stage ring.
+      float* lg = reinterpret_cast<float*>(sm + P.off_lg) + (size_t)row * K;
       float hid[kRouterHidden];
 #pragma unroll
       for (int i = 0; i < kRouterHidden / 4; ++i) {
@@ -594,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---- epilogue: TMEM -> registers -> swizzled [32 rows x 32 cols] box -> TMA reduce-add into y
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint8_t* stg = sm + P.off_stage + (size_t)warp * 2 * 4096;
+    const int nstg = P.nstg;
+    uint8_t* stg = sm + P.off_stage + (size_t)warp * nstg * 4096;
     int sb = 0;
     int64_t tc = 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tc) {
@@ -607,13 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
       for (int c = 0; c < BN / 32; ++c) {
         // boxes that start past the last row or column hold nothing of y: skipped outright
-        // (warp-uniform), so that the two staging buffers strictly alternate between issued
+        // (warp-uniform), so that the staging buffers are taken strictly in turn by issued
         // reductions and the wait below always covers the buffer about to be rewritten
         if (m0 >= N || n0 + c * 32 >= d_out) continue;
         float v[32];
         tmem_ld32(lane_base + (uint32_t)(buf * BN + c * 32), v);
         uint8_t* box = stg + (size_t)sb * 4096;
-        if (lane == 0) bulk_wait_read<1>();  // the reduction issued from this buffer last time has read it
+        if (lane == 0) bulk_wait_read_upto(nstg - 1);  // the reduction last issued from this buffer has read it
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -625,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_reduce_add_2d(&map_y, smem_u32(box), n0 + c * 32, m0);
           bulk_commit();
         }
-        sb ^= 1;
+        sb = sb + 1 == nstg ? 0 : sb + 1;
       }
       tc_fence_before();
       mbar_arrive(&ctrl->tempty[buf]);
