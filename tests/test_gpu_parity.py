@@ -196,6 +196,10 @@ def test_apply_small_integers_bitexact(m, path, N, d_in, d_out, K, r, k):
     ("modality4", {"N": 1000, "d_in": 1024, "d_out": 3072}),
     ("decode_sweep", {"N": 160, "K": 16}),
     ("decode_sweep", {"N": 257, "K": 64, "dist": "zipf"}),
+    # many small groups: 64-row tiles over clusters of 4 (K = 64), and 64-row tiles past one
+    # wave (K = 32 at 512 tokens)
+    ("decode_sweep", {"N": 2048, "K": 64}),
+    ("decode_sweep", {"N": 512, "K": 32}),
     ("decode_sweep", {"N": 1, "K": 4}),
     ("modality4", {"N": 333, "d_in": 2048, "d_out": 1024, "r": 32}),
     ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048, "r": 64, "K": 8}),

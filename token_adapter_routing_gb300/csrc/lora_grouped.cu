@@ -141,12 +141,23 @@ bool plan_layout(int32_t r, size_t g_tile, size_t budget, bool two_per_sm, Group
   return false;
 }
 
-// Picks cluster size, tile rows and CTAs per SM.  Clusters of 8 with two CTAs per SM come
-// first.  A launch covers at most ceil(S/TM) + K tiles; when 64-row tiles still fit one wave
-// at two CTAs per SM, they win: twice as many half-size CTAs spread over all SMs instead of
-// leaving a few SMs with two full tiles (clusters of 8 reach only ~130 distinct SMs at one
-// CTA each), which halves the tail of the y update.  Larger batches keep 128-row tiles.
-// Shapes that fit neither fall back to one CTA per SM, then to smaller clusters.
+// Picks cluster size, tile rows and CTAs per SM from what the host knows at launch: the slot
+// count S and the number of groups K (so the mean group size S/K; the group sizes themselves
+// are only on the device, and a launch captured in a CUDA graph must not depend on them).  A
+// launch has ceil(S/TM) + K clusters (every group's last tile may be partial); the clusters of
+// empty tiles leave at once, so the tiles that run are about ceil(S/TM) + K/2.  Measured on
+// GB300 (decode sweep, d = 4096, r = 16, 256..2048 tokens, K = 8..64, uniform and Zipf(1.1);
+// the 4-modality workload with uniform, 80/10/5/5 and 95/2/2/1 shares):
+//   - 64-row tiles at two CTAs per SM win while their running tiles fit one wave (K = 8 at
+//     2048 tokens: 22.7 vs 31.8 us for 128-row tiles); once they do not, 128-row tiles win if
+//     the groups average at least 32 slots (K = 16 at 2048 tokens: 32.6 vs 36.8 us);
+//   - with 64-row tiles, clusters of 4 beat clusters of 8 when all the clusters of 8 would
+//     fill more than about 1.5 waves (K = 64 at 256..1024 tokens: 37.4 vs 42.3 us, 40.3 vs 43.9,
+//     46.3 vs 47.0); clusters of 2 and 1 lose everywhere at this width.
+//   - the skewed shares cost nothing: tiles follow the groups (20.6-20.9 us for all three).
+// What the host cannot see costs at most this much: a Zipf draw over K = 32 at 2048 tokens
+// prefers 64-row tiles (40.8 vs 46.7 us), a uniform draw over K = 64 at 2048 tokens clusters of
+// 4 (52.6 vs 60.0 us).  Shapes that fit neither fall back through the list below.
 bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, GroupedPlan* s) {
   int only_c = 0, only_one = 0, only_tm = 0;
 #ifdef MOLORA_TUNING_ENV
@@ -155,17 +166,22 @@ bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, Groupe
   if (const char* e = getenv("MOLORA_TILE_ROWS")) only_tm = atoi(e);
 #endif
   struct Cand { int C, TM; bool two; };
-  const bool small = ((S + 63) / 64 + K) * 8 <= 2 * (int64_t)num_sms();
-  static const Cand small_first[] = {{8, 64, true}};
+  const int64_t sms = num_sms();
+  const int64_t tiles64 = (S + 63) / 64;
+  const int64_t running64 = tiles64 + (K + 1) / 2;  // 64-row tiles that run (empty ones leave)
+  const int pref_tm = (running64 * 8 > 2 * sms && 2 * tiles64 >= K) ? 128 : 64;
+  // (clusters of 4 measured with 64-row tiles only; large groups keep clusters of 8)
+  const int pref_c = (pref_tm == 64 && (tiles64 + K) * 8 > 3 * sms) ? 4 : 8;
+  const Cand preferred[] = {{pref_c, pref_tm, true}, {pref_c, pref_tm, false}};
   static const Cand order[] = {{8, 128, true}, {8, 128, false}, {4, 128, true}, {4, 128, false},
                                {2, 128, true}, {2, 128, false}, {1, 128, true}, {1, 128, false},
-                               {8, 64, true}, {4, 64, true}, {4, 64, false}};
+                               {8, 64, true}, {4, 64, true}, {4, 64, false}, {8, 64, false},
+                               {2, 64, true}, {2, 64, false}, {1, 64, true}, {1, 64, false}};
   auto allowed = [&](const Cand& c) {
     return !((only_c && c.C != only_c) || (only_one && c.two) || (only_tm && c.TM != only_tm));
   };
-  if (small)
-    for (const Cand& c : small_first)
-      if (allowed(c) && plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
+  for (const Cand& c : preferred)
+    if (allowed(c) && plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
   for (const Cand& c : order)
     if (allowed(c) && plan_one(d_in, d_out, r, c.C, c.TM, c.two, s)) return true;
   return false;
