@@ -291,6 +291,44 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tcgen05.ld of 32 consecutive fp32 columns of this warp's 32 TMEM lanes WITHOUT waiting: the
+// registers are not valid until tmem_ld_wait() has run on them.  Several loads may be in flight.
+__device__ __forceinline__ void tmem_ld32_start(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for every tcgen05.ld this thread issued; the registers of `r` are read-write operands, so
+// no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+// Binds a second register block to the same completed wait (a wait covers every load issued
+// before it): marks `r` as produced here without waiting again.
+__device__ __forceinline__ void tmem_ld_bind(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // Shared-memory matrix descriptor for tcgen05.mma (sm_100 family layout):
 //   bits  0-13  start address >> 4
 //   bits 16-29  leading-dimension byte offset >> 4
@@ -343,14 +381,16 @@ __device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uin
 // Called by `nthreads` threads (a multiple of 32, thread ids 0..nthreads-1): the 8 consecutive
 // lanes of a row each take a group and the row's first lane gathers the group partials by
 // shuffles into lg_s[rl * K + a] (shared scratch), then selects and writes logits (if
-// non-null), ids and w for token t_first + rl when it is below N and `ok`.  With `coef`
-// non-null it also stores each row's per-adapter weight (w_j for a selected adapter, else 0)
-// at coef[rl * K + a].  The selection runs twice (denominator, then weights), so nothing is
-// read back from global memory; the code is kept compact because it runs once per tile.
+// non-null), ids and w for token t_first + rl when it is below N, `ok` and `store`.  With
+// `coef` non-null it also stores each row's per-adapter weight (w_j for a selected adapter,
+// else 0) at coef[rl * K + a] (whether or not `store`).  The selection runs twice (denominator,
+// then weights), so nothing is read back from global memory; the code is kept compact because
+// it runs once per tile.
 __device__ __forceinline__ void router_rows(const float* recv, int C, int rows, int stride, int col0,
                                             const float* w2s, const float* b1s, const float* b2s, int K, int k,
                                             int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
-                                            float* w, float* lg_s, float* coef, int tid, int nthreads) {
+                                            float* w, float* lg_s, float* coef, int tid, int nthreads,
+                                            bool store = true) {
   const int lane = tid & 31;
   for (int base = 0; base < rows * 8; base += nthreads) {
     const int item = base + tid;
@@ -382,7 +422,7 @@ __device__ __forceinline__ void router_rows(const float* recv, int C, int rows, 
       if (coef)
         for (int a = 0; a < K; ++a) coef[rl * K + a] = 0.f;
       if (t < N && ok) {
-        if (logits)
+        if (logits && store)
           for (int a = 0; a < K; ++a) logits[t * K + a] = lg[a];
         float m = 0.f, denom = 0.f;
         for (int pass = 0; pass < 2; ++pass) {
@@ -399,8 +439,10 @@ __device__ __forceinline__ void router_rows(const float* recv, int C, int rows, 
               denom += e;
             } else {
               const float wj = e * inv;
-              ids[t * k + js] = best;
-              w[t * k + js] = wj;
+              if (store) {
+                ids[t * k + js] = best;
+                w[t * k + js] = wj;
+              }
               if (coef) coef[rl * K + best] = wj;
             }
           }

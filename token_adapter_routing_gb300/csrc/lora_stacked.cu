@@ -65,7 +65,8 @@ struct ShrinkPlan {
   uint32_t off_a, off_w1;
   uint32_t off_recv;     // router: all 64 hidden units of the 128 rows, fp32 [128][kHidStride], in
                          // the stage ring (free once every MMA of the tile's CTAs is done)
-  uint32_t off_lg;       // router: the rows' logits fp32 [128][K], after them in the ring
+  uint32_t off_lg;       // router: the rows' logits fp32 [K][128 + 1] (transposed)
+  uint32_t off_gst;      // G staging, 4 warps x (hi, lo) x [32 rows x 128 B], after those
   uint32_t off_par;      // router: W2 fp32 [64][K], b1 [64], b2 [K]; then coef fp32 [128][KC]
   uint32_t off_coef;
   uint32_t off_ctrl;
@@ -84,7 +85,7 @@ bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s, int 
   s->off_w1 = s->off_a + (uint32_t)(s->NA * kKBlock * 2);
   s->stage_bytes = (uint32_t)align_up(s->off_w1 + (size_t)s->NH * kKBlock * 2, 1024);
   const size_t recv = router ? (size_t)kRows * kHidStride * 4 : 0;
-  const size_t lg = router ? (size_t)kRows * K * 4 : 0;
+  const size_t lg = router ? (size_t)(kRows + 1) * K * 4 : 0;
   const size_t par = router ? sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + K) : 0;
   const size_t coef = sizeof(float) * (size_t)kRows * s->KC;
   const size_t ctrl = 256 + 16 * kMaxStages;
@@ -93,9 +94,11 @@ bool shrink_layout(int32_t K, int32_t r, int C, bool router, ShrinkPlan* s, int 
   s->PF = 8;
   s->off_recv = 0;
   s->off_lg = (uint32_t)recv;
+  s->off_gst = (uint32_t)align_up(recv + lg, 1024);
+  const size_t gst = (size_t)4 * 2 * 32 * 128;
   for (int S = max_stages; S >= 2; --S) {
     const size_t base = (size_t)S * s->stage_bytes;
-    if (base < recv + lg) break;  // the router's rows live in the ring after the MMAs
+    if (base < s->off_gst + gst) break;  // the epilogue's rows live in the ring after the MMAs
     const size_t off_par = base;
     const size_t off_coef = align_up(off_par + par, 16);
     const size_t off_ctrl = align_up(off_coef + coef, 64);
@@ -243,10 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KR = K * r;
   const int nkb = d_in / kKBlock;
   float* recv = reinterpret_cast<float*>(sm + P.off_recv);  // [128][kHidStride] hidden units (router), in the ring
-  float* w2s = reinterpret_cast<float*>(sm + P.off_par);    // [64][K]
-  float* b1s = w2s + kRouterHidden * K;
+  float* w2T = reinterpret_cast<float*>(sm + P.off_par);    // [K][64]: W2 transposed
+  float* b1s = w2T + kRouterHidden * K;
   float* b2s = b1s + kRouterHidden;
-  float* coef = reinterpret_cast<float*>(sm + P.off_coef);  // [128][KC]
+  float* coef = reinterpret_cast<float*>(sm + P.off_coef);  // [128][KC] (coefficients given by ids / w)
+  float* lg = reinterpret_cast<float*>(sm + P.off_lg);      // router: [K][128 + 1] logits, in the ring
   volatile int32_t* abort = &ctrl->abort;
 
   if (warp == 5) {
@@ -272,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   if (warp < 4) {
     if (kRouter) {
-      for (int i = tid; i < kRouterHidden * K; i += kEpiThreads) w2s[i] = __bfloat162float(rio.W2[i]);
+      for (int i = tid; i < kRouterHidden * K; i += kEpiThreads) {
+        const int u = i / K, a = i - u * K;
+        w2T[a * kRouterHidden + u] = __bfloat162float(rio.W2[i]);
+      }
       if (tid < kRouterHidden) b1s[tid] = rio.b1 ? rio.b1[tid] : 0.f;
       for (int i = tid; i < K; i += kEpiThreads) b2s[i] = rio.b2 ? rio.b2[i] : 0.f;
     } else {
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     have = __all_sync(0xffffffffu, mbar_wait_or_abort(&ctrl->mma_done, 0, abort) && !*abort);
     tc_fence_after();
     if (kRouter) {
-      // this CTA's hidden units, ReLU(x W1 + b1), held in registers until the ring is free
+      // this CTA's sums x W1 for its hidden units, held in registers until the ring is free
 #pragma unroll
       for (int c0 = 0; c0 < kRouterHidden; c0 += 16) {
         if (c0 < NH) {
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) hid_own[c0 + i] = fmaxf(v[i] + b1s[crank * NH + c0 + i], 0.f);
+          for (int i = 0; i < 16; ++i) hid_own[c0 + i] = v[i];
         }
       }
     }
@@ -425,78 +432,153 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < 4) {
     if (kRouter) {
-      // the router's second stage for this row, in the same order in every CTA of the tile:
-      // logit[a] = b2[a] + sum over u = 0..63 of hidden[u] W2[u,a]; top k by logit (strictly
-      // greater wins, so equal logits keep the lower index); softmax over the k, shifted by
-      // the largest.  The logits are parked in the (now idle) stage ring.
-      float* lg = reinterpret_cast<float*>(sm + P.off_lg) + (size_t)row * K;
-      float hid[kRouterHidden];
+      // the router's second stage for this row, identical in every CTA of the tile so all agree
+      // on ids and weights: hidden = ReLU(sum + b1); each logit is 8 group partials (an fmaf
+      // chain over the group's 8 hidden units, chains independent) added in group order, then
+      // b2; top k by logit (strictly greater wins, so equal logits keep the lower index);
+      // softmax over the k, shifted by the largest.  The logits are kept transposed,
+      // lgT[a][row], so a warp's accesses fall in distinct banks.  CTA 0 stores logits, ids
+      // and w; every CTA keeps the coefficients of its own adapters.
+      float* lgT = lg;  // [K][kRows + 1], used when K > 16
+      float h[kRouterHidden];
 #pragma unroll
       for (int i = 0; i < kRouterHidden / 4; ++i) {
         const float4 v = reinterpret_cast<const float4*>(recv + (size_t)row * kHidStride)[i];
-        hid[4 * i] = v.x, hid[4 * i + 1] = v.y, hid[4 * i + 2] = v.z, hid[4 * i + 3] = v.w;
+        h[4 * i] = fmaxf(v.x + b1s[4 * i], 0.f);
+        h[4 * i + 1] = fmaxf(v.y + b1s[4 * i + 1], 0.f);
+        h[4 * i + 2] = fmaxf(v.z + b1s[4 * i + 2], 0.f);
+        h[4 * i + 3] = fmaxf(v.w + b1s[4 * i + 3], 0.f);
       }
-      for (int a = 0; a < K; ++a) {
-        float s = 0.f;
+      auto logit = [&](int a) {  // 8 independent group chains, added in group order, then b2
+        const float4* wr = reinterpret_cast<const float4*>(w2T + a * kRouterHidden);
+        float p8[8];
 #pragma unroll
-        for (int u = 0; u < kRouterHidden; ++u) s = fmaf(hid[u], w2s[u * K + a], s);
-        lg[a] = s + b2s[a];
-      }
+        for (int g = 0; g < 8; ++g) {
+          const float4 w0 = wr[2 * g], w1 = wr[2 * g + 1];
+          float sg = 0.f;
+          sg = fmaf(h[g * 8 + 0], w0.x, sg);
+          sg = fmaf(h[g * 8 + 1], w0.y, sg);
+          sg = fmaf(h[g * 8 + 2], w0.z, sg);
+          sg = fmaf(h[g * 8 + 3], w0.w, sg);
+          sg = fmaf(h[g * 8 + 4], w1.x, sg);
+          sg = fmaf(h[g * 8 + 5], w1.y, sg);
+          sg = fmaf(h[g * 8 + 6], w1.z, sg);
+          sg = fmaf(h[g * 8 + 7], w1.w, sg);
+          p8[g] = sg;
+        }
+        float acc = p8[0];
+#pragma unroll
+        for (int g = 1; g < 8; ++g) acc += p8[g];
+        return acc + b2s[a];
+      };
       for (int j = 0; j < KC; ++j) coef[row * KC + j] = 0.f;
       const bool writer = crank == 0 && t < N && have;
-      if (writer && rio.logits)
-        for (int a = 0; a < K; ++a) rio.logits[t * K + a] = lg[a];
-      float m = 0.f, denom = 0.f;
-      for (int pass = 0; pass < 2; ++pass) {
-        const float inv = pass ? 1.f / denom : 0.f;
-        uint64_t used = 0;
-        for (int js = 0; js < k; ++js) {
-          int best = -1;
-          for (int a = 0; a < K; ++a)
-            if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
-          used |= 1ull << best;
-          if (js == 0) m = lg[best];
-          const float e = expf(lg[best] - m);
-          if (pass == 0) {
-            denom += e;
-          } else {
-            const float wj = e * inv;
-            if (writer) {
-              rio.ids[t * k + js] = best;
-              rio.w[t * k + js] = wj;
+      // top k by logit (strictly greater wins, so equal logits keep the lower index), softmax
+      // over the k shifted by the largest; run twice (denominator, then weights)
+      auto select = [&](auto get) {
+        float m = 0.f, denom = 0.f;
+        for (int pass = 0; pass < 2; ++pass) {
+          const float inv = pass ? 1.f / denom : 0.f;
+          uint64_t used = 0;
+          for (int js = 0; js < k; ++js) {
+            int best = -1;
+            float bl = 0.f;
+            get(used, best, bl);
+            used |= 1ull << best;
+            if (js == 0) m = bl;
+            const float e = expf(bl - m);
+            if (pass == 0) {
+              denom += e;
+            } else {
+              const float wj = e * inv;
+              if (writer) {
+                rio.ids[t * k + js] = best;
+                rio.w[t * k + js] = wj;
+              }
+              if (best >= a0 && best < a0 + KC) coef[row * KC + (best - a0)] = wj;
             }
-            if (best >= a0 && best < a0 + KC) coef[row * KC + (best - a0)] = wj;
           }
         }
+      };
+      if (K <= 16) {  // the row's logits stay in registers
+        float lr[16];
+#pragma unroll
+        for (int a = 0; a < 16; ++a) lr[a] = a < K ? logit(a) : 0.f;
+        if (writer && rio.logits)
+#pragma unroll
+          for (int a = 0; a < 16; ++a)
+            if (a < K) rio.logits[t * K + a] = lr[a];
+        select([&](uint64_t used, int& best, float& bl) {
+#pragma unroll
+          for (int a = 0; a < 16; ++a)
+            if (a < K && !((used >> a) & 1ull) && (best < 0 || lr[a] > bl)) best = a, bl = lr[a];
+        });
+      } else {  // kept transposed in shared memory, one column per row: distinct banks
+        for (int a = 0; a < K; ++a) lgT[a * (kRows + 1) + row] = logit(a);
+        if (writer && rio.logits)
+          for (int a = 0; a < K; ++a) rio.logits[t * K + a] = lgT[a * (kRows + 1) + row];
+        select([&](uint64_t used, int& best, float& bl) {
+          for (int a = 0; a < K; ++a) {
+            const float la = lgT[a * (kRows + 1) + row];
+            if (!((used >> a) & 1ull) && (best < 0 || la > bl)) best = a, bl = la;
+          }
+        });
       }
     }
-    // G = scale * c[t,a] * (x A_a), split into bf16 hi + lo, to the workspace rows.  Every lane
-    // of the warp loads TMEM (a warp-collective instruction); rows past N store nothing.
+    // G = scale * c[t,a] * (x A_a), split into bf16 hi + lo, to the workspace rows, 64
+    // columns at a time: each lane (a row) forms its values from TMEM into a swizzled staging
+    // box [32 rows x 128 B] per term, then the warp writes them back row-wise, eight lanes to a
+    // 128-byte row piece, so every store instruction covers four whole row pieces.  Every lane
+    // loads TMEM (a warp-collective instruction); rows past N store nothing.
     if (have) {
-      for (int j = 0; j < KC; ++j) {
-        const float cf = scale * coef[row * KC + j];
-        const int64_t base = t * KR + (int64_t)(a0 + j) * r;
-        for (int c0 = 0; c0 < r; c0 += 16) {
-          float v[16];
-          tmem_ld16(lane_base + (uint32_t)(j * r + c0), v);
-          if (t >= N) continue;
+      uint8_t* gst_hi = sm + P.off_gst + (size_t)warp * 2 * 4096;
+      uint8_t* gst_lo = gst_hi + 4096;
+      const int sub = lane >> 3, q = lane & 7;
+      for (int c64 = 0; c64 < NA; c64 += 64) {
+        const int wc = min(64, NA - c64);
+        // both 32-column loads in flight, one wait (columns read past NA stay inside the
+        // allocation, a power of two >= NA + the router's columns, and are not used)
+        uint32_t ra[32], rb[32];
+        tmem_ld32_start(lane_base + (uint32_t)c64, ra);
+        if (wc > 32) tmem_ld32_start(lane_base + (uint32_t)(c64 + 32), rb);
+        tmem_ld_wait(ra);
+        tmem_ld_bind(rb);
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const int c16 = pc * 16;
+          if (c16 >= wc) continue;
+          const int j = (c64 + c16) / r;  // a 16-column piece never straddles two adapters (r >= 16)
+          const float cf = scale * coef[row * KC + j];
           uint32_t hi[8], lo[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float g0 = cf * v[2 * i], g1 = cf * v[2 * i + 1];
+            const uint32_t u0 = pc < 2 ? ra[(pc & 1) * 16 + 2 * i] : rb[(pc & 1) * 16 + 2 * i];
+            const uint32_t u1 = pc < 2 ? ra[(pc & 1) * 16 + 2 * i + 1] : rb[(pc & 1) * 16 + 2 * i + 1];
+            const float g0 = cf * __uint_as_float(u0), g1 = cf * __uint_as_float(u1);
             const __nv_bfloat16 h0 = __float2bfloat16_rn(g0), h1 = __float2bfloat16_rn(g1);
             const __nv_bfloat16 l0 = __float2bfloat16_rn(g0 - __bfloat162float(h0));
             const __nv_bfloat16 l1 = __float2bfloat16_rn(g1 - __bfloat162float(h1));
             hi[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
             lo[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
           }
-          uint4* dh = reinterpret_cast<uint4*>(g_hi + base + c0);
-          uint4* dl = reinterpret_cast<uint4*>(g_lo + base + c0);
-          dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-          dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+          const uint32_t cc = (uint32_t)c16 / 8u;  // 16-byte chunk of the 128-byte staging row
+          *reinterpret_cast<uint4*>(gst_hi + sw128_offset((uint32_t)lane, cc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(gst_hi + sw128_offset((uint32_t)lane, cc + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          *reinterpret_cast<uint4*>(gst_lo + sw128_offset((uint32_t)lane, cc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(gst_lo + sw128_offset((uint32_t)lane, cc + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = it * 4 + sub;
+          const int64_t t_rr = t0 + warp * 32 + rr;
+          if (q * 8 < wc && t_rr < N) {
+            const int64_t off = t_rr * KR + (int64_t)a0 * r + c64 + q * 8;
+            *reinterpret_cast<uint4*>(g_hi + off) = *reinterpret_cast<const uint4*>(gst_hi + sw128_offset((uint32_t)rr, (uint32_t)q));
+            *reinterpret_cast<uint4*>(g_lo + off) = *reinterpret_cast<const uint4*>(gst_lo + sw128_offset((uint32_t)rr, (uint32_t)q));
+          }
+        }
+        __syncwarp();
       }
     }
     tc_fence_before();
@@ -655,20 +737,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int32_t m0 = (int32_t)((tile / n_tiles) * kRows) + warp * 32;
       const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
-      for (int c = 0; c < BN / 32; ++c) {
-        // boxes that start past the last row or column hold nothing of y: skipped outright
-        // (warp-uniform), so that the staging buffers are taken strictly in turn by issued
-        // reductions and the wait below always covers the buffer about to be rewritten
-        if (m0 >= N || n0 + c * 32 >= d_out) continue;
-        float v[32];
-        tmem_ld32(lane_base + (uint32_t)(buf * BN + c * 32), v);
+      // boxes that start past the last row or column hold nothing of y: skipped outright
+      // (warp-uniform), so that the staging buffers are taken strictly in turn by issued
+      // reductions and the wait below always covers the buffer about to be rewritten
+      const int cmax = m0 < N ? min(BN / 32, (d_out - n0 + 31) / 32) : 0;
+      auto emit = [&](const uint32_t(&v)[32], int c) {
         uint8_t* box = stg + (size_t)sb * 4096;
         if (lane == 0) bulk_wait_read_upto(nstg - 1);  // the reduction last issued from this buffer has read it
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(box + sw128_offset((uint32_t)lane, (uint32_t)i)) =
-              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          *reinterpret_cast<uint4*>(box + sw128_offset((uint32_t)lane, (uint32_t)i)) =
+              make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -676,6 +756,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit();
         }
         sb = sb + 1 == nstg ? 0 : sb + 1;
+      };
+      // TMEM loads one chunk ahead: the next 32 columns are in flight while this chunk is
+      // staged and handed to the TMA unit
+      const uint32_t cbase = lane_base + (uint32_t)(buf * BN);
+      uint32_t va[32], vb[32];
+      if (cmax > 0) tmem_ld32_start(cbase, va);
+      for (int c = 0; c < cmax; c += 2) {
+        tmem_ld_wait(va);
+        if (c + 1 < cmax) tmem_ld32_start(cbase + (uint32_t)((c + 1) * 32), vb);
+        emit(va, c);
+        if (c + 1 < cmax) {
+          tmem_ld_wait(vb);
+          if (c + 2 < cmax) tmem_ld32_start(cbase + (uint32_t)((c + 2) * 32), va);
+          emit(vb, c + 1);
+        }
       }
       tc_fence_before();
       mbar_arrive(&ctrl->tempty[buf]);
