@@ -738,7 +738,12 @@ def check_dispatch_of(ids, K, counts, offsets, perm):
                                        ("topk_mlp", {"N": 129, "d_in": 192}, 2),
                                        # K > 8: the router's general second stage
                                        ("topk_mlp", {"N": 300, "K": 16}, 3),
-                                       ("topk_mlp", {"N": 200, "d_in": 1024, "K": 64}, 2)])
+                                       ("topk_mlp", {"N": 200, "d_in": 1024, "K": 64}, 2),
+                                       # the cluster narrows as the tiles grow (one wave of CTAs
+                                       # on 152 SMs): 4, 2 and 1 CTAs per tile, ragged last tile
+                                       ("topk_scaling", {"N": 8192}, 2),
+                                       ("topk_scaling", {"N": 12001, "d_in": 1024}, 3),
+                                       ("topk_mlp", {"N": 40007, "d_in": 512, "d_out": 256, "K": 16}, 2)])
 def test_router_topk_vs_oracle(m, name, kw, k):
     wl = workloads.make(name, k=k, **kw)
     logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(wl.W2), k)

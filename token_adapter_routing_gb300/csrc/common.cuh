@@ -215,6 +215,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t rem
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
                : "memory");
 }
+// `bytes` (a multiple of 16) from this CTA's shared memory to CTA-cluster shared memory (a
+// dsmem_addr address, 16-byte aligned), counted on the mbarrier at `remote_bar` (a cluster address).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(remote_bar)
+               : "memory");
+}
 // Named barrier over `count` threads (a multiple of 32) of this CTA; threads of one warp
 // may arrive separately (non-.aligned form).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
@@ -371,85 +378,159 @@ __device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uin
   return row * row_bytes + ((chunk ^ f) << 4);
 }
 
-// The learned router's second stage (Table 1's 64d + 64K routing cost; Figure 2's top-k
-// weighted sum) for `rows` token rows whose 64 hidden-unit partial sums from C CTAs sit in
-// shared memory at recv[(cc * rows + rl) * stride + col0 + u]:
-//   hidden = ReLU(sum over cc in rank order + b1);  the hidden units form 8 groups of 8, each
-//   group's partial logit is an fmaf chain over its units, and the 8 group partials are added
-//   in group order, then b2;  top k by logit (strictly greater wins, so equal logits keep the
-//   lower index);  softmax renormalised over the k, shifted by the largest.
-// Called by `nthreads` threads (a multiple of 32, thread ids 0..nthreads-1): the 8 consecutive
-// lanes of a row each take a group and the row's first lane gathers the group partials by
-// shuffles into lg_s[rl * K + a] (shared scratch), then selects and writes logits (if
-// non-null), ids and w for token t_first + rl when it is below N, `ok` and `store`.  With
-// `coef` non-null it also stores each row's per-adapter weight (w_j for a selected adapter,
-// else 0) at coef[rl * K + a] (whether or not `store`).  The selection runs twice (denominator,
-// then weights), so nothing is read back from global memory; the code is kept compact because
-// it runs once per tile.
-__device__ __forceinline__ void router_rows(const float* recv, int C, int rows, int stride, int col0,
-                                            const float* w2s, const float* b1s, const float* b2s, int K, int k,
-                                            int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
-                                            float* w, float* lg_s, float* coef, int tid, int nthreads,
-                                            bool store = true) {
-  const int lane = tid & 31;
-  for (int base = 0; base < rows * 8; base += nthreads) {
+// The learned router's second stage (Table 1's O(64K) part; Table 10's softmax gating; Figure
+// 2's top-k) for `rows` consecutive tokens starting at t_first, eight lanes per token (nthreads a
+// multiple of 32).  recv holds C partial hidden vectors per token, source-major: source cc, row
+// rl at recv + (cc * rows + rl) * stride + col0, 64 floats; with `swz` its 16-byte chunks are
+// stored at chunk ^ (rl & 7) (the layout a conflict-free staging store leaves).
+//   hidden  h = ReLU(sum over sources in rank order + b1); lane g of a token sums units 8g..8g+7
+//           and hands them to the token's other lanes by shuffles;
+//   logits  lane g owns logits a = g + 8j (j < JL = ceil(K / 8)); each is eight group partials
+//           (an fmaf chain over the group's 8 units, from 0) added in group order, then b2;
+//   top k   k rounds of an 8-lane butterfly on (logit, index): larger logit wins, equal logits
+//           keep the lower index (the result of a sequential strictly-greater scan);
+//   softmax over the k, shifted by the largest: e_j = exp(l_j - l_0), denominator summed in
+//           selection order, w_j = e_j * (1 / denominator).
+// The arithmetic, and so every bit of the results, does not depend on the lane mapping.
+// Stores logits (if non-null and `store`), ids and w for tokens t < N when `ok`; writes the
+// token's coefficients coef[rl * K + a] (0 for unselected adapters) when coef is non-null.
+// JL is a template parameter so that no lane issues work for logits it does not own.
+template <int JL>
+__device__ __forceinline__ void router_rows_jl(const float* recv, int C, int rows, int stride, int col0, bool swz,
+                                               const float* w2s, const float* b1s, const float* b2s, int K, int k,
+                                               int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
+                                               float* w, float* coef, int tid, int nthreads, bool store) {
+  const int lane = tid & 31, g = lane & 7, gbase = lane & ~7;
+  for (int base = 0; base < rows * 8; base += nthreads) {  // warp-uniform trip count
     const int item = base + tid;
-    const int rl = item >> 3, g = item & 7;
+    const int rl = item >> 3;
     const bool valid = item < rows * 8;
-    const bool lead = valid && g == 0;
-    float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float hg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (valid) {
+      const int c0 = swz ? (2 * g) ^ (rl & 7) : 2 * g, c1 = swz ? (2 * g + 1) ^ (rl & 7) : 2 * g + 1;
       for (int cc = 0; cc < C; ++cc) {
-        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * rows + rl) * stride + col0 + g * 8);
-        const float4 p0 = src[0], p1 = src[1];
-        h[0] += p0.x, h[1] += p0.y, h[2] += p0.z, h[3] += p0.w;
-        h[4] += p1.x, h[5] += p1.y, h[6] += p1.z, h[7] += p1.w;
+        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * rows + rl) * stride + col0);
+        const float4 p0 = src[c0], p1 = src[c1];
+        hg[0] += p0.x, hg[1] += p0.y, hg[2] += p0.z, hg[3] += p0.w;
+        hg[4] += p1.x, hg[5] += p1.y, hg[6] += p1.z, hg[7] += p1.w;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = fmaxf(h[i] + b1s[g * 8 + i], 0.f);
+      for (int i = 0; i < 8; ++i) hg[i] = fmaxf(hg[i] + b1s[g * 8 + i], 0.f);
     }
-    for (int a = 0; a < K; ++a) {
-      float s = 0.f;
+    // logits g + 8j: group gg's units come from lane gg of the token (8 shuffles), then each
+    // logit's chain over them is added to its running sum (group order)
+    bool own[JL];
+    float lv[JL];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s = fmaf(h[i], w2s[(g * 8 + i) * K + a], s);
-      float acc = s;  // group 0's partial, then groups 1..7 in order (used by the row's first lane)
-      for (int gg = 1; gg < 8; ++gg) acc += __shfl_sync(0xffffffffu, s, (lane & ~7) + gg);
-      if (lead) lg_s[rl * K + a] = acc + b2s[a];
+    for (int j = 0; j < JL; ++j) own[j] = valid && g + 8 * j < K, lv[j] = 0.f;
+#pragma unroll(JL <= 2 ? 4 : 1)
+    for (int gg = 0; gg < 8; ++gg) {
+      float hc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hc[i] = __shfl_sync(0xffffffffu, hg[i], gbase | gg);
+#pragma unroll
+      for (int j = 0; j < JL; ++j) {
+        if (own[j]) {
+          const float* wc = w2s + (gg * 8) * K + g + 8 * j;
+          float sg = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sg = fmaf(hc[i], wc[i * K], sg);
+          lv[j] = gg == 0 ? sg : lv[j] + sg;
+        }
+      }
     }
-    if (lead) {
-      const int64_t t = t_first + rl;
-      const float* lg = lg_s + rl * K;
-      if (coef)
-        for (int a = 0; a < K; ++a) coef[rl * K + a] = 0.f;
-      if (t < N && ok) {
-        if (logits && store)
-          for (int a = 0; a < K; ++a) logits[t * K + a] = lg[a];
-        float m = 0.f, denom = 0.f;
-        for (int pass = 0; pass < 2; ++pass) {
-          const float inv = pass ? 1.f / denom : 0.f;
-          uint64_t used = 0;
-          for (int js = 0; js < k; ++js) {
-            int best = -1;
-            for (int a = 0; a < K; ++a)
-              if (!((used >> a) & 1ull) && (best < 0 || lg[a] > lg[best])) best = a;
-            used |= 1ull << best;
-            if (js == 0) m = lg[best];
-            const float e = expf(lg[best] - m);
-            if (pass == 0) {
-              denom += e;
-            } else {
-              const float wj = e * inv;
-              if (store) {
-                ids[t * k + js] = best;
-                w[t * k + js] = wj;
-              }
-              if (coef) coef[rl * K + best] = wj;
+#pragma unroll
+    for (int j = 0; j < JL; ++j)
+      if (own[j]) lv[j] += b2s[g + 8 * j];
+    const int64_t t = t_first + rl;
+    const bool out = valid && t < N && ok;
+    if (coef)
+#pragma unroll
+      for (int j = 0; j < JL; ++j)
+        if (own[j]) coef[rl * K + g + 8 * j] = 0.f;
+    if (out && logits && store)
+#pragma unroll
+      for (int j = 0; j < JL; ++j)
+        if (own[j]) logits[t * K + g + 8 * j] = lv[j];
+    __syncwarp();  // the zeroed coefficients before the selected ones
+    // One selection round: the best unselected logit of the token, known to all 8 lanes.
+    uint32_t used = 0;  // bit j: logit g + 8j already selected
+    auto select = [&](float& bv, int& bi) {
+      bv = 0.f, bi = -1;
+#pragma unroll
+      for (int j = 0; j < JL; ++j)
+        if (own[j] && !((used >> j) & 1u) && (bi < 0 || lv[j] > bv)) bv = lv[j], bi = g + 8 * j;
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) bv = ov, bi = oi;
+      }
+      if (bi >= 0 && (bi & 7) == g) used |= 1u << (bi >> 3);
+    };
+    float m = 0.f, denom = 0.f;
+    if (k <= 8) {  // lane g keeps slot g: one selection pass
+      float my_e = 0.f;
+      int my_i = 0;
+      for (int js = 0; js < k; ++js) {
+        float bv;
+        int bi;
+        select(bv, bi);
+        if (js == 0) m = bv;
+        const float e = expf(bv - m);
+        denom += e;
+        if (js == g) my_e = e, my_i = bi;
+      }
+      if (out && g < k) {
+        const float wj = my_e * (1.f / denom);
+        if (store) {
+          ids[t * k + g] = my_i;
+          w[t * k + g] = wj;
+        }
+        if (coef) coef[rl * K + my_i] = wj;
+      }
+    } else {  // the selection runs twice (denominator, then weights)
+      for (int pass = 0; pass < 2; ++pass) {
+        const float inv = pass ? 1.f / denom : 0.f;
+        used = 0;
+        for (int js = 0; js < k; ++js) {
+          float bv;
+          int bi;
+          select(bv, bi);
+          if (js == 0) m = bv;
+          const float e = expf(bv - m);
+          if (pass == 0) {
+            denom += e;
+          } else if (out && g == (js & 7)) {
+            const float wj = e * inv;
+            if (store) {
+              ids[t * k + js] = bi;
+              w[t * k + js] = wj;
             }
+            if (coef) coef[rl * K + bi] = wj;
           }
         }
       }
     }
   }
+}
+
+__device__ __forceinline__ void router_rows(const float* recv, int C, int rows, int stride, int col0, bool swz,
+                                            const float* w2s, const float* b1s, const float* b2s, int K, int k,
+                                            int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
+                                            float* w, float* coef, int tid, int nthreads, bool store = true) {
+  if (K <= 8)
+    router_rows_jl<1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
+                      tid, nthreads, store);
+  else if (K <= 16)
+    router_rows_jl<2>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
+                      tid, nthreads, store);
+  else if (K <= 32)
+    router_rows_jl<4>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
+                      tid, nthreads, store);
+  else
+    router_rows_jl<8>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
+                      tid, nthreads, store);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

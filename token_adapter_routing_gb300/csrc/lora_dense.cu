@@ -73,10 +73,10 @@ struct DensePlan {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Per-CTA scratch (fp32): the router's W2 [64 x K], b1 [64], b2 [8] and logits [RPC][K]
-// (router variant only), and the owner rows' adapter coefficients [RPC][K].
+// Per-CTA scratch (fp32): the router's W2 [64 x K], b1 [64] and b2 [8] (router variant only),
+// and the owner rows' adapter coefficients [RPC][K].
 inline size_t router_scratch_bytes(int K, int RPC) {
-  return sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + 8 + 2 * (size_t)RPC * K);
+  return sizeof(float) * ((size_t)kRouterHidden * K + kRouterHidden + 8 + (size_t)RPC * K);
 }
 
 // Shared memory: phase 1 holds one round's x tile [KSR/64 blocks][64 rows][128 B] (plus room
@@ -198,12 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* recv = reinterpret_cast<float*>(sm + P.off_s);  // [C sources][64/C rows][PC], before the epilogue
   const uint32_t stage_stride = (uint32_t)kPiece * 4u + 16u;
   const int RPC = kTileRows / C;
-  // router scratch: W2 and the biases as fp32, partial logits, per-row adapter coefficients
+  // router scratch: W2 and the biases as fp32, per-row adapter coefficients
   float* w2s = reinterpret_cast<float*>(sm + P.off_rt);
   float* b1s = w2s + kRouterHidden * K;
   float* b2s = b1s + kRouterHidden;
-  float* lg_s = b2s + 8;          // [RPC][K] logits
-  float* coef_s = lg_s + RPC * K;  // [RPC][K]
+  float* coef_s = b2s + 8;  // [RPC][K]
 
   if (warp == 4) {
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -399,8 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kRouter) {
       // the learned router for the owner's rows: hidden units from the C partials,
       // logits, top k and softmax; logits, ids and w go out, the coefficients to scratch
-      router_rows(recv, C, RPC, PC, KR, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have_h, rio.logits,
-                  rio.ids, rio.w, lg_s, coef_s, tid, kEpilogueThreads);
+      // (the plan takes K*r of 64 or 128 with r >= 16, so K <= 8: one logit per lane)
+      router_rows_jl<1>(recv, C, RPC, PC, KR, false, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have_h,
+                        rio.logits, rio.ids, rio.w, coef_s, tid, kEpilogueThreads, true);
       named_barrier(2, kEpilogueThreads);  // coefficients ready
     }
     // owner: rows [crank*RPC, (crank+1)*RPC) of the tile; each item is 8 columns of one row
