@@ -65,7 +65,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "topk", "router", "perseq", "skew",
-                                      "bf16y", "indirect", "split", "kernels"],
+                                      "bf16y", "indirect", "split", "kernels", "tiling"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
@@ -602,11 +602,21 @@ def run_mode(args):
     split      Table 6: per-token routing against per-sequence routing that must split the batch
                into its single-modality runs (one masked pass per run), on the 4-modality shape
                with interleaved text-heavy (70/10/10/10) and balanced runs, and separated (one
-               contiguous block per modality); one CUDA graph each, L2 flushed between replays."""
+               contiguous block per modality); one CUDA graph each, L2 flushed between replays.
+    tiling     Table 9's fixed vs adaptive tiles for the grouped apply: the plan the library
+               chooses (adaptive: tile rows and cluster size from the slot and adapter counts)
+               against fixed 64-row and fixed 128-row tiles in clusters of 8, and the scalar
+               path, on the 4-modality workload under the three skews and on the decode sweep
+               (K = 8..64, 256..2048 tokens, uniform and Zipf draws); the whole step (routing +
+               dispatch + apply), 50 steps back to back in one graph, median of 5.  Runs the
+               tuning build (build(tuning=True)), whose plan can be forced by environment."""
     import token_adapter_routing_gb300 as m
     from token_adapter_routing_gb300 import build as lib_build
-    lib_build.build()
-    m.load_library()
+    if args.mode == "tiling":
+        m.load_library(lib_build.build(tuning=True))
+    else:
+        lib_build.build()
+        m.load_library()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -732,6 +742,67 @@ def run_mode(args):
                   "algorithmic_bytes": algo, "apply_GBps": round(algo / (us * 1e-6) / 1e9, 1),
                   "frac_of_measured": round(algo / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                   "l2": f"inputs larger than L2 ({N_BATCHES} resident batches, back to back)"})
+    elif args.mode == "tiling":
+        def loop_us(fn, n=50, reps=5):
+            with torch.cuda.stream(stream):
+                fn()
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(n):
+                        fn()
+                g.replay()
+                stream.synchronize()
+                ts = []
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3 / n)
+            return statistics.median(ts)
+
+        def force(C=None, TM=None):
+            for key in ("MOLORA_CLUSTER", "MOLORA_TILE_ROWS", "MOLORA_ONE_PER_SM"):
+                os.environ.pop(key, None)
+            if C:
+                os.environ["MOLORA_CLUSTER"] = str(C)
+            if TM:
+                os.environ["MOLORA_TILE_ROWS"] = str(TM)
+
+        cases = [(WORKLOAD, {"dist": d}) for d in ("uniform", "80-10-5-5", "95-2-2-1")]
+        cases += [("decode_sweep", {"N": b, "K": K}) for K in (8, 16, 32, 64) for b in (256, 512, 1024, 2048)]
+        cases += [("decode_sweep", {"N": b, "K": K, "dist": "zipf"}) for K in (32, 64) for b in (512, 2048)]
+        for name, kw in cases:
+            wl = workloads.make(name, **kw)
+            tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+            x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+            adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+            counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+            offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+
+            def step():
+                m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
+                m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm,
+                                    path="grouped")
+
+            def scalar_step():
+                m.molora_route_vocab(tok, starts, adapter=adapter)
+                m.molora_lora_apply(x, A, B, adapter, y, wl.scale, path="scalar")
+
+            res = {"mode": "tiling", "workload": name, "N": wl.N, "K": wl.K, "dist": kw.get("dist", "uniform"),
+                   "unit": "us per step"}
+            force()
+            res["scalar"] = round(loop_us(scalar_step), 2)
+            res["adaptive"] = round(loop_us(step), 2)
+            force(8, 64)
+            res["fixed_64"] = round(loop_us(step), 2)
+            force(8, 128)
+            res["fixed_128"] = round(loop_us(step), 2)
+            force()
+            emit(res)
     elif args.mode == "skew":
         peaks, _ = measured_peaks()
         for dist in ("uniform", "80-10-5-5", "95-2-2-1"):

@@ -66,12 +66,15 @@ def library_path() -> str:
     return _build.LIB
 
 
-def load_library():
-    """Loads the compiled library (raises if it has not been built)."""
+def load_library(path=None):
+    """Loads the compiled library (raises if it has not been built).  ``path``: another build of
+    it (the tuning build of build.build(tuning=True)); only the first load in a process counts."""
     global _lib
     if _lib is not None:
+        if path is not None and os.path.realpath(path) != os.path.realpath(_lib._name):
+            raise RuntimeError(f"a different CUDA library ({_lib._name}) is already loaded")
         return _lib
-    path = library_path()
+    path = path or library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library {path} is missing: build it with token_adapter_routing_gb300.build.build()")
     lib = ctypes.CDLL(path)

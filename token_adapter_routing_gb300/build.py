@@ -3,6 +3,10 @@
 Each translation unit compiles in parallel; the shared library links the CUDA runtime
 statically and reaches the driver API (tensor-map encoding) through the runtime's
 entry-point query, so it needs no -lcuda.  The output stays inside the package directory.
+
+build(tuning=True) makes a second library (_build_tuning/libmolora_tuning.so) compiled with
+MOLORA_TUNING_ENV, whose kernels also read plan overrides from the environment (cluster size,
+tile rows, ring depths); bench.py's plan sweeps load it.  The product library never reads them.
 """
 
 from __future__ import annotations
@@ -18,6 +22,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmolora.so")
+BUILD_TUNING = os.path.join(PKG, "_build_tuning")
+LIB_TUNING = os.path.join(BUILD_TUNING, "libmolora_tuning.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden", "--expt-relaxed-constexpr",
@@ -40,22 +46,24 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), tuning: bool = False) -> str:
+    out_dir, lib = (BUILD_TUNING, LIB_TUNING) if tuning else (BUILD, LIB)
+    extra_flags = [*extra_flags, *(["-DMOLORA_TUNING_ENV"] if tuning else [])]
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(out_dir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -68,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
