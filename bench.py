@@ -959,7 +959,12 @@ def run_mode(args):
             if "router" in arms:
                 r_ms = _replay_ms(_graph(lambda: m.molora_router_topk(x, W1, W2, k, ids=ids, w=w, want_logits=False),
                                          stream), stream, min(args.replays, 200))
+                rb = wl.N * wl.d_in * 2 + wl.d_in * 64 * 2 + 64 * wl.K * 2 + wl.N * 2 * k * 4  # x, W1, W2, ids, w
                 res["router_alone_us_p50"] = round(_pct(r_ms, 0.5) * 1e3, 2)
+                res["router_alone_us_p99"] = round(_pct(r_ms, 0.99) * 1e3, 2)
+                res["router_alone_GBps_p50"] = round(rb / (_pct(r_ms, 0.5) * 1e-3) / 1e9, 1)
+                res["router_alone_frac_of_measured_hbm"] = (round(rb / (_pct(r_ms, 0.5) * 1e-3) / 1e9 / peak, 3)
+                                                            if peak else None)
             emit({"mode": "topk", "workload": "N=8192, d=4096, K=8, r=64, router d->64->K", "k": k,
                   "algorithmic_bytes": nbytes, **res,
                   "l2": "not flushed (back-to-back replays; 344 MB of inputs and outputs exceed the L2)"})
@@ -996,6 +1001,14 @@ def run_mode(args):
 
         r_ms = _replay_ms(g_router, stream, 100, flush)
         res = {}
+        # the router alone back to back (no flush), 200 replays
+        peak = measured_peaks()[0].get("hbm_gbs")
+        rb = wl.N * wl.d_in * 2 + wl.d_in * 64 * 2 + wl.N * (wl.K + 2 * wl.k) * 4
+        rms = _replay_ms(g_router, stream, 200)
+        res["b2b_router"] = {"p50_us": round(_pct(rms, 0.5) * 1e3, 2), "p99_us": round(_pct(rms, 0.99) * 1e3, 2),
+                             "GBps_p50": round(rb / (_pct(rms, 0.5) * 1e-3) / 1e9, 1),
+                             "frac_of_measured_hbm": (round(rb / (_pct(rms, 0.5) * 1e-3) / 1e9 / peak, 3)
+                                                      if peak else None)}
         for name, fn in (("grouped", path_grouped), ("dense", path_dense), ("fused", path_fused),
                          ("fused_stacked", path_stacked)):
             res[f"path_{name}_us_p50"] = round(_pct(_replay_ms(_graph(fn, stream), stream, 100, flush), 0.5) * 1e3, 2)
@@ -1003,7 +1016,6 @@ def run_mode(args):
         # measured HBM for x once, y read + written, A, B, W1, logits, ids and w
         nbytes = (wl.N * wl.d_in * 2 + 2 * wl.N * wl.d_out * 4 + wl.K * (wl.d_in * wl.r + wl.r * wl.d_out) * 2
                   + wl.d_in * 64 * 2 + wl.N * (wl.K + 2 * wl.k) * 4)
-        peak = measured_peaks()[0].get("hbm_gbs")
         for name, fn in (("fused", path_fused), ("fused_stacked", path_stacked)):
             ms = _replay_ms(_graph(fn, stream), stream, 200)
             p50, p99 = _pct(ms, 0.5), _pct(ms, 0.99)
