@@ -253,3 +253,14 @@ def test_binding_rejects_mis_sized_tensors_before_any_launch():
         m.molora_route_vocab(tok, starts, adapter=torch.zeros(N - 1, dtype=torch.int32))
     with pytest.raises(ValueError, match="adapter_of must"):
         m.molora_lora_apply_masked_pass(x, A, B, torch.zeros(N + 1, dtype=torch.int32), 0, y, 2.0)
+
+
+def test_launching_calls_run_on_the_tensors_device():
+    """Every launching binding runs with its tensors' device current (a device guard), so a
+    caller whose current device differs still launches where the data lives."""
+    import token_adapter_routing_gb300 as m
+    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+                 "molora_lora_apply", "molora_route_vocab_lora_apply", "molora_router_lora_apply",
+                 "molora_lora_apply_static_ws", "molora_lora_apply_masked_pass", "molora_selftest_bounded_wait"):
+        fn = getattr(m, name)
+        assert getattr(fn, "__wrapped__", None) is not None, f"{name} has no device guard"

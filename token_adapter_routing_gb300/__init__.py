@@ -17,6 +17,7 @@ grouping (Table 1, Figure 2), and the batched LoRA apply over a GPU-resident hot
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Optional
 
@@ -214,6 +215,22 @@ def _workspace(ws: Optional[torch.Tensor], device, call) -> int:
     return call(_p(ws), ctypes.byref(size))
 
 
+def _on_tensor_device(fn):
+    """Runs a launching call with the device of its first CUDA tensor argument current, so that
+    the library launches on the device that holds the tensors (and their stream), whichever
+    device the caller has current.  The call itself checks that all tensors share that device."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        for a in (*args, *kwargs.values()):
+            if isinstance(a, (list, tuple)) and a and isinstance(a[0], torch.Tensor):
+                a = a[0]
+            if isinstance(a, torch.Tensor) and a.is_cuda:
+                with torch.cuda.device(a.device):
+                    return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return call
+
+
 def molora_workspace_bytes(N, d_in, d_out, K, r, k, dtype=torch.bfloat16, path="auto", router=False) -> int:
     """Bytes of workspace molora_lora_apply (or, with router=True, molora_router_lora_apply)
     needs for these sizes (a query: nothing is launched).  Allocate them once, e.g. before
@@ -232,6 +249,7 @@ def molora_workspace_bytes(N, d_in, d_out, K, r, k, dtype=torch.bfloat16, path="
     return size.value
 
 
+@_on_tensor_device
 def molora_route_vocab(tok, starts, adapter=None, err_word=None, stream=None):
     """adapter[t] = a with starts[a] <= tok[t] < starts[a+1], else -1 (int32 [N])."""
     _need(adapter, "adapter", tok.numel())
@@ -247,6 +265,7 @@ def molora_route_vocab(tok, starts, adapter=None, err_word=None, stream=None):
     return adapter
 
 
+@_on_tensor_device
 def molora_router_topk(x, W1, W2, k, b1=None, b2=None, logits=None, ids=None, w=None, want_logits=True,
                        stream=None):
     """Learned router: returns (logits fp32 [N,K] or None, ids int32 [N,k], w fp32 [N,k])."""
@@ -282,6 +301,7 @@ def molora_router_topk(x, W1, W2, k, b1=None, b2=None, logits=None, ids=None, w=
     return logits, ids, w
 
 
+@_on_tensor_device
 def molora_dispatch(ids, K, counts=None, offsets=None, perm=None, err_word=None, stream=None):
     """Histogram, exclusive-scan offsets and stable slot permutation of ids [N] or [N, k]."""
     N = ids.shape[0]
@@ -305,6 +325,7 @@ def molora_dispatch(ids, K, counts=None, offsets=None, perm=None, err_word=None,
     return counts, offsets, perm
 
 
+@_on_tensor_device
 def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=None, perm=None, err_word=None,
                                 stream=None):
     """molora_route_vocab then molora_dispatch (k = 1) as one kernel: (adapter, counts, offsets, perm)."""
@@ -332,6 +353,7 @@ def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=
     return adapter, counts, offsets, perm
 
 
+@_on_tensor_device
 def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None, perm=None, err_word=None,
                       path="auto", ws=None, stream=None):
     """y[t] += scale * sum_j w[t,j] (x[t] A_{ids[t,j]}) B_{ids[t,j]}, in place on y (fp32, or bf16
@@ -410,6 +432,7 @@ def molora_lora_apply(x, A, B, ids, y, scale, w=None, counts=None, offsets=None,
     return y
 
 
+@_on_tensor_device
 def molora_route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter=None, counts=None, offsets=None,
                                   perm=None, err_word=None, stream=None):
     """The whole vocabulary-routed step in one call: routing, dispatch and the apply (k = 1).
@@ -453,6 +476,7 @@ def molora_route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter=None, 
     return adapter, counts, offsets, perm
 
 
+@_on_tensor_device
 def molora_router_lora_apply(x, W1, W2, A, B, k, y, scale, b1=None, b2=None, logits=None, ids=None, w=None,
                              want_logits=True, err_word=None, ws=None, use_ws=True, stream=None):
     """The learned router and the top-k apply with one pass over x: returns
@@ -512,6 +536,7 @@ def molora_router_lora_apply(x, W1, W2, A, B, k, y, scale, b1=None, b2=None, log
     return logits, ids, w
 
 
+@_on_tensor_device
 def molora_lora_apply_static_ws(x, A, B, ids, y, scale, w=None, err_word=None, stream=None):
     """The stacked apply for callers that cannot allocate device memory: the workspace is a
     fixed scratch buffer inside the library (STATIC_SCRATCH_BYTES; N*K*r up to 4M), shared by
@@ -542,6 +567,7 @@ def molora_lora_apply_static_ws(x, A, B, ids, y, scale, w=None, err_word=None, s
     return y
 
 
+@_on_tensor_device
 def molora_lora_apply_masked_pass(x, A, B, adapter_of, a, y, scale, err_word=None, path="auto", stream=None):
     """One per-sequence pass: y[t] += [adapter_of[t] == a] * scale * (x[t] A_a) B_a for every t."""
     if x.dim() != 2 or A.dim() != 3 or B.dim() != 3:
@@ -567,6 +593,7 @@ def molora_lora_apply_masked_pass(x, A, B, adapter_of, a, y, scale, err_word=Non
     return y
 
 
+@_on_tensor_device
 def molora_selftest_bounded_wait(err_word, limit_us=1000, stream=None):
     """Runs one CTA whose mbarrier wait can never complete; it must give up after limit_us and
     set DEV_WAIT_TIMEOUT in err_word (a device int32 tensor)."""
