@@ -215,6 +215,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t rem
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
                : "memory");
 }
+// `bytes` (a multiple of 16) from global memory (16-byte aligned) into this CTA's shared memory
+// (16-byte aligned), counted on the mbarrier `bar` of this CTA.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 // `bytes` (a multiple of 16) from this CTA's shared memory to CTA-cluster shared memory (a
 // dsmem_addr address, 16-byte aligned), counted on the mbarrier at `remote_bar` (a cluster address).
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t remote_bar) {

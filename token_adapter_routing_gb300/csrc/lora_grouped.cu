@@ -202,6 +202,7 @@ struct __align__(8) Ctrl {
   uint64_t bar_empty[2];  // epilogue drained a TMEM buffer
   uint64_t bar_recv;      // partial-h rows this CTA owns have arrived from every CTA
   uint64_t bar_g;         // all TM rows of g (hi and lo) have arrived from their owners
+  uint64_t bar_perm;      // the dispatch permutation, copied whole into the x buffers
   uint32_t tmem_base;
   int32_t abort;
   TileInfo tile;
@@ -257,6 +258,7 @@ __global__ void __maxnreg__(168)
       }
       mbar_init(&ctrl->bar_recv, 1);
       mbar_init(&ctrl->bar_g, 1);
+      mbar_init(&ctrl->bar_perm, 1);
       mbar_fence_init();
       // both receive the tile's TM rows x r values: fp32 partials, and g as two bf16 halves
       mbar_arrive_expect_tx(&ctrl->bar_recv, (uint32_t)P.TM * r * 4u);
@@ -282,6 +284,19 @@ __global__ void __maxnreg__(168)
   }
   pdl_wait();
   pdl_launch_dependents();
+  // The whole permutation (S slots) is copied into the x buffers, which stay idle until the
+  // gather, in parallel with the offsets: the tile's tokens then come from shared memory
+  // instead of a second dependent global load after the tile is decoded.
+  const int rounds = KS / P.XR;
+  const int nbuf = rounds > 1 ? 2 : 1;
+  const size_t blk_bytes = (size_t)TM * 128;          // one 64-column K-block of a buffer
+  const size_t buf_bytes = (size_t)(P.XR / kKBlock) * blk_bytes;
+  const bool perm_smem = mask_adapter < 0 && S > 0 && (S & 3) == 0 && S * 4 <= (int64_t)(nbuf * buf_bytes) &&
+                         (reinterpret_cast<uintptr_t>(perm) & 15) == 0;
+  if (perm_smem && warp == 4 && lane == 0) {
+    mbar_arrive_expect_tx(&ctrl->bar_perm, (uint32_t)(S * 4));
+    bulk_load_g2s(smem_u32(sm), perm, (uint32_t)(S * 4), &ctrl->bar_perm);
+  }
 
   // ---- which tile this cluster owns (identical in every CTA of the cluster)
   if (mask_adapter < 0)
@@ -322,6 +337,8 @@ __global__ void __maxnreg__(168)
   __syncthreads();
   const TileInfo tile = ctrl->tile;
   if (tile.adapter < 0) {  // the whole cluster idles: every CTA computed the same tile
+    // the permutation copy must land before the CTA leaves
+    if (perm_smem && warp == 4 && lane == 0) mbar_wait(&ctrl->bar_perm, 0);
     if (warp == 4) {
       tc_fence_after();
       tmem_dealloc(ctrl->tmem_base, P.tmem_cols);
@@ -346,6 +363,10 @@ __global__ void __maxnreg__(168)
     if (row < tile.nvalid) {
       if (mask_adapter >= 0) {
         tok = tile.row0 + row;
+      } else if (perm_smem) {
+        if (!mbar_wait(&ctrl->bar_perm, 0)) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+        slot = reinterpret_cast<const volatile int32_t*>(sm)[tile.group_off + tile.row0 + row];
+        if (slot >= 0 && slot < S) tok = slot / k;
       } else {
         slot = perm[tile.group_off + tile.row0 + row];
         if (slot >= 0 && slot < S) tok = slot / k;
@@ -361,10 +382,6 @@ __global__ void __maxnreg__(168)
 
   // ---- shrink: rounds of XR columns, each gathered, then consumed by XR/16 MMAs.  Rounds
   // alternate between two x buffers: round rd+1 is in flight while round rd is multiplied.
-  const int rounds = KS / P.XR;
-  const int nbuf = rounds > 1 ? 2 : 1;
-  const size_t blk_bytes = (size_t)TM * 128;          // one 64-column K-block of a buffer
-  const size_t buf_bytes = (size_t)(P.XR / kKBlock) * blk_bytes;
   const uint32_t idesc_shrink = idesc_bf16_f32(kTileM, r, false, true);
   if (warp == 4) {
     if (indirect) {
@@ -733,12 +750,14 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
     return cudaErrorNotSupported;
   s.prefetch_y = 1;
-  // DRAM idles for about 2 us while the tile is decoded; prefetching 40% of y (at most
-  // 16 MiB) fills that window and measured best on GB300 (4-modality workload, back-to-back
-  // steps: 0, 25, 33, 40, 50 and 60% tried).  The rest of y follows per row, late.
+  // DRAM idles for about 2 us while the tile is decoded; prefetching 60% of y (at most
+  // 24 MiB) fills that window and measured best on GB300 (4-modality workload, back-to-back
+  // steps, with the permutation read into shared memory: 0, 20, 40, 60 and 80% tried; 40%
+  // was best while the tile's tokens took a second dependent global load).  The rest of y
+  // follows per row, late.
   const uint64_t y_bytes = (uint64_t)N * d_out * (y_bf16 ? 2u : 4u);
-  const uint64_t early = y_bytes * 2u / 5u;
-  s.early_y = (early < (16ull << 20) ? early : (16ull << 20)) & ~uint64_t(15);
+  const uint64_t early = y_bytes * 3u / 5u;
+  s.early_y = (early < (24ull << 20) ? early : (24ull << 20)) & ~uint64_t(15);
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
   if (const char* e = getenv("MOLORA_EARLY_Y")) {
