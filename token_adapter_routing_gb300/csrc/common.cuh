@@ -402,119 +402,151 @@ __device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uin
 // Stores logits (if non-null and `store`), ids and w for tokens t < N when `ok`; writes the
 // token's coefficients coef[rl * K + a] (0 for unselected adapters) when coef is non-null.
 // JL is a template parameter so that no lane issues work for logits it does not own.
-template <int JL>
+template <int JL, int RPT>
 __device__ __forceinline__ void router_rows_jl(const float* recv, int C, int rows, int stride, int col0, bool swz,
                                                const float* w2s, const float* b1s, const float* b2s, int K, int k,
                                                int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
                                                float* w, float* coef, int tid, int nthreads, bool store) {
   const int lane = tid & 31, g = lane & 7, gbase = lane & ~7;
-  for (int base = 0; base < rows * 8; base += nthreads) {  // warp-uniform trip count
-    const int item = base + tid;
-    const int rl = item >> 3;
-    const bool valid = item < rows * 8;
-    float hg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (valid) {
-      const int c0 = swz ? (2 * g) ^ (rl & 7) : 2 * g, c1 = swz ? (2 * g + 1) ^ (rl & 7) : 2 * g + 1;
-      for (int cc = 0; cc < C; ++cc) {
-        const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * rows + rl) * stride + col0);
-        const float4 p0 = src[c0], p1 = src[c1];
-        hg[0] += p0.x, hg[1] += p0.y, hg[2] += p0.z, hg[3] += p0.w;
-        hg[4] += p1.x, hg[5] += p1.y, hg[6] += p1.z, hg[7] += p1.w;
-      }
+  // each thread carries RPT tokens at once (items tid, tid + nthreads, ...): independent chains
+  for (int base = 0; base < rows * 8; base += nthreads * RPT) {  // warp-uniform trip count
+    int rl[RPT];
+    bool valid[RPT];
+    float hg[RPT][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hg[i] = fmaxf(hg[i] + b1s[g * 8 + i], 0.f);
+    for (int q = 0; q < RPT; ++q) {
+      const int item = base + q * nthreads + tid;
+      rl[q] = item >> 3;
+      valid[q] = item < rows * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hg[q][i] = 0.f;
+      if (valid[q]) {
+        const int c0 = swz ? (2 * g) ^ (rl[q] & 7) : 2 * g, c1 = swz ? (2 * g + 1) ^ (rl[q] & 7) : 2 * g + 1;
+        for (int cc = 0; cc < C; ++cc) {
+          const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)cc * rows + rl[q]) * stride + col0);
+          const float4 p0 = src[c0], p1 = src[c1];
+          hg[q][0] += p0.x, hg[q][1] += p0.y, hg[q][2] += p0.z, hg[q][3] += p0.w;
+          hg[q][4] += p1.x, hg[q][5] += p1.y, hg[q][6] += p1.z, hg[q][7] += p1.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hg[q][i] = fmaxf(hg[q][i] + b1s[g * 8 + i], 0.f);
+      }
     }
     // logits g + 8j: group gg's units come from lane gg of the token (8 shuffles), then each
     // logit's chain over them is added to its running sum (group order)
-    bool own[JL];
-    float lv[JL];
+    bool own[RPT][JL];
+    float lv[RPT][JL];
 #pragma unroll
-    for (int j = 0; j < JL; ++j) own[j] = valid && g + 8 * j < K, lv[j] = 0.f;
+    for (int q = 0; q < RPT; ++q)
+#pragma unroll
+      for (int j = 0; j < JL; ++j) own[q][j] = valid[q] && g + 8 * j < K, lv[q][j] = 0.f;
 #pragma unroll(JL <= 2 ? 4 : 1)
     for (int gg = 0; gg < 8; ++gg) {
-      float hc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hc[i] = __shfl_sync(0xffffffffu, hg[i], gbase | gg);
+      for (int q = 0; q < RPT; ++q) {
+        float hc[8];
 #pragma unroll
-      for (int j = 0; j < JL; ++j) {
-        if (own[j]) {
-          const float* wc = w2s + (gg * 8) * K + g + 8 * j;
-          float sg = 0.f;
+        for (int i = 0; i < 8; ++i) hc[i] = __shfl_sync(0xffffffffu, hg[q][i], gbase | gg);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) sg = fmaf(hc[i], wc[i * K], sg);
-          lv[j] = gg == 0 ? sg : lv[j] + sg;
+        for (int j = 0; j < JL; ++j) {
+          if (own[q][j]) {
+            const float* wc = w2s + (gg * 8) * K + g + 8 * j;
+            float sg = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sg = fmaf(hc[i], wc[i * K], sg);
+            lv[q][j] = gg == 0 ? sg : lv[q][j] + sg;
+          }
         }
       }
     }
+    int64_t t[RPT];
+    bool out[RPT];
 #pragma unroll
-    for (int j = 0; j < JL; ++j)
-      if (own[j]) lv[j] += b2s[g + 8 * j];
-    const int64_t t = t_first + rl;
-    const bool out = valid && t < N && ok;
-    if (coef)
+    for (int q = 0; q < RPT; ++q) {
 #pragma unroll
       for (int j = 0; j < JL; ++j)
-        if (own[j]) coef[rl * K + g + 8 * j] = 0.f;
-    if (out && logits && store)
+        if (own[q][j]) lv[q][j] += b2s[g + 8 * j];
+      t[q] = t_first + rl[q];
+      out[q] = valid[q] && t[q] < N && ok;
+      if (coef)
 #pragma unroll
-      for (int j = 0; j < JL; ++j)
-        if (own[j]) logits[t * K + g + 8 * j] = lv[j];
+        for (int j = 0; j < JL; ++j)
+          if (own[q][j]) coef[rl[q] * K + g + 8 * j] = 0.f;
+      if (out[q] && logits && store)
+#pragma unroll
+        for (int j = 0; j < JL; ++j)
+          if (own[q][j]) logits[t[q] * K + g + 8 * j] = lv[q][j];
+    }
     __syncwarp();  // the zeroed coefficients before the selected ones
-    // One selection round: the best unselected logit of the token, known to all 8 lanes.
-    uint32_t used = 0;  // bit j: logit g + 8j already selected
-    auto select = [&](float& bv, int& bi) {
+    // One selection round for token q: its best unselected logit, known to all 8 lanes.
+    uint32_t used[RPT];  // bit j: logit g + 8j already selected
+    auto select = [&](int q, float& bv, int& bi) {
       bv = 0.f, bi = -1;
 #pragma unroll
       for (int j = 0; j < JL; ++j)
-        if (own[j] && !((used >> j) & 1u) && (bi < 0 || lv[j] > bv)) bv = lv[j], bi = g + 8 * j;
+        if (own[q][j] && !((used[q] >> j) & 1u) && (bi < 0 || lv[q][j] > bv)) bv = lv[q][j], bi = g + 8 * j;
 #pragma unroll
       for (int off = 1; off < 8; off <<= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
         if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) bv = ov, bi = oi;
       }
-      if (bi >= 0 && (bi & 7) == g) used |= 1u << (bi >> 3);
+      if (bi >= 0 && (bi & 7) == g) used[q] |= 1u << (bi >> 3);
     };
-    float m = 0.f, denom = 0.f;
+    float m[RPT], denom[RPT];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) m[q] = 0.f, denom[q] = 0.f, used[q] = 0;
     if (k <= 8) {  // lane g keeps slot g: one selection pass
-      float my_e = 0.f;
-      int my_i = 0;
+      float my_e[RPT];
+      int my_i[RPT];
+#pragma unroll
+      for (int q = 0; q < RPT; ++q) my_e[q] = 0.f, my_i[q] = 0;
       for (int js = 0; js < k; ++js) {
-        float bv;
-        int bi;
-        select(bv, bi);
-        if (js == 0) m = bv;
-        const float e = expf(bv - m);
-        denom += e;
-        if (js == g) my_e = e, my_i = bi;
-      }
-      if (out && g < k) {
-        const float wj = my_e * (1.f / denom);
-        if (store) {
-          ids[t * k + g] = my_i;
-          w[t * k + g] = wj;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+          float bv;
+          int bi;
+          select(q, bv, bi);
+          if (js == 0) m[q] = bv;
+          const float e = expf(bv - m[q]);
+          denom[q] += e;
+          if (js == g) my_e[q] = e, my_i[q] = bi;
         }
-        if (coef) coef[rl * K + my_i] = wj;
+      }
+#pragma unroll
+      for (int q = 0; q < RPT; ++q) {
+        if (out[q] && g < k) {
+          const float wj = my_e[q] * (1.f / denom[q]);
+          if (store) {
+            ids[t[q] * k + g] = my_i[q];
+            w[t[q] * k + g] = wj;
+          }
+          if (coef) coef[rl[q] * K + my_i[q]] = wj;
+        }
       }
     } else {  // the selection runs twice (denominator, then weights)
       for (int pass = 0; pass < 2; ++pass) {
-        const float inv = pass ? 1.f / denom : 0.f;
-        used = 0;
+        float inv[RPT];
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) inv[q] = pass ? 1.f / denom[q] : 0.f, used[q] = 0;
         for (int js = 0; js < k; ++js) {
-          float bv;
-          int bi;
-          select(bv, bi);
-          if (js == 0) m = bv;
-          const float e = expf(bv - m);
-          if (pass == 0) {
-            denom += e;
-          } else if (out && g == (js & 7)) {
-            const float wj = e * inv;
-            if (store) {
-              ids[t * k + js] = bi;
-              w[t * k + js] = wj;
+#pragma unroll
+          for (int q = 0; q < RPT; ++q) {
+            float bv;
+            int bi;
+            select(q, bv, bi);
+            if (js == 0) m[q] = bv;
+            const float e = expf(bv - m[q]);
+            if (pass == 0) {
+              denom[q] += e;
+            } else if (out[q] && g == (js & 7)) {
+              const float wj = e * inv[q];
+              if (store) {
+                ids[t[q] * k + js] = bi;
+                w[t[q] * k + js] = wj;
+              }
+              if (coef) coef[rl[q] * K + bi] = wj;
             }
-            if (coef) coef[rl * K + bi] = wj;
           }
         }
       }
@@ -522,22 +554,27 @@ __device__ __forceinline__ void router_rows_jl(const float* recv, int C, int row
   }
 }
 
+// Chooses the instantiation: logits per lane from K, and two tokens per thread when the rows
+// need more than one pass of the threads and K <= 8 (the registers allow it there).
 __device__ __forceinline__ void router_rows(const float* recv, int C, int rows, int stride, int col0, bool swz,
                                             const float* w2s, const float* b1s, const float* b2s, int K, int k,
                                             int64_t t_first, int64_t N, bool ok, float* logits, int32_t* ids,
                                             float* w, float* coef, int tid, int nthreads, bool store = true) {
-  if (K <= 8)
-    router_rows_jl<1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
-                      tid, nthreads, store);
+  if (K <= 8 && rows * 8 > nthreads)
+    router_rows_jl<1, 2>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w,
+                         coef, tid, nthreads, store);
+  else if (K <= 8)
+    router_rows_jl<1, 1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w,
+                         coef, tid, nthreads, store);
   else if (K <= 16)
-    router_rows_jl<2>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
-                      tid, nthreads, store);
+    router_rows_jl<2, 1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w,
+                         coef, tid, nthreads, store);
   else if (K <= 32)
-    router_rows_jl<4>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
-                      tid, nthreads, store);
+    router_rows_jl<4, 1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w,
+                         coef, tid, nthreads, store);
   else
-    router_rows_jl<8>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w, coef,
-                      tid, nthreads, store);
+    router_rows_jl<8, 1>(recv, C, rows, stride, col0, swz, w2s, b1s, b2s, K, k, t_first, N, ok, logits, ids, w,
+                         coef, tid, nthreads, store);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

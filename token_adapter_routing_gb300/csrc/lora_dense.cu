@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the learned router for the owner's rows: hidden units from the C partials,
       // logits, top k and softmax; logits, ids and w go out, the coefficients to scratch
       // (the plan takes K*r of 64 or 128 with r >= 16, so K <= 8: one logit per lane)
-      router_rows_jl<1>(recv, C, RPC, PC, KR, false, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have_h,
+      router_rows_jl<1, 1>(recv, C, RPC, PC, KR, false, w2s, b1s, b2s, K, k, t0 + crank * RPC, N, got && have_h,
                         rio.logits, rio.ids, rio.w, coef_s, tid, kEpilogueThreads, true);
       named_barrier(2, kEpilogueThreads);  // coefficients ready
     }
