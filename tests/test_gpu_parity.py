@@ -370,7 +370,9 @@ def make_adapters(N, d_in, d_out, K, r, seed):
 @pytest.mark.parametrize("K,r,k,N,d_in,d_out", [(4, 16, 2, 700, 1024, 1536), (4, 16, 1, 300, 512, 512),
                                                 (8, 16, 3, 513, 1024, 1024), (4, 32, 4, 200, 1024, 2048),
                                                 (8, 16, 2, 333, 2048, 1024), (2, 64, 2, 260, 1024, 512),
-                                                (4, 16, 4, 130, 1024, 1024), (4, 16, 2, 64, 4096, 1024)])
+                                                (4, 16, 4, 130, 1024, 1024), (4, 16, 2, 64, 4096, 1024),
+                                                # 63 tiles: clusters of 4 in one wave (152 SMs), ragged tail
+                                                (4, 16, 2, 4001, 2048, 1024)])
 def test_apply_dense_vs_oracle(m, K, r, k, N, d_in, d_out):
     x, A, B, y0 = make_adapters(N, d_in, d_out, K, r, seed=N + K + r)
     ids, w = random_topk(N, K, k, seed=k + 5)

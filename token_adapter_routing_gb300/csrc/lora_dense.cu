@@ -37,6 +37,9 @@
 
 #include <cstring>
 #include <mutex>
+#ifdef MOLORA_TUNING_ENV
+#include <cstdlib>
+#endif
 
 #include "common.cuh"
 #include "kernels.h"
@@ -122,15 +125,39 @@ bool dense_plan(int32_t d_in, int32_t d_out, int32_t K, int32_t r, int C, int ro
   return s->smem <= budget;
 }
 
-// Two CTAs per SM first (clusters of 8 first, one round first), else one per SM.
-bool dense_choose(int32_t d_in, int32_t d_out, int32_t K, int32_t r, bool router, DensePlan* s) {
+// Two CTAs per SM first, else one per SM.  Among the plans of a tier (one round first), the
+// widest cluster whose CTAs all fit one wave (tiles x C <= CTAs resident at once): a second,
+// partial wave repeats every CTA's serial front (gather, cluster reduction) behind the first
+// wave's epilogue.  Measured on GB300 for the top-2 dense apply at 4096 tokens, 2048 -> 6144,
+// K = 4, r = 16: clusters of 4 in one wave 49.1 us, clusters of 8 in 1.7 waves 53.2 us.  When
+// no cluster fits one wave, the widest that fits the tier.
+bool dense_choose(int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, bool router, DensePlan* s) {
   // K*r = 256 would need 128 KB of G tiles alone (hi and lo, M = 128 rows): it never fits.
   // The stacked shrink operand is made of 64-column blocks: K*r is 64 or 128.
   if (!(r == 16 || r == 32 || r == 64) || (K * r != 64 && K * r != 128)) return false;
-  for (size_t budget : {kTwoPerSm, kMaxSmem})
+  int only_c = 0, only_rounds = 0;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_DENSE_CLUSTER")) only_c = atoi(e);
+  if (const char* e = getenv("MOLORA_DENSE_ROUNDS")) only_rounds = atoi(e);
+#endif
+  const int64_t tiles = (N + kTileRows - 1) / kTileRows;
+  for (size_t budget : {kTwoPerSm, kMaxSmem}) {
+    const int64_t resident = (budget == kTwoPerSm ? 2 : 1) * (int64_t)num_sms();
+    bool found = false;
+    DensePlan widest{};
     for (int C : {8, 4, 2, 1})
-      for (int rounds : {1, 2})
-        if (dense_plan(d_in, d_out, K, r, C, rounds, budget, router, s)) return true;
+      for (int rounds : {1, 2}) {
+        if ((only_c && C != only_c) || (only_rounds && rounds != only_rounds)) continue;
+        if (!dense_plan(d_in, d_out, K, r, C, rounds, budget, router, s)) continue;
+        if (tiles * C <= resident) return true;
+        if (!found) widest = *s, found = true;
+        break;  // this cluster size's first fitting plan
+      }
+    if (found) {
+      *s = widest;
+      return true;
+    }
+  }
   return false;
 }
 
@@ -571,15 +598,13 @@ bool dense_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 }  // namespace
 
 bool dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
-  (void)N;
   DensePlan s;
-  return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, false, &s) && dense_encoder() != nullptr;
+  return dtype == MOLORA_BF16 && dense_choose(N, d_in, d_out, K, r, false, &s) && dense_encoder() != nullptr;
 }
 
 bool router_dense_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r) {
-  (void)N;
   DensePlan s;
-  return dtype == MOLORA_BF16 && dense_choose(d_in, d_out, K, r, true, &s) && dense_encoder() != nullptr;
+  return dtype == MOLORA_BF16 && dense_choose(N, d_in, d_out, K, r, true, &s) && dense_encoder() != nullptr;
 }
 
 // Where the dense path beat the scalar and grouped ones on GB300 (top-2, r = 16, warm and L2
@@ -605,7 +630,7 @@ cudaError_t launch_dense(const void* x, int64_t N, int32_t d_in, int32_t d_out, 
                          bool y_bf16, int32_t* err_word, const void* W1, const RouterIo& rio, cudaStream_t stream) {
   const bool router = W1 != nullptr;
   DensePlan s;
-  if (!dense_choose(d_in, d_out, K, r, router, &s)) return cudaErrorNotSupported;
+  if (!dense_choose(N, d_in, d_out, K, r, router, &s)) return cudaErrorNotSupported;
   CUtensorMap map_b, map_w1;
   // B seen as [K*r x d_out]: a box is all K*r rows (every adapter) by 64 columns
   if (!dense_map(&map_b, B, (uint64_t)K * r, (uint64_t)d_out, 64, (uint32_t)(K * r), CU_TENSOR_MAP_SWIZZLE_128B))
