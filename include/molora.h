@@ -278,10 +278,9 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
 /*
  * molora_router_lora_apply -- the learned router and the top-k apply in one pass over x
  * (Table 1: routing cost O(64d + 64K) on top of the apply; Figure 2: top-k adapters combined
- * by a weighted sum).  Its results equal, bit for bit, those of molora_router_topk followed
- * by molora_lora_apply on the dense path (MOLORA_PATH_DENSE), computed in one kernel that
- * reads each x row once for both: the router's x W1 is 64 more columns of the apply's shrink
- * x [A_0 | ... | A_{K-1}].
+ * by a weighted sum).  It computes molora_router_topk followed by molora_lora_apply on the
+ * dense path (MOLORA_PATH_DENSE) in one kernel that reads each x row once for both: the
+ * router's x W1 is 64 more columns of the apply's shrink x [A_0 | ... | A_{K-1}].
  *
  *   logits, ids, w   as molora_router_topk (same hidden width 64, same top-k and softmax rule)
  *   y[t,:] += scale * sum_j w[t,j] * (x[t,:] A_{ids[t,j]}) B_{ids[t,j]}
@@ -294,8 +293,12 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
  * Every y element receives one addition, so results are reproducible for any k.
  * Two kernel families:
  *   - one kernel, K*r = 64 or 128, y fp32 or bf16, d_in and d_out multiples of 64 that split
- *     evenly over its cluster; logits, ids, w and y equal molora_router_topk followed by the
- *     dense molora_lora_apply bit for bit.  Used without a workspace (ws_bytes == NULL);
+ *     evenly over its cluster.  Its logits, ids, w and y equal molora_router_topk followed by
+ *     the dense molora_lora_apply bit for bit whenever both split d_in over the same number
+ *     of CTAs (each takes the widest cluster whose CTAs fit one wave: 64-token tiles here,
+ *     128-token tiles in molora_router_topk; with 152 SMs both split 8 ways up to 2432
+ *     tokens).  Otherwise the hidden units' partial sums group differently and the logits
+ *     may differ in the last bits.  Used without a workspace (ws_bytes == NULL);
  *   - the stacked pair (the shrink with the router, then the expand GEMM), K*r up to 1024,
  *     fp32 y, d_in a multiple of 64.  Its router sums the 64 hidden units in order for each
  *     logit, so its logits may differ from molora_router_topk's in the last bits.  Used

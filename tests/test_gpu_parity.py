@@ -832,7 +832,8 @@ def test_router_apply_fused_vs_oracle(m, kw, k):
 
 @pytest.mark.parametrize("kw,k", FUSED_CASES[:3])
 def test_router_apply_fused_equals_two_calls(m, kw, k):
-    # the same summation orders as the separate router and dense apply: identical results
+    # the same summation orders as the separate router and dense apply (at these sizes both
+    # split d_in 8 ways): identical results
     wl = workloads.make("topk_mlp", k=k, **kw)
     x, W1, W2, A, B = dev(wl.x), dev(wl.W1), dev(wl.W2), dev(wl.A), dev(wl.B)
     y_f, y_s = dev(wl.y0).clone(), dev(wl.y0).clone()

@@ -146,7 +146,7 @@ bool dense_choose(int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, 
     bool found = false;
     DensePlan widest{};
     for (int C : {8, 4, 2, 1})
-      for (int rounds : {1, 2}) {
+      for (int rounds : {1, 2, 4}) {
         if ((only_c && C != only_c) || (only_rounds && rounds != only_rounds)) continue;
         if (!dense_plan(d_in, d_out, K, r, C, rounds, budget, router, s)) continue;
         if (tiles * C <= resident) return true;

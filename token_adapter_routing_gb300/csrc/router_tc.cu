@@ -11,7 +11,8 @@
 // mbarrier), and the owner sums the C partials in rank order (deterministic).  Eight lanes per
 // token then form the hidden units, the logits, the top k (strictly greater wins, so equal
 // logits keep the lower index) and the softmax over the k, all in registers (router_rows in
-// common.cuh, shared with the fused router + apply kernel, so both give identical results).
+// common.cuh, shared with the fused router + apply kernel: the same arithmetic, so both give
+// identical results whenever they split d_in the same way).
 #include <cudaTypedefs.h>
 
 #include <mutex>
