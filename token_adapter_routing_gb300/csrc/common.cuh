@@ -163,6 +163,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* ma
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
+// As tma_load_2d, but the box lands at the same shared-memory offset in every CTA of
+// `cta_mask` (this cluster's ranks), each counting the bytes on its own mbarrier at bar's offset.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t sdst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                      uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(sdst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
 // smem box -> global through a tensor map, each element ADDED to the destination (the
 // element type of the map: fp32 add for a FLOAT32 map); rows and columns outside the tensor
 // are skipped.  Completes as a bulk group of the issuing thread.
@@ -269,6 +279,13 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
+               : "memory");
+}
+// As umma_commit, arriving on the mbarrier at bar's offset in every CTA of `cta_mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(cta_mask)
                : "memory");
 }
 

@@ -607,16 +607,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int BN = P.BN, S = P.S, nkb = P.nkb;
   const int64_t m_tiles = (N + kRows - 1) / kRows;
   const int n_tiles = (d_out + BN - 1) / BN;
-  const int64_t tiles = m_tiles * n_tiles;
+  // A cluster of two CTAs takes pairs of tiles: the same columns, consecutive 128-row blocks
+  // (rank 0 the even block, rank 1 the odd one).  Both need the same B blocks, so each loads
+  // half of every B block and multicasts it to both.  A rank-1 tile past the last row block
+  // reads G as zeros (out of bounds) and writes nothing.
+  const int rank = (int)cluster_ctarank();
+  const int64_t ptiles = (m_tiles + 1) / 2 * n_tiles;  // tile pairs
+  const int64_t cl = blockIdx.x / 2, ncl = gridDim.x / 2;
+  auto tile_m0 = [&](int64_t pt) { return (int32_t)(((pt / n_tiles) * 2 + rank) * kRows); };
+  auto tile_n0 = [&](int64_t pt) { return (int32_t)((pt % n_tiles) * BN); };
   volatile int32_t* abort = &ctrl->abort;
   // this thread's row segment of a tile, prefetched into L2 one tile ahead
-  auto prefetch_y = [&](int64_t tile) {
-    if (tile >= tiles) return;
-    const int64_t m = tile / n_tiles;
-    const int n = (int)(tile % n_tiles);
-    const int64_t t = m * kRows + tid;
-    const int cols = min(BN, d_out - n * BN);
-    if (t < N && cols > 0) prefetch_l2_bulk(y + t * d_out + (int64_t)n * BN, (uint32_t)cols * 4u);
+  auto prefetch_y = [&](int64_t pt) {
+    if (pt >= ptiles) return;
+    const int64_t t = (int64_t)tile_m0(pt) + tid;
+    const int n0 = tile_n0(pt);
+    const int cols = min(BN, d_out - n0);
+    if (t < N && cols > 0) prefetch_l2_bulk(y + t * d_out + n0, (uint32_t)cols * 4u);
   };
 
   if (warp == 5) {
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&ctrl->full[s], 1);
-      mbar_init(&ctrl->empty[s], 1);
+      mbar_init(&ctrl->empty[s], 2);  // released by both CTAs' MMAs (B lands in both)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctrl->tfull[b], 1);
@@ -641,12 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_y);
   }
   // y is not written by the kernel this one may overlap; a prefetch only moves lines into L2
-  if (warp < 4) prefetch_y(blockIdx.x);
+  if (warp < 4) prefetch_y(cl);
   pdl_wait();  // G comes from the previous kernel
   pdl_launch_dependents();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  cluster_arrive();
+  cluster_wait();  // the partner's barriers are initialised before any multicast reaches them
 
   if (warp == 4) {
     // ---- TMA producer: per tile, nkb K-blocks of G_hi, G_lo and B
@@ -654,9 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = P.stage_bytes;
       int64_t it = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int32_t m0 = (int32_t)((tile / n_tiles) * kRows);
-        const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
+      for (int64_t pt = cl; pt < ptiles && ok; pt += ncl) {
+        const int32_t m0 = tile_m0(pt);
+        const int32_t n0 = tile_n0(pt);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = (int)(it % S);
           const int64_t use = it / S;
@@ -668,16 +677,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&ctrl->full[s], bytes);
           tma_load_2d(smem_u32(st), &map_ghi, kb * kKBlock, m0, &ctrl->full[s]);
           tma_load_2d(smem_u32(st + P.off_glo), &map_glo, kb * kKBlock, m0, &ctrl->full[s]);
-          for (int q = 0; q < BN / 64; ++q)
-            tma_load_2d(smem_u32(st + P.off_b + (size_t)q * kKBlock * 128), &map_b, n0 + q * 64, kb * kKBlock,
-                        &ctrl->full[s]);
+          // this CTA's half of the B boxes, into both CTAs (each counts all of B on its own full[s])
+          for (int q = rank; q < BN / 64; q += 2)
+            tma_load_2d_multicast(smem_u32(st + P.off_b + (size_t)q * kKBlock * 128), &map_b, n0 + q * 64,
+                                  kb * kKBlock, &ctrl->full[s], (uint16_t)0x3);
         }
       }
-      // nothing may land in shared memory after the CTA has left
+      // nothing may land in shared memory after the CTA has left: the last fill of every stage
+      // (the partner's multicast halves included) and both CTAs' last releases of it
       const int64_t issued = it;
       for (int s = 0; s < S && s < issued; ++s) {
         const int64_t last = (issued - 1 - s) / S;
         mbar_wait(&ctrl->full[s], (uint32_t)last & 1u);
+        mbar_wait(&ctrl->empty[s], (uint32_t)last & 1u);
       }
     }
     __syncwarp();
@@ -687,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kRows, (uint32_t)BN, false, true);
       int64_t it = 0, tc = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tc) {
+      for (int64_t pt = cl; pt < ptiles && ok; pt += ncl, ++tc) {
         const int buf = (int)(tc & 1);
         const int64_t use = tc >> 1;
         if (use > 0 && !mbar_wait_or_abort(&ctrl->tempty[buf], (uint32_t)(use - 1) & 1u, abort)) {
@@ -712,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f16(d, dh, db, idesc, (kb | ks) != 0);
             umma_f16(d, dl, db, idesc, 1);
           }
-          umma_commit(&ctrl->empty[s]);
+          umma_commit_multicast(&ctrl->empty[s], (uint16_t)0x3);  // the stage is free in both CTAs' eyes
         }
         if (!ok) break;
         umma_commit(&ctrl->tfull[buf]);
@@ -729,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = sm + P.off_stage + (size_t)warp * nstg * 4096;
     int sb = 0;
     int64_t tc = 0;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tc) {
+    for (int64_t pt = cl; pt < ptiles; pt += ncl, ++tc) {
       const int buf = (int)(tc & 1);
-      prefetch_y(tile + gridDim.x);
+      prefetch_y(pt + ncl);
       // warp-uniform, since the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&ctrl->tfull[buf], (uint32_t)(tc >> 1) & 1u, abort))) break;
       tc_fence_after();
-      const int32_t m0 = (int32_t)((tile / n_tiles) * kRows) + warp * 32;
-      const int32_t n0 = (int32_t)((tile % n_tiles) * BN);
+      const int32_t m0 = tile_m0(pt) + warp * 32;
+      const int32_t n0 = tile_n0(pt);
       // boxes that start past the last row or column hold nothing of y: skipped outright
       // (warp-uniform), so that the staging buffers are taken strictly in turn by issued
       // reductions and the wait below always covers the buffer about to be rewritten
@@ -779,8 +791,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
   __syncthreads();
+  if (warp == 5) mbar_wait(&ctrl->mma_done, 0);
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();  // neither CTA leaves while the other may still write or arrive into it
   if (warp == 5) {
-    mbar_wait(&ctrl->mma_done, 0);
     tc_fence_after();
     tmem_dealloc(tmem, 2u * (uint32_t)BN);
   }
@@ -908,9 +923,11 @@ cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t 
                                 dim3((unsigned)(tiles * sp.C)), dim3(kThreads), sp.smem, stream, cluster, N, d_in, K,
                                 r, k, ids, w, scale, g_hi, g_lo, err_word, rio, sp, map_x, map_a, map_w1);
   if (e != cudaSuccess) return e;
-  const int64_t exp_tiles = tiles * ((d_out + ep.BN - 1) / ep.BN);
-  const int grid = (int)(exp_tiles < num_sms() ? exp_tiles : num_sms());
-  return launch_kernel(stacked_expand_kernel, dim3((unsigned)grid), dim3(kThreads), ep.smem, stream, 0, N, d_out, y,
+  // persistent clusters of two CTAs over pairs of tiles (see stacked_expand_kernel)
+  const int64_t exp_pairs = (tiles + 1) / 2 * ((d_out + ep.BN - 1) / ep.BN);
+  const int64_t max_clusters = num_sms() / 2;
+  const int grid = 2 * (int)(exp_pairs < max_clusters ? exp_pairs : max_clusters);
+  return launch_kernel(stacked_expand_kernel, dim3((unsigned)grid), dim3(kThreads), ep.smem, stream, 2, N, d_out, y,
                        err_word, ep, map_ghi, map_glo, map_b, map_y);
 }
 
