@@ -1050,6 +1050,22 @@ def run_mode(args):
             res[f"b2b_{name}"] = {"p50_us": round(p50 * 1e3, 2), "p99_us": round(p99 * 1e3, 2),
                                   "tokens_per_s_p50": round(wl.N / (p50 * 1e-3), 1),
                                   "frac_of_measured_hbm": round(nbytes / (p50 * 1e-3) / 1e9 / peak, 3) if peak else None}
+        # the one-kernel path as the main line times it: 20 calls in one CUDA graph over three
+        # (x, y) batches (350 MB, more than the L2), one event pair around the replay
+        gb = torch.Generator().manual_seed(8765)
+        lb = [(x, y)] + [(torch.randn(x.shape, generator=gb).to(x.dtype).to(dev),
+                          torch.randn(y.shape, generator=gb).to(dev)) for _ in range(2)]
+        st = {"i": 0}
+
+        def fused_rot():
+            xb, yb = lb[st["i"] % len(lb)]
+            st["i"] += 1
+            m.molora_router_lora_apply(xb, W1, W2, A, B, wl.k, yb, wl.scale, logits=logits, ids=ids, w=w,
+                                       use_ws=False)
+        lus = _loop_us(fused_rot, stream, n=20, reps=7)
+        res["b2b_fused_loop"] = {"us_per_call": round(lus, 2), "tokens_per_s": round(wl.N / (lus * 1e-6), 1),
+                                 "frac_of_measured_hbm": round(nbytes / (lus * 1e-6) / 1e9 / peak, 3) if peak else None,
+                                 "timing": "20 calls in one CUDA graph over 3 (x, y) batches (> L2)"}
         res["algorithmic_bytes"] = nbytes
         path_grouped()  # ids, w, counts, offsets and perm for the apply-only graphs
         torch.cuda.synchronize()
