@@ -98,6 +98,19 @@ __device__ __forceinline__ void cp_async_16(uint32_t sdst, const void* gsrc, uin
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes)
                : "memory");
 }
+// An L2 policy that makes the lines it touches the first to be evicted: for data read exactly
+// once (x), so that it does not push out lines that are still to be used (y prefetched ahead).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// cp_async_16 under an L2 cache policy (l2_policy_evict_first).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t sdst, const void* gsrc, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(sdst), "l"(gsrc),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // One arrival on `bar` once every cp.async this thread issued so far has landed (the
 // barrier's expected count includes this arrival).

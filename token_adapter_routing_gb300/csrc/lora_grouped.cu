@@ -403,6 +403,10 @@ __global__ void __maxnreg__(168)
     }
   }
   // lanes 8q..8q+7 copy the eight 16-byte chunks of one 128-byte row segment
+  // x is read once: its lines go first, so that the prefetched y lines stay for the reductions
+  // (measured: 19.30 -> 18.76 us on the 4-modality apply; the same hint on the y reductions
+  // changed nothing)
+  const uint64_t x_policy = l2_policy_evict_first();
   auto gather = [&](int rd) {
     uint8_t* xb = xs + (rd % nbuf) * buf_bytes;
     const int sub = lane >> 3, chunk = lane & 7;
@@ -414,7 +418,7 @@ __global__ void __maxnreg__(168)
         const int row = it * 16 + warp * 4 + sub;
         const int32_t tok = ctrl->tok[row];
         const __nv_bfloat16* src = tok >= 0 ? x + (int64_t)tok * d_in + col : x;
-        cp_async_16(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u);
+        cp_async_16_hint(blk + sw128_offset(row, chunk), src, tok >= 0 ? 16u : 0u, x_policy);
       }
     }
     cp_async_commit();
