@@ -754,13 +754,12 @@ cudaError_t launch_lora_grouped(const void* x, int64_t N, int32_t d_in, int32_t 
   if (!choose(d_in, d_out, r, mask_adapter >= 0 ? N : N * (int64_t)k, mask_adapter >= 0 ? 1 : K, &s))
     return cudaErrorNotSupported;
   s.prefetch_y = 1;
-  // DRAM idles for about 2 us while the tile is decoded; prefetching 60% of y (at most
+  // DRAM idles for about 2 us while the tile is decoded; prefetching 45% of y (at most
   // 24 MiB) fills that window and measured best on GB300 (4-modality workload, back-to-back
-  // steps, with the permutation read into shared memory: 0, 20, 40, 60 and 80% tried; 40%
-  // was best while the tile's tokens took a second dependent global load).  The rest of y
-  // follows per row, late.
+  // steps, x gathered evict-first: 20, 30, 40, 50, 60, 80 and 100% tried, 40-50% best).  The
+  // rest of y follows per row, late.
   const uint64_t y_bytes = (uint64_t)N * d_out * (y_bf16 ? 2u : 4u);
-  const uint64_t early = y_bytes * 3u / 5u;
+  const uint64_t early = y_bytes * 9u / 20u;
   s.early_y = (early < (24ull << 20) ? early : (24ull << 20)) & ~uint64_t(15);
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_PREFETCH_Y")) s.prefetch_y = atoi(e);
