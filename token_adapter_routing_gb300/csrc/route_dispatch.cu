@@ -100,6 +100,16 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
   pdl_wait();
   pdl_launch_dependents();
+  // this thread's slots' ids (up to kPre per thread), loaded before the ranges so that the two
+  // global loads are in flight together rather than one after the other
+  constexpr int kPre = 4;
+  const bool pre_ok = S <= (int64_t)kPre * blockDim.x;
+  int32_t pre[kPre];
+#pragma unroll
+  for (int q = 0; q < kPre; ++q) {
+    const int64_t s = threadIdx.x + (int64_t)q * blockDim.x;
+    pre[q] = pre_ok && s < S ? src[s] : 0;
+  }
   if (kVocab) {
     for (int i = threadIdx.x; i <= K; i += blockDim.x) s_starts[i] = starts[i];
     __syncthreads();
@@ -114,14 +124,22 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
 
   // every slot's id, read once; invalid ids become -1
   bool bad = false, outside = false;
-  for (int64_t s = threadIdx.x; s < S; s += blockDim.x) {
+  for (int64_t s = threadIdx.x, q = 0; s < S; s += blockDim.x, ++q) {
+    int32_t v = 0;
+    if (pre_ok) {
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        if (i == q) v = pre[i];
+    } else {
+      v = src[s];
+    }
     int32_t a;
     if (kVocab) {
-      a = vocab_range(s_starts, K, src[s]);
+      a = vocab_range(s_starts, K, v);
       outside |= a < 0;
       adapter[s] = a;
     } else {
-      a = src[s];
+      a = v;
     }
     if (a < 0 || a >= K) {
       bad = true;
