@@ -205,6 +205,9 @@ def test_apply_small_integers_bitexact(m, path, N, d_in, d_out, K, r, k):
     ("modality4", {"N": 517, "d_in": 1024, "d_out": 2048, "r": 64, "K": 8}),
     ("modality4", {"dist": "80-10-5-5"}),
     ("modality4", {"dist": "95-2-2-1"}),
+    # the permutation (6000 slots) is larger than the idle x buffers (2048 slots at d_in = 512):
+    # the tile's tokens come from global memory instead of a shared-memory copy
+    ("modality4", {"N": 6000, "d_in": 512, "d_out": 512}),
     # d_in = 8192: a K-slice of 1024 columns per CTA takes two x rounds over two buffers
     ("modality4", {"N": 300, "d_in": 8192, "d_out": 1024}),
     ("modality4", {"N": 200, "d_in": 8192, "d_out": 1024, "r": 64}),
