@@ -170,6 +170,33 @@ MOLORA_API molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t
                                           int32_t* perm, int32_t* err_word, cudaStream_t stream);
 
 /*
+ * molora_route_vocab_dispatch_ex -- molora_route_vocab_dispatch with flags; flags == 0 is
+ * exactly molora_route_vocab_dispatch.  Outputs are identical with and without flags.
+ *
+ * MOLORA_INPUTS_READY: the caller promises that tok and starts are not written by the kernel
+ * enqueued just before this call on `stream`, nor by anything that kernel does not itself wait
+ * for.  Examples: the ids were copied in from the host, or written by an earlier step.  Every
+ * kernel of this library lets its successor start only after everything before it has
+ * finished, so after any call of this library the promise concerns only writes made before
+ * that call.
+ *   - The kernel then starts while the preceding kernel still runs.  It reads tok and starts
+ *     and builds the histogram, offsets and permutation in shared memory.
+ *   - It waits for the preceding kernel to finish only before its first store, because that
+ *     kernel may still read the buffers this call writes (the previous step's adapter,
+ *     counts, offsets or perm).
+ *   - This moves the routing of step i+1 under the apply of step i when both are enqueued back
+ *     to back; programmatic dependent launch, Figure 4's one captured graph per step.
+ *   - Applies up to N = 40960 tokens, the sizes held in shared memory. Larger N runs as
+ *     flags == 0.
+ * Any other bit set in flags: MOLORA_ERR_INVALID_ARG, nothing launched.
+ */
+#define MOLORA_INPUTS_READY 1u
+MOLORA_API molora_status molora_route_vocab_dispatch_ex(const int32_t* tok, int64_t N, const int32_t* starts,
+                                             int32_t K, int32_t* adapter, int32_t* counts, int32_t* offsets,
+                                             int32_t* perm, int32_t* err_word, uint32_t flags,
+                                             cudaStream_t stream);
+
+/*
  * molora_route_vocab_lora_apply -- the whole vocabulary-routed step: molora_route_vocab_dispatch
  * followed by molora_lora_apply on its outputs (k = 1, weights 1), with the same results:
  *

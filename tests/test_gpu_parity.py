@@ -161,6 +161,80 @@ def test_route_vocab_dispatch_fused_bad_ranges(m):
         assert torch.equal(got.cpu(), sep.cpu())
 
 
+@pytest.mark.parametrize("N,K,outside", [(0, 4, False), (1, 1, False), (2048, 4, False), (513, 7, True),
+                                         (40960, 64, False), (40961, 16, True), (100000, 8, False)])
+def test_route_vocab_dispatch_inputs_ready_equals_plain(m, N, K, outside):
+    """With INPUTS_READY (reads before the wait on the preceding kernel, stores after it) the
+    outputs and error bits are the oracle's and those of the plain call, on both sides of the
+    staging limit (above it the flag has no effect)."""
+    g = torch.Generator().manual_seed(7 * N + K)
+    starts = torch.cat([torch.zeros(1, dtype=torch.int32),
+                        torch.sort(torch.randperm(31999, generator=g)[:K - 1] + 1).values.int(),
+                        torch.tensor([32000], dtype=torch.int32)])
+    lo, hi = (-50, 32050) if outside else (0, 32000)
+    tok = torch.randint(lo, hi, (N,), generator=g, dtype=torch.int32)
+    e1, e2 = err_word(), err_word()
+    got = m.molora_route_vocab_dispatch_ex(dev(tok), dev(starts), m.INPUTS_READY, err_word=e1)
+    plain = m.molora_route_vocab_dispatch(dev(tok), dev(starts), err_word=e2)
+    torch.cuda.synchronize()
+    ref_a, n_out = oracle.route_vocab(tok, starts)
+    rc, ro, rp, _ = oracle.dispatch(ref_a, K)
+    for a, b, ref in zip(got, plain, (ref_a, rc, ro, rp)):
+        assert torch.equal(a.cpu(), ref) and torch.equal(a.cpu(), b.cpu())
+    assert int(e1.item()) == int(e2.item())
+    assert (int(e1.item()) != 0) == (n_out > 0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_inputs_ready_steps_reuse_dispatch_buffers(m, path):
+    """Back-to-back steps that route into the SAME adapter/counts/offsets/perm buffers: each
+    step's routing kernel starts while the previous step's apply still reads those buffers, and
+    must store only after it has finished.  Every step's y matches the oracle, enqueued eagerly
+    and replayed from one captured graph."""
+    wls = [workloads.make("modality4", seed=4242 + i) for i in range(3)]
+    K = wls[0].K
+    bufs = dict(adapter=torch.empty(wls[0].N, dtype=torch.int32, device="cuda"),
+                counts=torch.empty(K, dtype=torch.int32, device="cuda"),
+                offsets=torch.empty(K + 1, dtype=torch.int32, device="cuda"),
+                perm=torch.empty(wls[0].N, dtype=torch.int32, device="cuda"))
+    ins = [dict(tok=dev(w.tok), starts=dev(w.starts), x=dev(w.x), A=dev(w.A), B=dev(w.B)) for w in wls]
+    refs = []
+    for w in wls:
+        ref_a, _ = oracle.route_vocab(w.tok, w.starts)
+        refs.append(oracle.lora_apply(w.x, w.A, w.B, ref_a, w.y0, w.scale)[0])
+
+    def steps(ys, e):
+        for i, w in enumerate(wls):
+            a, c, o, p = m.molora_route_vocab_dispatch_ex(ins[i]["tok"], ins[i]["starts"], m.INPUTS_READY,
+                                                          err_word=e, **bufs)
+            m.molora_lora_apply(ins[i]["x"], ins[i]["A"], ins[i]["B"], a, ys[i], w.scale, counts=c, offsets=o,
+                                perm=p, err_word=e, path=path)
+
+    e = err_word()
+    ys = [dev(w.y0).clone() for w in wls]
+    steps(ys, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    for y, ref in zip(ys, refs):
+        assert_apply_close(y, ref)
+
+    s = torch.cuda.Stream()
+    e = err_word()
+    ys = [dev(w.y0).clone() for w in wls]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        steps(ys, e)
+    for y, w in zip(ys, wls):  # capture enqueues nothing: start again from y0
+        y.copy_(dev(w.y0))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    for y, ref in zip(ys, refs):
+        assert_apply_close(y, ref)
+
+
 # ------------------------------------------------------------------------- apply
 
 def small_int_case(N, d_in, d_out, K, r, k, seed, dtype=torch.bfloat16):

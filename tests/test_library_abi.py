@@ -81,6 +81,15 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_route_vocab_dispatch(fake, 8, None, 4, fake, fake, fake, fake, None, None) == INVALID
     assert lib.molora_route_vocab_dispatch(fake, 8, fake, 4, fake, fake, None, fake, None, None) == INVALID
     assert lib.molora_route_vocab_dispatch(fake, -1, fake, 4, fake, fake, fake, fake, None, None) == INVALID
+    # the flags variant: the same checks, and any flag bit other than INPUTS_READY (1) is refused
+    lib.molora_route_vocab_dispatch_ex.argtypes = [P, I64, P, I32, P, P, P, P, P, ctypes.c_uint32, P]
+    rvd_ex = lib.molora_route_vocab_dispatch_ex
+    assert rvd_ex(fake, 8, fake, 4, fake, fake, fake, fake, None, 2, None) == INVALID
+    assert rvd_ex(fake, 8, fake, 4, fake, fake, fake, fake, None, 0x80000001, None) == INVALID
+    assert rvd_ex(fake, 8, fake, 0, fake, fake, fake, fake, None, 1, None) == INVALID
+    assert rvd_ex(None, 8, fake, 4, fake, fake, fake, fake, None, 1, None) == INVALID
+    assert rvd_ex(fake, 8, fake, 4, fake, fake, None, fake, None, 0, None) == INVALID
+    assert rvd_ex(fake, -1, fake, 4, fake, fake, fake, fake, None, 1, None) == INVALID
 
     def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0,
               ws=None, ws_bytes=None):
@@ -249,6 +258,8 @@ def test_binding_rejects_mis_sized_tensors_before_any_launch():
     starts = torch.arange(K + 1, dtype=torch.int32)
     with pytest.raises(ValueError, match="perm must"):
         m.molora_route_vocab_dispatch(tok, starts, perm=torch.zeros(N + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="counts must"):
+        m.molora_route_vocab_dispatch_ex(tok, starts, m.INPUTS_READY, counts=torch.zeros(K + 1, dtype=torch.int32))
     with pytest.raises(ValueError, match="adapter must"):
         m.molora_route_vocab(tok, starts, adapter=torch.zeros(N - 1, dtype=torch.int32))
     with pytest.raises(ValueError, match="adapter_of must"):
@@ -260,7 +271,7 @@ def test_launching_calls_run_on_the_tensors_device():
     caller whose current device differs still launches where the data lives."""
     import token_adapter_routing_gb300 as m
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_lora_apply", "molora_route_vocab_lora_apply", "molora_router_lora_apply",
+                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_route_vocab_lora_apply", "molora_router_lora_apply",
                  "molora_lora_apply_static_ws", "molora_lora_apply_masked_pass", "molora_selftest_bounded_wait"):
         fn = getattr(m, name)
         assert getattr(fn, "__wrapped__", None) is not None, f"{name} has no device guard"

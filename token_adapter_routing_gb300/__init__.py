@@ -44,10 +44,12 @@ DEV_BAD_RANGES = 0x2
 DEV_BAD_ADAPTER_ID = 0x4
 DEV_BAD_PERMUTATION = 0x8
 DEV_WAIT_TIMEOUT = 0x10
+INPUTS_READY = 0x1  # molora_route_vocab_dispatch_ex flag
 MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+            "molora_route_vocab_dispatch_ex",
             "molora_lora_apply", "molora_router_lora_apply", "molora_route_vocab_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
             "molora_lora_apply_masked_pass", "molora_select_path", "molora_status_string", "molora_version",
@@ -84,6 +86,7 @@ def load_library(path=None):
     lib.molora_router_topk.argtypes = [P, S, I64, I32, P, P, P, P, I32, I32, P, P, P, P]
     lib.molora_dispatch.argtypes = [P, I64, I32, I32, P, P, P, P, P]
     lib.molora_route_vocab_dispatch.argtypes = [P, I64, P, I32, P, P, P, P, P, P]
+    lib.molora_route_vocab_dispatch_ex.argtypes = [P, I64, P, I32, P, P, P, P, P, ctypes.c_uint32, P]
     lib.molora_lora_apply.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P, P, P]
     lib.molora_lora_apply_ex.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, P, P, P, F, P, P, P, P, S,
                                          P]
@@ -102,7 +105,7 @@ def load_library(path=None):
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
+                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
                  "molora_router_lora_apply", "molora_route_vocab_lora_apply", "molora_lora_apply_masked_pass",
                  "molora_select_path", "molora_version", "molora_selftest_bounded_wait",
                  "molora_lora_apply_static_ws"):
@@ -329,6 +332,18 @@ def molora_dispatch(ids, K, counts=None, offsets=None, perm=None, err_word=None,
 def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=None, perm=None, err_word=None,
                                 stream=None):
     """molora_route_vocab then molora_dispatch (k = 1) as one kernel: (adapter, counts, offsets, perm)."""
+    return _route_vocab_dispatch(tok, starts, adapter, counts, offsets, perm, err_word, stream, None)
+
+
+@_on_tensor_device
+def molora_route_vocab_dispatch_ex(tok, starts, flags, adapter=None, counts=None, offsets=None, perm=None,
+                                   err_word=None, stream=None):
+    """molora_route_vocab_dispatch with flags (INPUTS_READY: tok and starts are not written by the
+    kernel enqueued just before, so the kernel reads them before waiting on it)."""
+    return _route_vocab_dispatch(tok, starts, adapter, counts, offsets, perm, err_word, stream, int(flags))
+
+
+def _route_vocab_dispatch(tok, starts, adapter, counts, offsets, perm, err_word, stream, flags):
     N, K = tok.numel(), starts.numel() - 1
     for name, t, n in (("adapter", adapter, N), ("counts", counts, K), ("offsets", offsets, K + 1), ("perm", perm, N)):
         _need(t, name, n)
@@ -347,9 +362,12 @@ def molora_route_vocab_dispatch(tok, starts, adapter=None, counts=None, offsets=
     _sized(counts, "counts", K, torch.int32, dev)
     _sized(offsets, "offsets", K + 1, torch.int32, dev)
     _sized(perm, "perm", N, torch.int32, dev)
-    _check("molora_route_vocab_dispatch", load_library().molora_route_vocab_dispatch(
-        _p(tok), N, _p(starts), K, _p(adapter), _p(counts), _p(offsets), _p(perm), _p(_err_word(err_word, dev)),
-        _stream(stream, dev)))
+    args = (_p(tok), N, _p(starts), K, _p(adapter), _p(counts), _p(offsets), _p(perm), _p(_err_word(err_word, dev)))
+    if flags is None:
+        _check("molora_route_vocab_dispatch", load_library().molora_route_vocab_dispatch(*args, _stream(stream, dev)))
+    else:
+        _check("molora_route_vocab_dispatch_ex",
+               load_library().molora_route_vocab_dispatch_ex(*args, flags, _stream(stream, dev)))
     return adapter, counts, offsets, perm
 
 

@@ -22,10 +22,11 @@ cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* sta
 
 cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* err_word, cudaStream_t stream);
-// Vocabulary routing and dispatch in one single-CTA kernel (k = 1).
+// Vocabulary routing and dispatch in one single-CTA kernel (k = 1).  early != 0: tok and starts
+// are not written by the preceding kernel, so they are read before waiting on it.
 cudaError_t launch_route_vocab_dispatch(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
                                         int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
-                                        int32_t* err_word, cudaStream_t stream);
+                                        int32_t* err_word, int early, cudaStream_t stream);
 
 // Token-major CUDA-core apply.  mask_adapter >= 0 turns it into one masked per-sequence pass:
 // adapter mask_adapter for every token, weight [ids[t] == mask_adapter] (k must be 1).

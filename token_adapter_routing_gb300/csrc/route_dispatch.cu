@@ -89,7 +89,7 @@ template <bool kVocab>
 __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     dispatch_kernel(const int32_t* __restrict__ src, const int32_t* __restrict__ starts, int64_t S, int32_t K,
                     int32_t* adapter, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                    int32_t* __restrict__ perm, int32_t* err_word) {
+                    int32_t* __restrict__ perm, int32_t* err_word, int early) {
   extern __shared__ int32_t s_ids[];  // [S] when S <= kStageSlots
   __shared__ int32_t cnt[kDispatchWarps][kMaxAdapters];
   __shared__ int32_t s_total[kMaxAdapters];
@@ -97,9 +97,16 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   __shared__ int32_t s_starts[kMaxAdapters + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = S <= kStageSlots;
+  // With `early`, the token ids and ranges are not written by the kernel before this one, so
+  // reading them, the histogram, the scan and the ranks run before waiting on that kernel
+  // (which may still be reading this call's output buffers); every store comes after the wait.
+  // The ids must stay in shared memory for that, so only staged sizes read early.
+  const bool read_early = kVocab && early && staged;
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
-  pdl_wait();
-  pdl_launch_dependents();
+  if (!read_early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   // this thread's slots' ids (up to kPre per thread), loaded before the ranges so that the two
   // global loads are in flight together rather than one after the other
   constexpr int kPre = 4;
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     if (kVocab) {
       a = vocab_range(s_starts, K, v);
       outside |= a < 0;
-      adapter[s] = a;
+      if (!read_early) adapter[s] = a;  // (read_early: stored from s_ids after the wait)
     } else {
       a = v;
     }
@@ -182,6 +189,11 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
     s_off[K] = run;
   }
   __syncthreads();
+  if (read_early) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t s = threadIdx.x; s < S; s += blockDim.x) adapter[s] = s_ids[s];
+  }
   if (threadIdx.x < K) {
     const int a = threadIdx.x;
     int32_t run = s_off[a];
@@ -212,7 +224,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
 template <bool kVocab>
 static cudaError_t launch_dispatch_impl(const int32_t* src, const int32_t* starts, int64_t S, int32_t K,
                                         int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
-                                        int32_t* err_word, cudaStream_t stream) {
+                                        int32_t* err_word, int early, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
@@ -223,19 +235,19 @@ static cudaError_t launch_dispatch_impl(const int32_t* src, const int32_t* start
   if (attr != cudaSuccess) return attr;
   const size_t smem = S <= kStageSlots ? (size_t)S * 4 : 0;
   return launch_kernel(dispatch_kernel<kVocab>, dim3(1), dim3(kDispatchWarps * 32), smem, stream, 0, src, starts, S,
-                       K, adapter, counts, offsets, perm, err_word);
+                       K, adapter, counts, offsets, perm, err_word, early);
 }
 
 cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* err_word, cudaStream_t stream) {
-  return launch_dispatch_impl<false>(ids, nullptr, N * (int64_t)k, K, nullptr, counts, offsets, perm, err_word,
+  return launch_dispatch_impl<false>(ids, nullptr, N * (int64_t)k, K, nullptr, counts, offsets, perm, err_word, 0,
                                      stream);
 }
 
 cudaError_t launch_route_vocab_dispatch(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
                                         int32_t* adapter, int32_t* counts, int32_t* offsets, int32_t* perm,
-                                        int32_t* err_word, cudaStream_t stream) {
-  return launch_dispatch_impl<true>(tok, starts, N, K, adapter, counts, offsets, perm, err_word, stream);
+                                        int32_t* err_word, int early, cudaStream_t stream) {
+  return launch_dispatch_impl<true>(tok, starts, N, K, adapter, counts, offsets, perm, err_word, early, stream);
 }
 
 // ---------------------------------------------------------------------------------------
