@@ -173,12 +173,15 @@ MOLORA_API molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t
  * molora_route_vocab_dispatch_ex -- molora_route_vocab_dispatch with flags; flags == 0 is
  * exactly molora_route_vocab_dispatch.  Outputs are identical with and without flags.
  *
- * MOLORA_INPUTS_READY: the caller promises that tok and starts are not written by the kernel
- * enqueued just before this call on `stream`, nor by anything that kernel does not itself wait
- * for.  Examples: the ids were copied in from the host, or written by an earlier step.  Every
- * kernel of this library lets its successor start only after everything before it has
- * finished, so after any call of this library the promise concerns only writes made before
- * that call.
+ * MOLORA_INPUTS_READY: the caller promises that tok and starts are not written by any kernel
+ * that may still run when this call's kernel starts.  Examples: the ids were copied in from
+ * the host, or written by an earlier step.  That kernel starts once the kernel enqueued just
+ * before it lets it start:
+ *   - Every other call of this library lets its successor start only after everything before
+ *     it has finished. Enqueued after one of them, the promise concerns only the kernel just
+ *     before this call.
+ *   - A call made with this flag lets its successor start at once.  After a chain of such
+ *     calls, the promise extends to the kernel before the chain.
  *   - The kernel then starts while the preceding kernel still runs.  It reads tok and starts
  *     and builds the histogram, offsets and permutation in shared memory.
  *   - It waits for the preceding kernel to finish only before its first store, because that

@@ -100,11 +100,14 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   // With `early`, the token ids and ranges are not written by the kernel before this one, so
   // reading them, the histogram, the scan and the ranks run before waiting on that kernel
   // (which may still be reading this call's output buffers); every store comes after the wait.
-  // The ids must stay in shared memory for that, so only staged sizes read early.
+  // The ids must stay in shared memory for that, so only staged sizes read early.  The next
+  // kernel may start at once: it waits for this one to finish before it reads what it wrote.
   const bool read_early = kVocab && early && staged;
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
   if (!read_early) {
     pdl_wait();
+    pdl_launch_dependents();
+  } else {
     pdl_launch_dependents();
   }
   // this thread's slots' ids (up to kPre per thread), loaded before the ranges so that the two
@@ -191,7 +194,6 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   __syncthreads();
   if (read_early) {
     pdl_wait();
-    pdl_launch_dependents();
     for (int64_t s = threadIdx.x; s < S; s += blockDim.x) adapter[s] = s_ids[s];
   }
   if (threadIdx.x < K) {
