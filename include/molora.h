@@ -224,6 +224,21 @@ MOLORA_API molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64
                                             int32_t* err_word, cudaStream_t stream);
 
 /*
+ * molora_route_vocab_lora_apply_ex -- molora_route_vocab_lora_apply with flags; flags == 0 is
+ * exactly molora_route_vocab_lora_apply, and results are identical with and without flags.
+ * MOLORA_INPUTS_READY means what it means for molora_route_vocab_dispatch_ex: the caller's
+ * promise about tok and starts, which lets this step's routing kernel run under the kernel
+ * enqueued before it, for example the previous step's apply.  Any other bit:
+ * MOLORA_ERR_INVALID_ARG, nothing launched.
+ */
+MOLORA_API molora_status molora_route_vocab_lora_apply_ex(const int32_t* tok, int64_t N, const int32_t* starts,
+                                               int32_t K, const void* x, molora_dtype dtype, int32_t d_in,
+                                               int32_t d_out, const void* A, const void* B, int32_t r,
+                                               float scale, void* y, int32_t y_bf16, int32_t* adapter,
+                                               int32_t* counts, int32_t* offsets, int32_t* perm,
+                                               int32_t* err_word, uint32_t flags, cudaStream_t stream);
+
+/*
  * molora_lora_apply -- batched per-token LoRA apply over the hot set (Figure 2; Table 10
  * shapes; Figure 4 hot set):
  *

@@ -235,6 +235,32 @@ def test_inputs_ready_steps_reuse_dispatch_buffers(m, path):
         assert_apply_close(y, ref)
 
 
+def test_inputs_ready_one_call_steps_reuse_dispatch_buffers(m):
+    """The one-call step with INPUTS_READY, three steps back to back into one set of dispatch
+    buffers: every step's y matches the oracle, and the routing outputs left behind are the
+    last step's."""
+    wls = [workloads.make("modality4", seed=5151 + i) for i in range(3)]
+    K = wls[0].K
+    bufs = dict(adapter=torch.empty(wls[0].N, dtype=torch.int32, device="cuda"),
+                counts=torch.empty(K, dtype=torch.int32, device="cuda"),
+                offsets=torch.empty(K + 1, dtype=torch.int32, device="cuda"),
+                perm=torch.empty(wls[0].N, dtype=torch.int32, device="cuda"))
+    e = err_word()
+    ys = [dev(w.y0).clone() for w in wls]
+    for w, y in zip(wls, ys):
+        m.molora_route_vocab_lora_apply_ex(dev(w.tok), dev(w.starts), dev(w.x), dev(w.A), dev(w.B), y, w.scale,
+                                           m.INPUTS_READY, err_word=e, **bufs)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    for w, y in zip(wls, ys):
+        ref_a, _ = oracle.route_vocab(w.tok, w.starts)
+        assert_apply_close(y, oracle.lora_apply(w.x, w.A, w.B, ref_a, w.y0, w.scale)[0])
+    last_a, _ = oracle.route_vocab(wls[-1].tok, wls[-1].starts)
+    rc, ro, rp, _ = oracle.dispatch(last_a, K)
+    for got, ref in ((bufs["adapter"], last_a), (bufs["counts"], rc), (bufs["offsets"], ro), (bufs["perm"], rp)):
+        assert torch.equal(got.cpu(), ref)
+
+
 # ------------------------------------------------------------------------- apply
 
 def small_int_case(N, d_in, d_out, K, r, k, seed, dtype=torch.bfloat16):

@@ -90,6 +90,15 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert rvd_ex(None, 8, fake, 4, fake, fake, fake, fake, None, 1, None) == INVALID
     assert rvd_ex(fake, 8, fake, 4, fake, fake, None, fake, None, 0, None) == INVALID
     assert rvd_ex(fake, -1, fake, 4, fake, fake, fake, fake, None, 1, None) == INVALID
+    lib.molora_route_vocab_lora_apply_ex.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P,
+                                                     P, P, ctypes.c_uint32, P]
+
+    def step_ex(flags=1, K=4, y=fake, adapter=fake):
+        return lib.molora_route_vocab_lora_apply_ex(fake, 16, fake, K, fake, 1, 64, 64, fake, fake, 16, 2.0, y, 0,
+                                                    adapter, fake, fake, fake, None, flags, None)
+
+    assert step_ex(flags=4) == INVALID and step_ex(flags=0xFFFFFFFF) == INVALID
+    assert step_ex(K=0) == INVALID and step_ex(y=None) == INVALID and step_ex(adapter=None) == INVALID
 
     def apply(x=fake, dtype=1, N=16, d_in=64, d_out=64, A=fake, B=fake, K=4, r=16, ids=fake, k=1, y=fake, path=0,
               ws=None, ws_bytes=None):
@@ -271,7 +280,8 @@ def test_launching_calls_run_on_the_tensors_device():
     caller whose current device differs still launches where the data lives."""
     import token_adapter_routing_gb300 as m
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_route_vocab_lora_apply", "molora_router_lora_apply",
+                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_route_vocab_lora_apply",
+                 "molora_route_vocab_lora_apply_ex", "molora_router_lora_apply",
                  "molora_lora_apply_static_ws", "molora_lora_apply_masked_pass", "molora_selftest_bounded_wait"):
         fn = getattr(m, name)
         assert getattr(fn, "__wrapped__", None) is not None, f"{name} has no device guard"

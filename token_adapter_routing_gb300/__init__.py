@@ -49,7 +49,7 @@ MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
 EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-            "molora_route_vocab_dispatch_ex",
+            "molora_route_vocab_dispatch_ex", "molora_route_vocab_lora_apply_ex",
             "molora_lora_apply", "molora_router_lora_apply", "molora_route_vocab_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
             "molora_lora_apply_masked_pass", "molora_select_path", "molora_status_string", "molora_version",
@@ -97,6 +97,8 @@ def load_library(path=None):
                                              I32, P, P, P, P]
     lib.molora_route_vocab_lora_apply.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P, P,
                                                   P, P]
+    lib.molora_route_vocab_lora_apply_ex.argtypes = [P, I64, P, I32, P, S, I32, I32, P, P, I32, F, P, I32, P, P, P,
+                                                     P, P, ctypes.c_uint32, P]
     lib.molora_lora_apply_masked_pass.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, I32, F, P, P, S, P]
     lib.molora_lora_apply_static_ws.argtypes = [P, S, I64, I32, I32, P, P, I32, I32, P, P, I32, F, P, P, P]
     lib.molora_select_path.argtypes = [S, I64, I32, I32, I32, I32, I32]
@@ -105,7 +107,7 @@ def load_library(path=None):
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
     for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
+                 "molora_route_vocab_dispatch_ex", "molora_route_vocab_lora_apply_ex", "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
                  "molora_router_lora_apply", "molora_route_vocab_lora_apply", "molora_lora_apply_masked_pass",
                  "molora_select_path", "molora_version", "molora_selftest_bounded_wait",
                  "molora_lora_apply_static_ws"):
@@ -455,6 +457,19 @@ def molora_route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter=None, 
                                   perm=None, err_word=None, stream=None):
     """The whole vocabulary-routed step in one call: routing, dispatch and the apply (k = 1).
     Returns (adapter, counts, offsets, perm); y (fp32 or bf16) is updated in place."""
+    return _route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter, counts, offsets, perm, err_word, stream,
+                                   None)
+
+
+@_on_tensor_device
+def molora_route_vocab_lora_apply_ex(tok, starts, x, A, B, y, scale, flags, adapter=None, counts=None, offsets=None,
+                                     perm=None, err_word=None, stream=None):
+    """molora_route_vocab_lora_apply with flags (INPUTS_READY: as for molora_route_vocab_dispatch_ex)."""
+    return _route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter, counts, offsets, perm, err_word, stream,
+                                   int(flags))
+
+
+def _route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter, counts, offsets, perm, err_word, stream, flags):
     N, K = tok.numel(), starts.numel() - 1
     if x.dim() != 2 or x.shape[0] != N:
         raise ValueError("x must be [N, d_in] with one row per token")
@@ -487,10 +502,15 @@ def molora_route_vocab_lora_apply(tok, starts, x, A, B, y, scale, adapter=None, 
     _sized(counts, "counts", K, torch.int32, dev)
     _sized(offsets, "offsets", K + 1, torch.int32, dev)
     _sized(perm, "perm", N, torch.int32, dev)
-    _check("molora_route_vocab_lora_apply", load_library().molora_route_vocab_lora_apply(
-        _p(tok), N, _p(starts), K, _p(x), _dtype_code(x), d_in, d_out, _p(A), _p(B), r, float(scale), _p(y),
-        1 if y.dtype == torch.bfloat16 else 0, _p(adapter), _p(counts), _p(offsets), _p(perm),
-        _p(_err_word(err_word, dev)), _stream(stream, dev)))
+    args = (_p(tok), N, _p(starts), K, _p(x), _dtype_code(x), d_in, d_out, _p(A), _p(B), r, float(scale), _p(y),
+            1 if y.dtype == torch.bfloat16 else 0, _p(adapter), _p(counts), _p(offsets), _p(perm),
+            _p(_err_word(err_word, dev)))
+    if flags is None:
+        _check("molora_route_vocab_lora_apply",
+               load_library().molora_route_vocab_lora_apply(*args, _stream(stream, dev)))
+    else:
+        _check("molora_route_vocab_lora_apply_ex",
+               load_library().molora_route_vocab_lora_apply_ex(*args, flags, _stream(stream, dev)))
     return adapter, counts, offsets, perm
 
 

@@ -184,21 +184,34 @@ molora_status molora_route_vocab_dispatch_ex(const int32_t* tok, int64_t N, cons
   return launched(launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, early, stream));
 }
 
+molora_status molora_route_vocab_lora_apply_ex(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                               const void* x, molora_dtype dtype, int32_t d_in, int32_t d_out,
+                                               const void* A, const void* B, int32_t r, float scale, void* y,
+                                               int32_t y_bf16, int32_t* adapter, int32_t* counts, int32_t* offsets,
+                                               int32_t* perm, int32_t* err_word, uint32_t flags, cudaStream_t stream) {
+  if (flags & ~(uint32_t)MOLORA_INPUTS_READY) return MOLORA_ERR_INVALID_ARG;
+  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, tok, 1, y);
+  if (st != MOLORA_OK) return st;
+  if (!starts || !counts || !offsets || (N > 0 && (!adapter || !perm))) return MOLORA_ERR_INVALID_ARG;
+  const int early = (flags & MOLORA_INPUTS_READY) ? 1 : 0;
+  if (N == 0)  // the empty histogram, as molora_route_vocab_dispatch writes it
+    return launched(launch_route_vocab_dispatch(tok, 0, starts, K, adapter, counts, offsets, perm, err_word, early,
+                                                stream));
+  const molora_path path = select_without_ws(dtype, N, d_in, d_out, K, r, 1, false);
+  if (launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, early, stream) !=
+      cudaSuccess)
+    return MOLORA_ERR_CUDA;
+  return apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, adapter, nullptr, 1, counts, offsets, perm, scale, y,
+                    y_bf16 != 0, err_word, path, stream);
+}
+
 molora_status molora_route_vocab_lora_apply(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
                                             const void* x, molora_dtype dtype, int32_t d_in, int32_t d_out,
                                             const void* A, const void* B, int32_t r, float scale, void* y,
                                             int32_t y_bf16, int32_t* adapter, int32_t* counts, int32_t* offsets,
                                             int32_t* perm, int32_t* err_word, cudaStream_t stream) {
-  const molora_status st = check_apply_args(x, dtype, N, d_in, d_out, A, B, K, r, tok, 1, y);
-  if (st != MOLORA_OK) return st;
-  if (!starts || !counts || !offsets || (N > 0 && (!adapter || !perm))) return MOLORA_ERR_INVALID_ARG;
-  if (N == 0)  // the empty histogram, as molora_route_vocab_dispatch writes it
-    return launched(launch_route_vocab_dispatch(tok, 0, starts, K, adapter, counts, offsets, perm, err_word, 0, stream));
-  const molora_path path = select_without_ws(dtype, N, d_in, d_out, K, r, 1, false);
-  if (launch_route_vocab_dispatch(tok, N, starts, K, adapter, counts, offsets, perm, err_word, 0, stream) != cudaSuccess)
-    return MOLORA_ERR_CUDA;
-  return apply_impl(x, dtype, N, d_in, d_out, A, B, K, r, adapter, nullptr, 1, counts, offsets, perm, scale, y,
-                    y_bf16 != 0, err_word, path, stream);
+  return molora_route_vocab_lora_apply_ex(tok, N, starts, K, x, dtype, d_in, d_out, A, B, r, scale, y, y_bf16,
+                                          adapter, counts, offsets, perm, err_word, 0u, stream);
 }
 
 molora_path molora_select_path(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r,
