@@ -375,6 +375,46 @@ def assert_bf16y_close(y_gpu, y0_bf16, y_ref32, rounds, slot_updates=None):
     assert not bool(bad.any()), f"{int(bad.sum())} elements beyond {rounds} bf16 ulp; worst {err.max().item():.3e}"
 
 
+@pytest.mark.parametrize("N,d_in,d_out,K,r,k", [(1, 4096, 4096, 16, 16, 1), (64, 4096, 4096, 8, 16, 2),
+                                                (160, 4096, 4096, 16, 16, 1), (300, 2048, 2048, 8, 64, 2),
+                                                (77, 1024, 3072, 4, 32, 1)])
+def test_scalar_decode_sizes_small_integers_bitexact(m, N, d_in, d_out, K, r, k):
+    """The scalar path at decode batch sizes with d up to 4096, where it splits each token's
+    output columns over several CTAs. Small-integer inputs make every partial sum exact, so y
+    must equal the oracle bit for bit, and a second run must reproduce it."""
+    x, A, B, y0, ids, w = small_int_case(N, d_in, d_out, K, r, k, 3 * N + r)
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 0.5, w)
+    assert y_ref.abs().max().item() < 2 ** 24
+    ys = []
+    for _ in range(2):
+        y = dev(y0).clone()
+        e = err_word()
+        m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 0.5, w=dev(w), err_word=e, path="scalar")
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0
+        ys.append(y.cpu())
+    assert torch.equal(ys[0], y_ref) and torch.equal(ys[1], y_ref)
+
+
+@pytest.mark.parametrize("N,d,K,r,k,dtype", [(100, 4096, 16, 16, 2, torch.bfloat16), (200, 4096, 16, 16, 1, torch.bfloat16),
+                                             (50, 2048, 4, 16, 1, torch.float32), (9, 4096, 4, 64, 3, torch.bfloat16)])
+def test_scalar_decode_sizes_vs_oracle(m, N, d, K, r, k, dtype):
+    """Random inputs at decode batch sizes on the scalar path (bf16 and fp32 x, top-1 to 3),
+    against the oracle."""
+    g = torch.Generator().manual_seed(N * 7 + r)
+    x = torch.randn(N, d, generator=g).to(dtype)
+    A = (torch.randn(K, d, r, generator=g) / math.sqrt(d)).to(dtype)
+    B = (torch.randn(K, r, d, generator=g) / math.sqrt(r)).to(dtype)
+    y0 = torch.randn(N, d, generator=g)
+    ids = torch.stack([torch.randperm(K, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.softmax(torch.randn(N, k, generator=g), dim=1)
+    y = dev(y0).clone()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 2.0, w=dev(w), path="scalar")
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 2.0, w)
+    assert_apply_close(y, y_ref)
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("k", [1, 2])
 def test_apply_bf16y_small_integers_bitexact(m, path, k):
