@@ -104,12 +104,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32, 1)
   // kernel may start at once: it waits for this one to finish before it reads what it wrote.
   const bool read_early = kVocab && early && staged;
   for (int i = threadIdx.x; i < kDispatchWarps * kMaxAdapters; i += blockDim.x) (&cnt[0][0])[i] = 0;
-  if (!read_early) {
-    pdl_wait();
-    pdl_launch_dependents();
-  } else {
-    pdl_launch_dependents();
-  }
+  if (!read_early) pdl_wait();
+  pdl_launch_dependents();
   // this thread's slots' ids (up to kPre per thread), loaded before the ranges so that the two
   // global loads are in flight together rather than one after the other
   constexpr int kPre = 4;
