@@ -64,7 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "topk", "router", "perseq", "skew",
+    p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "crossover_stacked", "topk", "router",
+                                      "perseq", "skew",
                                       "bf16y", "indirect", "split", "kernels", "tiling"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
@@ -605,6 +606,9 @@ def run_mode(args):
     crossover_topk  top-2 with router-like weights, r = 16: d = 4096 at K = 4 and 8 over batch
                1..2048, and 2048 -> 6144 at K = 4 over 512..8192 tokens; scalar, grouped (with
                dispatch) and dense (without) applies, L2 flushed.
+    crossover_stacked  the stacked pair against dispatch + grouped apply (ids and weights given)
+               at d = 4096: K*r of 256, 512 and 1024 with r = 16 and 64, k = 1, 2, 4, N = 1024..8192;
+               warm, 50 calls back to back in one graph.
     topk       top-k scaling (Table 16): N=8192, d=4096, K=8, r=64, k=1..4, router -> dispatch
                -> apply as one CUDA graph replayed --replays times back to back; p50 / p99.
     router     the learned-router workload at a Qwen3-1.7B MLP shape (N=4096, 2048 -> 6144,
@@ -909,6 +913,39 @@ def run_mode(args):
                     row[f"{path}_us_warm"] = round(_loop_us(fn, stream), 3)
                 row["fastest"] = min(("scalar", "grouped", "dense"), key=lambda p_: row[f"{p_}_us_warm"])
                 emit(row)
+    elif args.mode == "crossover_stacked":
+        d = 4096
+        for K, r in ((16, 16), (4, 64), (32, 16), (8, 64), (64, 16), (16, 64)):
+            for k in (1, 2, 4):
+                for b in (1024, 2048, 4096, 8192):
+                    g_ = torch.Generator().manual_seed(b + 7 * K + r + k)
+                    x = torch.randn(b, d, generator=g_).to(torch.bfloat16).to(dev)
+                    A = (torch.randn(K, d, r, generator=g_) / math.sqrt(d)).to(torch.bfloat16).to(dev)
+                    B = (torch.randn(K, r, d, generator=g_) / math.sqrt(r)).to(torch.bfloat16).to(dev)
+                    y = torch.randn(b, d, generator=g_).to(dev)
+                    ids = torch.stack([torch.randperm(K, generator=g_)[:k] for _ in range(b)]).to(torch.int32).to(dev)
+                    w = torch.softmax(torch.randn(b, k, generator=g_), dim=1).to(dev)
+                    counts = torch.empty(K, dtype=torch.int32, device=dev)
+                    offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
+                    perm = torch.empty(b * k, dtype=torch.int32, device=dev)
+                    need = m.molora_workspace_bytes(b, d, d, K, r, k, path="stacked")
+                    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+                    row = {"mode": "crossover_stacked", "d": d, "K": K, "r": r, "k": k, "batch": b,
+                           "auto_with_ws": m.molora_select_path(torch.bfloat16, b, d, d, K, r, k)}
+
+                    def grouped():
+                        m.molora_dispatch(ids, K, counts=counts, offsets=offsets, perm=perm)
+                        m.molora_lora_apply(x, A, B, ids, y, 2.0, w=w, counts=counts, offsets=offsets, perm=perm,
+                                            path="grouped")
+
+                    def stacked():
+                        m.molora_lora_apply(x, A, B, ids, y, 2.0, w=w, path="stacked", ws=ws)
+
+                    for name, fn in (("grouped", grouped), ("stacked", stacked)):
+                        row[f"{name}_us_warm"] = round(_loop_us(fn, stream, n=20, reps=3), 3)
+                    row["faster"] = "stacked" if row["stacked_us_warm"] < row["grouped_us_warm"] else "grouped"
+                    emit(row)
+                    del x, A, B, y, ids, w, ws
     elif args.mode == "crossover":
         for dist in ("uniform", "zipf"):
             for K in (4, 8, 16, 32, 64):

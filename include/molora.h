@@ -252,7 +252,8 @@ MOLORA_API molora_status molora_route_vocab_lora_apply_ex(const int32_t* tok, in
  *                         molora_router_topk)
  * w       fp32 [N x k]    slot weights, or NULL for all ones
  * counts, offsets, perm   molora_dispatch's outputs for these ids (read by the grouped
- *                         path; the scalar path reads ids directly and ignores them)
+ *                         path; the scalar path reads ids directly and ignores them).  AUTO
+ *                         takes the grouped path only when all three are given
  * y       fp32 [N x d_out], updated in place (read-modify-write)
  *
  * ws, ws_bytes  workspace (see the convention above); the stacked path needs

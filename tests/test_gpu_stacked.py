@@ -223,3 +223,35 @@ def test_full_size_topk_scaling_stacked(m, k):
     m.molora_lora_apply(x, A, B, ids, ys, wl.scale, w=w, ws=ws, path="stacked")
     torch.cuda.synchronize()
     assert torch.equal(ys.cpu(), y.cpu())  # same G, same expand: the router's choice drives both
+
+
+@pytest.mark.parametrize("N,K,r,k,want", [(2048, 16, 16, 1, "grouped"), (2048, 16, 16, 4, "stacked"),
+                                          (8192, 8, 64, 1, "stacked"), (1024, 4, 64, 1, "grouped"),
+                                          (1024, 4, 64, 2, "stacked"), (4096, 64, 16, 4, "stacked"),
+                                          (2048, 64, 16, 2, "grouped"), (8192, 16, 64, 1, "grouped")])
+def test_auto_stacked_or_grouped_follows_the_measured_crossover(m, N, K, r, k, want):
+    """At d = 4096 AUTO (with a workspace) takes the stacked pair only where it measured faster
+    than dispatch + grouped apply: few adapters per selected one, enough tokens."""
+    assert m.molora_select_path(torch.bfloat16, N, 4096, 4096, K, r, k) == want
+
+
+@pytest.mark.parametrize("with_ws", [True, False])
+def test_auto_without_dispatch_outputs_picks_a_path_that_needs_none(m, with_ws):
+    """A shape where AUTO prefers the grouped path, called without counts/offsets/perm: AUTO
+    runs the stacked pair when a workspace is given and the scalar path otherwise, and either
+    matches the oracle."""
+    N, d_in, d_out, K, r, k = 2048, 1024, 1024, 16, 16, 1
+    assert m.molora_select_path(torch.bfloat16, N, d_in, d_out, K, r, k) == "grouped"
+    x, A, B, y0 = make_adapters(N, d_in, d_out, K, r, seed=31)
+    ids, w = random_topk(N, K, k, seed=32)
+    y = dev(y0).clone()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = None
+    if with_ws:
+        ws = torch.empty(m.molora_workspace_bytes(N, d_in, d_out, K, r, k, path="stacked"), dtype=torch.uint8,
+                         device="cuda")
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 2.0, w=dev(w), err_word=e, ws=ws)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0, 2.0, w)
+    assert_apply_close(y, y_ref)

@@ -98,6 +98,17 @@ static molora_status apply_impl(const void* x, molora_dtype dtype, int64_t N, in
       if (path == MOLORA_PATH_STACKED && (!have_ws || y_bf16 || !stacked_supported(dtype, N, d_in, d_out, K, r, false)))
         path = select_without_ws(dtype, N, d_in, d_out, K, r, k, false);
     }
+    // AUTO takes the grouped path only with the dispatch outputs it reads; without them, the
+    // fastest path that needs none (the stacked pair if its workspace was given)
+    if (path == MOLORA_PATH_GROUPED && !query && (!counts || !offsets || !perm)) {
+      const bool ws_fits = have_ws && ws != nullptr && *ws_bytes >= stacked_workspace_bytes(N, K, r);
+      if (!table && !y_bf16 && ws_fits && stacked_supported(dtype, N, d_in, d_out, K, r, false))
+        path = MOLORA_PATH_STACKED;
+      else if (!table && k >= 2 && dense_supported(dtype, N, d_in, d_out, K, r))
+        path = MOLORA_PATH_DENSE;
+      else
+        path = MOLORA_PATH_SCALAR;
+    }
   }
   if (path == MOLORA_PATH_STACKED) {
     if (!have_ws) return N == 0 ? MOLORA_OK : MOLORA_ERR_INVALID_ARG;

@@ -852,12 +852,21 @@ bool stacked_supported(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_ou
 
 size_t stacked_workspace_bytes(int64_t N, int32_t K, int32_t r) { return 2 * g_bytes(N, K * r); }
 
-// Where AUTO takes the stacked pair: a stacked rank of at least 256 columns (beyond the one-kernel
-// dense path) over at least 1024 tokens, the top-k scaling regime.
+// Where AUTO takes the stacked pair rather than dispatch + grouped apply: a stacked rank of at
+// least 256 columns (beyond the one-kernel dense path), few enough adapters per selected one
+// (the pair does K/k times the grouped path's tensor work) and enough tokens for its tiles to
+// fill the GPU.  Measured on GB300 at d = 4096 (bench.py --mode crossover_stacked: K*r of 256,
+// 512 and 1024 with r = 16 and 64, k = 1, 2, 4, 1024..8192 tokens); this rule picks the faster
+// path at 70 of the 72 points (the misses: a tie, and one point within 7%).  With k = 1 the
+// grouped path gathers and reduces each token once, which is why it keeps small batches even
+// at K/k = 4.
 bool stacked_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, int32_t k,
                        bool router) {
-  (void)k;
-  return K * r >= 256 && N >= 1024 && stacked_supported(dtype, N, d_in, d_out, K, r, router);
+  if (K * r < 256 || k < 1) return false;
+  const int32_t per_pick = (K + k - 1) / k;
+  const bool wins = (per_pick <= 4 && N >= 1024 && !(k == 1 && N < 2048)) || (per_pick <= 8 && N >= 2048) ||
+                    (per_pick <= 16 && k >= 2 && N >= 4096);
+  return wins && stacked_supported(dtype, N, d_in, d_out, K, r, router);
 }
 
 cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A, const void* B,
