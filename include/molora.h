@@ -351,6 +351,10 @@ MOLORA_API molora_status molora_lora_apply_indirect(const void* x, molora_dtype 
  *     whenever a buffer is passed (ws != NULL) and it applies.
  * A query (ws == NULL, ws_bytes != NULL) returns the stacked pair's size where it applies and
  * the one kernel does not or is measured slower, else 0.
+ * The stacked pair evaluates all K adapters for every token.  With many adapters per selected
+ * one and few tokens, molora_router_topk then molora_dispatch and the grouped apply (the
+ * separate calls) measured faster on GB300 at d = 4096, by the rule molora_lora_apply's AUTO
+ * uses for its own workspace path: e.g. top-1 over 16 adapters of rank 16, or top-2 over 64.
  * Other shapes return MOLORA_ERR_UNSUPPORTED (use the separate calls).  dtype must be
  * MOLORA_BF16; x, W1, A, B and y must be 16-byte aligned.
  */
