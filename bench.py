@@ -349,7 +349,8 @@ def run_ours(args, rank, world, local):
         "flushed_timing": "ms_per_step_flushed: one batch, a 256 MiB write before each step, CUDA events around "
                           "each graph replay (includes the graph launch)",
         "extra_timing": "route_dispatch_us: the fused routing + dispatch kernel alone over the same batches, back "
-                        "to back; apply_warm_us: the apply on one batch over and over (x and y stay in L2)",
+                        "to back (with INPUTS_READY, so each call reads while the previous one runs); "
+                        "apply_warm_us: the apply on one batch over and over (x and y stay in L2)",
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
