@@ -285,3 +285,21 @@ def test_launching_calls_run_on_the_tensors_device():
                  "molora_lora_apply_static_ws", "molora_lora_apply_masked_pass", "molora_selftest_bounded_wait"):
         fn = getattr(m, name)
         assert getattr(fn, "__wrapped__", None) is not None, f"{name} has no device guard"
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc not available")
+def test_header_compiles_as_c99(tmp_path):
+    """include/molora.h is a C ABI: a C99 translation unit that includes it and takes the
+    address of every declared entry point compiles without warnings from the header itself."""
+    import subprocess
+    cuda_inc = "/usr/local/cuda/include"
+    if not os.path.isdir(cuda_inc):
+        pytest.skip("CUDA headers not available")
+    body = "\n".join(f"  (void)&{name};" for name in declared_symbols())
+    src = tmp_path / "abi.c"
+    src.write_text(f'#include "molora.h"\nint main(void) {{\n  uint32_t f = MOLORA_INPUTS_READY;\n  (void)f;\n{body}\n'
+                   "  return 0;\n}\n")
+    out = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                          "-c", str(src), "-o", str(tmp_path / "abi.o")], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "molora.h" not in out.stderr, out.stderr
