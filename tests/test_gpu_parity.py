@@ -665,6 +665,25 @@ def test_apply_indirect_equals_slab(m, path, name, kw):
     assert_apply_close(y_ind, y_ref)
 
 
+def test_apply_auto_without_dispatch_outputs_indirect_and_slab(m):
+    """The 4-modality shape, where AUTO prefers the grouped path, called without counts,
+    offsets and perm: AUTO falls back to a path that needs none (the scalar path for both the
+    slab and the indirect layout here), and both match the oracle and each other bit for bit."""
+    wl = workloads.make("modality4")
+    assert m.molora_select_path(wl.dtype, wl.N, wl.d_in, wl.d_out, wl.K, wl.r, 1) == "grouped"
+    adapter = m.molora_route_vocab(dev(wl.tok), dev(wl.starts))
+    A_list, B_list = separate_adapters(wl)
+    y_slab, y_ind = dev(wl.y0).clone(), dev(wl.y0).clone()
+    e = err_word()
+    m.molora_lora_apply(dev(wl.x), dev(wl.A), dev(wl.B), adapter, y_slab, wl.scale, err_word=e)
+    m.molora_lora_apply(dev(wl.x), A_list, B_list, adapter, y_ind, wl.scale, err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(y_ind.cpu(), y_slab.cpu())
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
+    assert_apply_close(y_slab, y_ref)
+
+
 def test_apply_indirect_auto_never_takes_the_dense_path(m):
     # k = 2 at a shape where AUTO prefers the dense path for slabs: with the indirect layout it
     # must choose among the kernels that read the adapter table, and still match the oracle
