@@ -15,7 +15,8 @@
 //   streams the tile's x K-blocks and the matching A rows through a ring of stages, one
 //   thread issues tcgen05.mma (M = 128, N = the CTA's K*r/C columns) into TMEM.  With the
 //   learned router (kRouter), W1's 64 columns ride along, 64/C per CTA, as a second MMA per
-//   K step; the CTAs of a tile exchange their ReLU'd hidden units through distributed shared
+//   K step issued by a second thread (warp 6), so the two MMA streams are issued in parallel
+//   and a stage is released by both threads' commits; the CTAs of a tile exchange their ReLU'd hidden units through distributed shared
 //   memory, and every CTA evaluates the router's second stage for all 128 rows in the same
 //   order (so all agree on ids and weights) and keeps the coefficients of its own adapters.
 //   The epilogue scales each adapter's r columns by scale * c[t,a] and writes G as two bf16
@@ -45,6 +46,7 @@ constexpr int kRows = 128;      // tile rows = TMEM lanes = MMA M
 constexpr int kKBlock = 64;     // K elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = kEpiThreads + 64;  // + TMA producer warp (4) + MMA warp (5)
+constexpr int kShrThreads = kThreads + 32;  // shrink: + a second MMA warp (6) for the router's W1
 constexpr size_t kMaxSmem = 227 * 1024;
 constexpr size_t kSmemSlack = 1024;         // alignment of the dynamic smem base to 1024 B
 constexpr int kMaxStages = 6;
@@ -228,7 +230,7 @@ struct StackRouterIo {
 };
 
 template <bool kRouter>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kShrThreads, 1)
     stacked_shrink_kernel(int64_t N, int32_t d_in, int32_t K, int32_t r, int32_t k, const int32_t* __restrict__ ids,
                           const float* __restrict__ w, float scale, __nv_bfloat16* __restrict__ g_hi,
                           __nv_bfloat16* __restrict__ g_lo, int32_t* err_word, const StackRouterIo rio,
@@ -260,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&ctrl->full[s], 1);
-      mbar_init(&ctrl->empty[s], 1);
+      mbar_init(&ctrl->empty[s], kRouter ? 2 : 1);
     }
-    mbar_init(&ctrl->mma_done, 1);
+    mbar_init(&ctrl->mma_done, kRouter ? 2 : 1);
     mbar_init(&ctrl->recv, 1);
     ctrl->abort = 0;
     mbar_fence_init();
@@ -334,9 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_a = idesc_bf16_f32(kRows, (uint32_t)NA, false, true);
-      const uint32_t idesc_h = idesc_bf16_f32(kRows, (uint32_t)(NH > 0 ? NH : 16), false, true);
       const SmemLayout swa = swizzle_for_row_bytes((uint32_t)r * 2u);
-      const SmemLayout swh = swizzle_for_row_bytes((uint32_t)NH * 2u);
       bool ok = true;
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int s = kb % S;
@@ -350,11 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da = smem_desc(smem_u32(st + P.off_a + (size_t)ks * 16 * r * 2), (uint32_t)kKBlock * r * 2,
                                         8u * r * 2, swa);
           umma_f16(tmem, dx, da, idesc_a, (kb | ks) != 0);
-          if (kRouter) {
-            const uint64_t dh =
-                smem_desc(smem_u32(st + P.off_w1 + (size_t)ks * 16 * NH * 2), (uint32_t)kKBlock * NH * 2, 8u * NH * 2, swh);
-            umma_f16(tmem + (uint32_t)NA, dx, dh, idesc_h, (kb | ks) != 0);
-          }
         }
         umma_commit(&ctrl->empty[s]);  // the stage is free once these MMAs have read it
       }
@@ -364,6 +359,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
         umma_commit(&ctrl->mma_done);  // still arrives once every MMA issued above has finished
       }
+    }
+    __syncwarp();
+  } else if (kRouter && warp == 6) {
+    // ---- the router's W1 MMAs, issued in parallel with the adapters' by a second thread
+    if (lane == 0) {
+      const uint32_t idesc_h = idesc_bf16_f32(kRows, (uint32_t)NH, false, true);
+      const SmemLayout swh = swizzle_for_row_bytes((uint32_t)NH * 2u);
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % S;
+        ok = mbar_wait_or_abort(&ctrl->full[s], (uint32_t)(kb / S) & 1u, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t* st = sm + (size_t)s * P.stage_bytes;
+        for (int ks = 0; ks < kKBlock / 16; ++ks) {
+          const uint64_t dx = smem_desc(smem_u32(st + ks * 32), 16, 1024, kSwizzle128B);
+          const uint64_t dh =
+              smem_desc(smem_u32(st + P.off_w1 + (size_t)ks * 16 * NH * 2), (uint32_t)kKBlock * NH * 2, 8u * NH * 2, swh);
+          umma_f16(tmem + (uint32_t)NA, dx, dh, idesc_h, (kb | ks) != 0);
+        }
+        umma_commit(&ctrl->empty[s]);
+      }
+      if (!ok) report(err_word, MOLORA_DEV_WAIT_TIMEOUT);
+      umma_commit(&ctrl->mma_done);
     }
     __syncwarp();
   }
@@ -929,7 +948,7 @@ cudaError_t launch_lora_stacked(const void* x, int64_t N, int32_t d_in, int32_t 
   // the router variant exchanges hidden units within a tile's CTAs: a cluster of C
   const int cluster = router && sp.C > 1 ? sp.C : 0;
   cudaError_t e = launch_kernel(router ? stacked_shrink_kernel<true> : stacked_shrink_kernel<false>,
-                                dim3((unsigned)(tiles * sp.C)), dim3(kThreads), sp.smem, stream, cluster, N, d_in, K,
+                                dim3((unsigned)(tiles * sp.C)), dim3(kShrThreads), sp.smem, stream, cluster, N, d_in, K,
                                 r, k, ids, w, scale, g_hi, g_lo, err_word, rio, sp, map_x, map_a, map_w1);
   if (e != cudaSuccess) return e;
   // persistent clusters of two CTAs over pairs of tiles (see stacked_expand_kernel)
