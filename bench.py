@@ -64,8 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="CPU seconds for the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "crossover_stacked", "topk", "router",
-                                      "perseq", "skew",
+    p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "crossover_stacked", "decode_step", "topk",
+                                      "router", "perseq", "skew",
                                       "bf16y", "indirect", "split", "kernels", "tiling"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
@@ -607,6 +607,10 @@ def run_mode(args):
     crossover_topk  top-2 with router-like weights, r = 16: d = 4096 at K = 4 and 8 over batch
                1..2048, and 2048 -> 6144 at K = 4 over 512..8192 tokens; scalar, grouped (with
                dispatch) and dense (without) applies, L2 flushed.
+    decode_step  the decode step on the scalar path (vocabulary routing, then the scalar apply) at
+               batch 1, 32, 160 and 512 (d = 4096, r = 16, K = 16), with and without
+               INPUTS_READY on the routing call; warm, 50 steps back to back in one graph over
+               four batches of inputs sharing one adapter buffer.
     crossover_stacked  the stacked pair against dispatch + grouped apply (ids and weights given)
                at d = 4096: K*r of 256, 512 and 1024 with r = 16 and 64, k = 1, 2, 4, N = 1024..8192;
                warm, 50 calls back to back in one graph.
@@ -914,6 +918,26 @@ def run_mode(args):
                     row[f"{path}_us_warm"] = round(_loop_us(fn, stream), 3)
                 row["fastest"] = min(("scalar", "grouped", "dense"), key=lambda p_: row[f"{p_}_us_warm"])
                 emit(row)
+    elif args.mode == "decode_step":
+        for b in (1, 32, 160, 512):
+            wls = [workloads.make("decode_sweep", seed=100 + i, N=b, K=16) for i in range(4)]
+            ins = [dict(tok=w_.tok.to(dev), starts=w_.starts.to(dev), x=w_.x.to(dev), A=w_.A.to(dev),
+                        B=w_.B.to(dev), y=w_.y0.to(dev)) for w_ in wls]
+            adapter = torch.empty(b, dtype=torch.int32, device=dev)
+            row = {"mode": "decode_step", "batch": b, "K": 16, "d": 4096, "r": 16, "path": "scalar"}
+            for flag in (0, 1):
+                state = {"i": 0}
+
+                def step(flag=flag, state=state):
+                    d_ = ins[state["i"] % 4]
+                    state["i"] += 1
+                    if flag:
+                        m.molora_route_vocab_ex(d_["tok"], d_["starts"], m.INPUTS_READY, adapter=adapter)
+                    else:
+                        m.molora_route_vocab(d_["tok"], d_["starts"], adapter=adapter)
+                    m.molora_lora_apply(d_["x"], d_["A"], d_["B"], adapter, d_["y"], 2.0, path="scalar")
+                row["step_us_inputs_ready" if flag else "step_us"] = round(_loop_us(step, stream), 3)
+            emit(row)
     elif args.mode == "crossover_stacked":
         d = 4096
         for K, r in ((16, 16), (4, 64), (32, 16), (8, 64), (64, 16), (16, 64)):

@@ -98,6 +98,10 @@ typedef enum {
 #define MOLORA_DEV_WAIT_TIMEOUT 0x10        /* a bounded on-chip wait ran out; work abandoned */
 
 #define MOLORA_MAX_ADAPTERS 64   /* K: hot-set size limit (the decode sweep goes to 64) */
+
+/* Flags of the *_ex routing calls (molora_route_vocab_ex, molora_route_vocab_dispatch_ex,
+ * molora_route_vocab_lora_apply_ex): see molora_route_vocab_dispatch_ex for the promise. */
+#define MOLORA_INPUTS_READY 1u
 #define MOLORA_ROUTER_HIDDEN 64  /* hidden width of the learned router (Table 1 cost term 64d) */
 
 /*
@@ -113,6 +117,20 @@ typedef enum {
  */
 MOLORA_API molora_status molora_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
                                  int32_t* adapter, int32_t* err_word, cudaStream_t stream);
+
+/*
+ * molora_route_vocab_ex -- molora_route_vocab with flags; flags == 0 is exactly
+ * molora_route_vocab, and the outputs are identical with and without flags.
+ * MOLORA_INPUTS_READY (above; described with molora_route_vocab_dispatch_ex) is the same promise
+ * about tok and starts.  Each thread then routes its token before the kernel waits for the one
+ * enqueued before it (which may still read `adapter`: the previous step's routing, in a decode
+ * loop) and stores after; the next kernel may start at once.  Applies while N <= 256 * 8 * the
+ * SM count (one pass of the grid); larger N runs as flags == 0.  Any other bit:
+ * MOLORA_ERR_INVALID_ARG.
+ */
+MOLORA_API molora_status molora_route_vocab_ex(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                    int32_t* adapter, int32_t* err_word, uint32_t flags,
+                                    cudaStream_t stream);
 
 /*
  * molora_router_topk -- learned router TopK(g(x)) (Table 1; Figure 2 with k = 2;
@@ -196,7 +214,6 @@ MOLORA_API molora_status molora_route_vocab_dispatch(const int32_t* tok, int64_t
  *     flags == 0.
  * Any other bit set in flags: MOLORA_ERR_INVALID_ARG, nothing launched.
  */
-#define MOLORA_INPUTS_READY 1u
 MOLORA_API molora_status molora_route_vocab_dispatch_ex(const int32_t* tok, int64_t N, const int32_t* starts,
                                              int32_t K, int32_t* adapter, int32_t* counts, int32_t* offsets,
                                              int32_t* perm, int32_t* err_word, uint32_t flags,

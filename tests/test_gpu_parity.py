@@ -185,6 +185,76 @@ def test_route_vocab_dispatch_inputs_ready_equals_plain(m, N, K, outside):
     assert (int(e1.item()) != 0) == (n_out > 0)
 
 
+@pytest.mark.parametrize("N,K,outside", [(1, 1, False), (160, 16, False), (513, 7, True), (4096, 64, False),
+                                         (400000, 8, True)])
+def test_route_vocab_inputs_ready_equals_plain(m, N, K, outside):
+    """molora_route_vocab_ex with INPUTS_READY (each token routed before the wait, stored after)
+    gives the oracle's routing and the plain call's outputs and error bits; 400000 tokens is more
+    than one pass of its grid, where the flag has no effect."""
+    g = torch.Generator().manual_seed(11 * N + K)
+    starts = torch.cat([torch.zeros(1, dtype=torch.int32),
+                        torch.sort(torch.randperm(31999, generator=g)[:K - 1] + 1).values.int(),
+                        torch.tensor([32000], dtype=torch.int32)])
+    lo, hi = (-50, 32050) if outside else (0, 32000)
+    tok = torch.randint(lo, hi, (N,), generator=g, dtype=torch.int32)
+    e1, e2 = err_word(), err_word()
+    got = m.molora_route_vocab_ex(dev(tok), dev(starts), m.INPUTS_READY, err_word=e1)
+    plain = m.molora_route_vocab(dev(tok), dev(starts), err_word=e2)
+    torch.cuda.synchronize()
+    ref, n_out = oracle.route_vocab(tok, starts)
+    assert torch.equal(got.cpu(), ref) and torch.equal(plain.cpu(), ref)
+    assert int(e1.item()) == int(e2.item()) and (int(e1.item()) != 0) == (n_out > 0)
+
+
+def test_route_vocab_inputs_ready_bad_ranges(m):
+    starts = torch.tensor([0, 30, 20, 40], dtype=torch.int32)
+    tok = torch.arange(0, 45, dtype=torch.int32)
+    e1, e2 = err_word(), err_word()
+    a1 = m.molora_route_vocab_ex(dev(tok), dev(starts), m.INPUTS_READY, err_word=e1)
+    a2 = m.molora_route_vocab(dev(tok), dev(starts), err_word=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) & m.DEV_BAD_RANGES and int(e1.item()) == int(e2.item())
+    assert torch.equal(a1.cpu(), a2.cpu())
+
+
+def test_inputs_ready_decode_steps_reuse_the_adapter_buffer(m):
+    """Decode-sized steps (batch 160, K = 16) on the scalar path: each step's flagged routing
+    writes the adapter buffer the previous step's apply is still reading, and must store only
+    after it finishes. Every step's y matches the oracle, eagerly and from one captured graph."""
+    wls = [workloads.make("decode_sweep", seed=6060 + i, N=160, K=16) for i in range(3)]
+    adapter = torch.empty(160, dtype=torch.int32, device="cuda")
+    ins = [dict(tok=dev(w.tok), starts=dev(w.starts), x=dev(w.x), A=dev(w.A), B=dev(w.B)) for w in wls]
+    refs = [oracle.lora_apply(w.x, w.A, w.B, oracle.route_vocab(w.tok, w.starts)[0], w.y0, w.scale)[0] for w in wls]
+
+    def steps(ys, e):
+        for i, w in enumerate(wls):
+            m.molora_route_vocab_ex(ins[i]["tok"], ins[i]["starts"], m.INPUTS_READY, adapter=adapter, err_word=e)
+            m.molora_lora_apply(ins[i]["x"], ins[i]["A"], ins[i]["B"], adapter, ys[i], w.scale, err_word=e,
+                                path="scalar")
+
+    e = err_word()
+    ys = [dev(w.y0).clone() for w in wls]
+    steps(ys, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    for y, ref in zip(ys, refs):
+        assert_apply_close(y, ref)
+    s = torch.cuda.Stream()
+    ys = [dev(w.y0).clone() for w in wls]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        steps(ys, e)
+    for y, w in zip(ys, wls):
+        y.copy_(dev(w.y0))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    for y, ref in zip(ys, refs):
+        assert_apply_close(y, ref)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_inputs_ready_steps_reuse_dispatch_buffers(m, path):
     """Back-to-back steps that route into the SAME adapter/counts/offsets/perm buffers: each

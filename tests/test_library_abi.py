@@ -68,6 +68,11 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.molora_route_vocab(fake, 10, fake, 65, fake, None, None) == INVALID
     assert lib.molora_route_vocab(None, 10, fake, 4, fake, None, None) == INVALID
     assert lib.molora_route_vocab(None, 0, None, 4, None, None, None) == 0
+    lib.molora_route_vocab_ex.argtypes = [P, I64, P, I32, P, P, ctypes.c_uint32, P]
+    assert lib.molora_route_vocab_ex(fake, 10, fake, 4, fake, None, 2, None) == INVALID
+    assert lib.molora_route_vocab_ex(fake, 10, fake, 0, fake, None, 1, None) == INVALID
+    assert lib.molora_route_vocab_ex(None, 10, fake, 4, fake, None, 1, None) == INVALID
+    assert lib.molora_route_vocab_ex(None, 0, None, 4, None, None, 1, None) == 0
     # dispatch: k > K, k < 1, K > 64, null outputs
     assert lib.molora_dispatch(fake, 8, 5, 4, fake, fake, fake, None, None) == INVALID
     assert lib.molora_dispatch(fake, 8, 0, 4, fake, fake, fake, None, None) == INVALID
@@ -279,8 +284,9 @@ def test_launching_calls_run_on_the_tensors_device():
     """Every launching binding runs with its tensors' device current (a device guard), so a
     caller whose current device differs still launches where the data lives."""
     import token_adapter_routing_gb300 as m
-    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
-                 "molora_route_vocab_dispatch_ex", "molora_lora_apply", "molora_route_vocab_lora_apply",
+    for name in ("molora_route_vocab", "molora_route_vocab_ex", "molora_router_topk", "molora_dispatch",
+                 "molora_route_vocab_dispatch", "molora_route_vocab_dispatch_ex", "molora_lora_apply",
+                 "molora_route_vocab_lora_apply",
                  "molora_route_vocab_lora_apply_ex", "molora_router_lora_apply",
                  "molora_lora_apply_static_ws", "molora_lora_apply_masked_pass", "molora_selftest_bounded_wait"):
         fn = getattr(m, name)

@@ -48,7 +48,7 @@ INPUTS_READY = 0x1  # molora_route_vocab_dispatch_ex flag
 MAX_ADAPTERS = 64
 ROUTER_HIDDEN = 64
 
-EXPORTED = ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+EXPORTED = ("molora_route_vocab", "molora_route_vocab_ex", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
             "molora_route_vocab_dispatch_ex", "molora_route_vocab_lora_apply_ex",
             "molora_lora_apply", "molora_router_lora_apply", "molora_route_vocab_lora_apply",
             "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
@@ -83,6 +83,7 @@ def load_library(path=None):
     lib = ctypes.CDLL(path)
     P, I64, I32, F, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_int
     lib.molora_route_vocab.argtypes = [P, I64, P, I32, P, P, P]
+    lib.molora_route_vocab_ex.argtypes = [P, I64, P, I32, P, P, ctypes.c_uint32, P]
     lib.molora_router_topk.argtypes = [P, S, I64, I32, P, P, P, P, I32, I32, P, P, P, P]
     lib.molora_dispatch.argtypes = [P, I64, I32, I32, P, P, P, P, P]
     lib.molora_route_vocab_dispatch.argtypes = [P, I64, P, I32, P, P, P, P, P, P]
@@ -106,7 +107,7 @@ def load_library(path=None):
     lib.molora_status_string.restype = ctypes.c_char_p
     lib.molora_version.argtypes = []
     lib.molora_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P]
-    for name in ("molora_route_vocab", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
+    for name in ("molora_route_vocab", "molora_route_vocab_ex", "molora_router_topk", "molora_dispatch", "molora_route_vocab_dispatch",
                  "molora_route_vocab_dispatch_ex", "molora_route_vocab_lora_apply_ex", "molora_lora_apply", "molora_lora_apply_ex", "molora_lora_apply_bf16y", "molora_lora_apply_indirect",
                  "molora_router_lora_apply", "molora_route_vocab_lora_apply", "molora_lora_apply_masked_pass",
                  "molora_select_path", "molora_version", "molora_selftest_bounded_wait",
@@ -257,6 +258,17 @@ def molora_workspace_bytes(N, d_in, d_out, K, r, k, dtype=torch.bfloat16, path="
 @_on_tensor_device
 def molora_route_vocab(tok, starts, adapter=None, err_word=None, stream=None):
     """adapter[t] = a with starts[a] <= tok[t] < starts[a+1], else -1 (int32 [N])."""
+    return _route_vocab(tok, starts, adapter, err_word, stream, None)
+
+
+@_on_tensor_device
+def molora_route_vocab_ex(tok, starts, flags, adapter=None, err_word=None, stream=None):
+    """molora_route_vocab with flags (INPUTS_READY: tok and starts are not written by the kernel
+    enqueued just before, so each token is routed before waiting on it)."""
+    return _route_vocab(tok, starts, adapter, err_word, stream, int(flags))
+
+
+def _route_vocab(tok, starts, adapter, err_word, stream, flags):
     _need(adapter, "adapter", tok.numel())
     _cuda(tok, "tok", torch.int32, 1)
     dev = tok.device
@@ -265,8 +277,11 @@ def molora_route_vocab(tok, starts, adapter=None, err_word=None, stream=None):
     if adapter is None:
         adapter = torch.empty(N, dtype=torch.int32, device=dev)
     _sized(adapter, "adapter", N, torch.int32, dev)
-    _check("molora_route_vocab", load_library().molora_route_vocab(
-        _p(tok), N, _p(starts), K, _p(adapter), _p(_err_word(err_word, dev)), _stream(stream, dev)))
+    args = (_p(tok), N, _p(starts), K, _p(adapter), _p(_err_word(err_word, dev)))
+    if flags is None:
+        _check("molora_route_vocab", load_library().molora_route_vocab(*args, _stream(stream, dev)))
+    else:
+        _check("molora_route_vocab_ex", load_library().molora_route_vocab_ex(*args, flags, _stream(stream, dev)))
     return adapter
 
 

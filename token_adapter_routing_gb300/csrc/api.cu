@@ -146,12 +146,19 @@ using namespace molora;
 
 extern "C" {
 
-molora_status molora_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K, int32_t* adapter,
-                                 int32_t* err_word, cudaStream_t stream) {
+molora_status molora_route_vocab_ex(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
+                                    int32_t* adapter, int32_t* err_word, uint32_t flags, cudaStream_t stream) {
+  if (flags & ~(uint32_t)MOLORA_INPUTS_READY) return MOLORA_ERR_INVALID_ARG;
   if (N < 0 || K < 1 || K > kMaxAdapters) return MOLORA_ERR_INVALID_ARG;
   if (N == 0) return MOLORA_OK;
   if (!tok || !starts || !adapter) return MOLORA_ERR_INVALID_ARG;
-  return launched(launch_route_vocab(tok, N, starts, K, adapter, err_word, stream));
+  const int early = (flags & MOLORA_INPUTS_READY) ? 1 : 0;
+  return launched(launch_route_vocab(tok, N, starts, K, adapter, err_word, early, stream));
+}
+
+molora_status molora_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K, int32_t* adapter,
+                                 int32_t* err_word, cudaStream_t stream) {
+  return molora_route_vocab_ex(tok, N, starts, K, adapter, err_word, 0u, stream);
 }
 
 molora_status molora_router_topk(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,

@@ -17,8 +17,9 @@ struct AdapterTable {
   const void* b[MOLORA_MAX_ADAPTERS];
 };
 
+// early != 0: tok and starts are not written by the preceding kernel (see route_vocab_kernel).
 cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K,
-                               int32_t* adapter, int32_t* err_word, cudaStream_t stream);
+                               int32_t* adapter, int32_t* err_word, int early, cudaStream_t stream);
 
 cudaError_t launch_dispatch(const int32_t* ids, int64_t N, int32_t k, int32_t K, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* err_word, cudaStream_t stream);

@@ -10,24 +10,30 @@
 namespace molora {
 
 // One thread per token; the K+1 range starts sit in shared memory and each token does a
-// binary search for the last start <= its id.
+// binary search for the last start <= its id.  With `early` (the ids and ranges are not written
+// by the kernel before this one, and one pass of the grid covers N), each thread routes its
+// token before waiting on that kernel and stores the result, and any error bit, after it: the
+// kernel before may still read `adapter` (the previous step's routing).
 __global__ void __launch_bounds__(256) route_vocab_kernel(const int32_t* __restrict__ tok, int64_t N,
                                                           const int32_t* __restrict__ starts, int32_t K,
-                                                          int32_t* __restrict__ adapter, int32_t* err_word) {
+                                                          int32_t* __restrict__ adapter, int32_t* err_word,
+                                                          int early) {
   __shared__ int32_t s_starts[kMaxAdapters + 1];
-  pdl_wait();
+  const int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  const bool read_early = early && step >= N;
+  if (!read_early) pdl_wait();
   pdl_launch_dependents();
   for (int i = threadIdx.x; i <= K; i += blockDim.x) s_starts[i] = starts[i];
   __syncthreads();
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  bool bad_ranges = false;
+  if (blockIdx.x == 0 && threadIdx.x == 0)
     for (int a = 0; a < K; ++a)
       if (s_starts[a] >= s_starts[a + 1]) {
-        report(err_word, MOLORA_DEV_BAD_RANGES);
+        bad_ranges = true;
         break;
       }
-  }
-  bool outside = false;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < N; t += (int64_t)gridDim.x * blockDim.x) {
+  auto route = [&](int64_t t, bool& outside) {
     const int32_t v = tok[t];
     int32_t a = -1;
     if (v >= s_starts[0] && v < s_starts[K]) {
@@ -43,16 +49,26 @@ __global__ void __launch_bounds__(256) route_vocab_kernel(const int32_t* __restr
     } else {
       outside = true;
     }
-    adapter[t] = a;
+    return a;
+  };
+  bool outside = false;
+  if (read_early) {
+    const int32_t a = t0 < N ? route(t0, outside) : -1;
+    pdl_wait();
+    if (t0 < N) adapter[t0] = a;
+  } else {
+    for (int64_t t = t0; t < N; t += step) adapter[t] = route(t, outside);
   }
+  if (bad_ranges) report(err_word, MOLORA_DEV_BAD_RANGES);
   if (__any_sync(0xffffffffu, outside) && (threadIdx.x & 31) == 0) report(err_word, MOLORA_DEV_TOKEN_OUTSIDE_RANGES);
 }
 
 cudaError_t launch_route_vocab(const int32_t* tok, int64_t N, const int32_t* starts, int32_t K, int32_t* adapter,
-                               int32_t* err_word, cudaStream_t stream) {
+                               int32_t* err_word, int early, cudaStream_t stream) {
   const int64_t blocks = (N + 255) / 256;
   const int grid = (int)(blocks < 8 * num_sms() ? blocks : 8 * num_sms());
-  return launch_kernel(route_vocab_kernel, dim3(grid), dim3(256), 0, stream, 0, tok, N, starts, K, adapter, err_word);
+  return launch_kernel(route_vocab_kernel, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream, 0, tok, N, starts, K,
+                       adapter, err_word, early);
 }
 
 // ---------------------------------------------------------------------------------------
