@@ -4,6 +4,7 @@
 //     below the crossover a scalar per-token kernel beats the tensor-core kernel), which
 //     also serves fp32 inputs, rank 8 and shapes the grouped tcgen05 path does not take;
 //   * a CUDA-core learned router TopK(g(x)) (Table 1) for fp32 or odd shapes.
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -51,6 +52,11 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 }
 
 constexpr int kScalarThreads = 256;
+// Batches up to this many tokens split each token over a cluster (see lora_scalar_kernel).
+// Measured on GB300, routing + scalar apply at d = 4096, r = 16, K = 16, clusters of 8: 6.3 →
+// 3.8 µs at 1 token, 7.1 → 4.6 at 32, 8.0 → 6.9 at 96; from 128 tokens the clusters no longer
+// fit one wave and it loses (9.0 → 10.8).
+constexpr int64_t kScalarSplitMaxTokens = 96;
 
 // y element access: fp32, or bf16 (the fp32 sum rounded to nearest even once per update).
 __device__ __forceinline__ void y_add4(float* p, const float (&a)[4]) {
@@ -79,12 +85,19 @@ __device__ __forceinline__ void y_add1(__nv_bfloat16* p, float a) {
 // g_j = scale * w_j * h.  Phase 2: each thread owns 4 output columns and accumulates
 // sum_j sum_q g_j[q] B_a[q, c..c+3] in registers, then updates y once.  Every y element is
 // read and written exactly once whatever k is, so the result is deterministic.
-template <typename T, typename YT, int R>
+//
+// kSplit (small batches): a cluster of `split` CTAs per token instead, CTA c taking the rows
+// [c d_in / split, (c+1) d_in / split) of the shrink and the columns [c d_out / split, ...) of
+// the expand.  Each CTA stores its partial h into slot c of every CTA of the cluster (after a
+// cluster barrier that every CTA has started), and after a second one adds the slots in rank
+// order, so all agree bit for bit.  A token's shrink chain is then `split` times shorter,
+// which is what a decode step at small batch waits on.
+template <typename T, typename YT, int R, bool kSplit>
 __global__ void __launch_bounds__(kScalarThreads)
     lora_scalar_kernel(const T* __restrict__ x, int32_t d_in, int32_t d_out, const T* __restrict__ A,
                        const T* __restrict__ B, int32_t K, const int32_t* __restrict__ ids,
                        const float* __restrict__ w, int32_t k, float scale, YT* __restrict__ y,
-                       int32_t cols_per_split, int32_t mask_adapter, int32_t* err_word, int32_t indirect,
+                       int32_t split_param, int32_t mask_adapter, int32_t* err_word, int32_t indirect,
                        const __grid_constant__ AdapterTable table) {
   using C16 = Chunk16<T>;
   constexpr int VEC = C16::kVec;
@@ -93,13 +106,21 @@ __global__ void __launch_bounds__(kScalarThreads)
   extern __shared__ float smem[];
   float* g = smem;                 // [k][R]
   float* red = smem + k * R;       // [8 warps][R]
-  int32_t* s_adapter = reinterpret_cast<int32_t*>(red + (kScalarThreads / 32) * R);  // [k]
+  // kSplit: split_param CTAs per token, their partials [split][k][R]; else the columns per CTA
+  const int csplit = kSplit ? split_param : 1;
+  float* part = red + (kScalarThreads / 32) * R;
+  int32_t* s_adapter = reinterpret_cast<int32_t*>(kSplit ? part + csplit * k * R : part);  // [k]
 
-  const int64_t t = blockIdx.x;
+  const int64_t t = kSplit ? (int64_t)(blockIdx.x / (unsigned)csplit) : (int64_t)blockIdx.x;
+  const int crank = kSplit ? (int)(blockIdx.x % (unsigned)csplit) : 0;  // == %cluster_ctarank
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t r_begin = kSplit ? (int32_t)((int64_t)d_in * crank / csplit) : 0;
+  const int32_t r_end = kSplit ? (int32_t)((int64_t)d_in * (crank + 1) / csplit) : d_in;
   const T* xr = x + t * (int64_t)d_in;
+  if constexpr (kSplit) cluster_arrive();  // a peer's shared memory is written only once all have started
   pdl_wait();
   pdl_launch_dependents();
+  if constexpr (kSplit) cluster_wait();
 
   for (int j = 0; j < k; ++j) {
     int32_t a;
@@ -123,9 +144,9 @@ __global__ void __launch_bounds__(kScalarThreads)
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
     const T* Aa = indirect ? static_cast<const T*>(table.a[a]) : A + (int64_t)a * d_in * R;
-    const int64_t nchunks = (int64_t)d_in * CPR;
+    const int64_t nchunks = (int64_t)r_end * CPR;
 #pragma unroll 4
-    for (int64_t c = tid; c < nchunks; c += kScalarThreads) {
+    for (int64_t c = (int64_t)r_begin * CPR + tid; c < nchunks; c += kScalarThreads) {
       const float xv = to_f(xr[c / CPR]);
       float av[VEC];
       C16::load(Aa + c * VEC, av);
@@ -145,15 +166,33 @@ __global__ void __launch_bounds__(kScalarThreads)
       float h = 0.f;
 #pragma unroll
       for (int q = 0; q < kScalarThreads / 32; ++q) h += red[q * R + tid];
-      g[j * R + tid] = scale * wj * h;
+      if constexpr (kSplit) {
+        // this rank's partial sum, into slot crank of every CTA of the cluster
+        const uint32_t local = smem_u32(part + (crank * k + j) * R + tid);
+        for (int p = 0; p < csplit; ++p) st_cluster_f32(dsmem_addr(local, (uint32_t)p), h);
+        g[j * R + tid] = scale * wj;  // the weight, until the partials are in
+      } else {
+        g[j * R + tid] = scale * wj * h;
+      }
     }
     if (tid == 0) s_adapter[j] = a;
     __syncthreads();
   }
+  if constexpr (kSplit) {
+    // every rank's partials are in every CTA (the barrier orders the remote stores); nothing is
+    // read or written remotely after it, so a CTA may leave whenever it is done
+    cluster_sync();
+    for (int i = tid; i < k * R; i += kScalarThreads) {
+      if (s_adapter[i / R] < 0) continue;
+      float h = 0.f;
+      for (int p = 0; p < csplit; ++p) h += part[p * k * R + i];
+      g[i] *= h;
+    }
+  }
   __syncthreads();
 
-  const int32_t c_begin = blockIdx.y * cols_per_split;
-  const int32_t c_end = min(d_out, c_begin + cols_per_split);
+  const int32_t c_begin = kSplit ? (int32_t)((int64_t)d_out * crank / csplit) : (int32_t)blockIdx.y * split_param;
+  const int32_t c_end = kSplit ? (int32_t)((int64_t)d_out * (crank + 1) / csplit) : min(d_out, c_begin + split_param);
   YT* yr = y + t * (int64_t)d_out;
   if ((d_out & 3) == 0) {
     for (int32_t c = c_begin + 4 * tid; c < c_end; c += 4 * kScalarThreads) {
@@ -188,22 +227,61 @@ __global__ void __launch_bounds__(kScalarThreads)
   }
 }
 
+template <typename T, typename YT, int R>
+static cudaError_t launch_scalar_r(dim3 grid, size_t smem, int cluster, bool split, cudaStream_t stream,
+                                   const T* xp, int32_t d_in, int32_t d_out, const T* Ap, const T* Bp, int32_t K,
+                                   const int32_t* ids, const float* w, int32_t k, float scale, YT* yp,
+                                   int32_t split_param, int32_t mask_adapter, int32_t* err_word, int32_t ind,
+                                   const AdapterTable& tab) {
+  if (split)
+    return launch_kernel(lora_scalar_kernel<T, YT, R, true>, grid, dim3(kScalarThreads), smem, stream, cluster, xp,
+                         d_in, d_out, Ap, Bp, K, ids, w, k, scale, yp, split_param, mask_adapter, err_word, ind, tab);
+  return launch_kernel(lora_scalar_kernel<T, YT, R, false>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
+                       d_out, Ap, Bp, K, ids, w, k, scale, yp, split_param, mask_adapter, err_word, ind, tab);
+}
+
 template <typename T, typename YT>
 static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32_t d_out, const void* A,
                                    const void* B, int32_t K, int32_t r, const int32_t* ids, const float* w,
                                    int32_t k, float scale, void* y, int32_t mask_adapter, int32_t* err_word,
                                    cudaStream_t stream, const AdapterTable* table) {
-  // Enough CTAs to cover the GPU twice: small batches split the output columns (each split
-  // recomputes the token's cheap shrink).
-  const int64_t want = 2 * (int64_t)num_sms();
-  int64_t splits = N >= want ? 1 : (want + N - 1) / N;
-  const int64_t max_splits = d_out >= 512 ? d_out / 512 : 1;
-  if (splits > max_splits) splits = max_splits;
-  int32_t cols = (int32_t)((d_out + splits - 1) / splits);
-  cols = (cols + 3) & ~3;
-  splits = (d_out + cols - 1) / cols;
-  const size_t smem = sizeof(float) * ((size_t)k * r + (kScalarThreads / 32) * r) + sizeof(int32_t) * k;
-  dim3 grid((unsigned)N, (unsigned)splits);
+  const size_t base_smem = sizeof(float) * ((size_t)k * r + (kScalarThreads / 32) * r) + sizeof(int32_t) * k;
+  // Small batches: a cluster of C CTAs per token splits d_in for the shrink (C times shorter a
+  // chain) and d_out for the expand.  The widest C with row and column splits that keep 4-column
+  // groups aligned, at least 256 rows and columns per CTA, and the shared memory within 48 KB.
+  int64_t split_max = kScalarSplitMaxTokens;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_SCALAR_SPLIT_MAX")) split_max = atoi(e);
+#endif
+  int csplit = 1;
+  if (N <= split_max)
+    for (int c : {8, 4, 2}) {
+      if (d_in % c == 0 && d_out % (4 * c) == 0 && d_in / c >= 256 && d_out / c >= 256 &&
+          base_smem + sizeof(float) * (size_t)c * k * r <= 48 * 1024) {
+        csplit = c;
+        break;
+      }
+    }
+  dim3 grid;
+  size_t smem = base_smem;
+  int32_t split_param;
+  if (csplit > 1) {
+    grid = dim3((unsigned)(N * csplit));
+    smem += sizeof(float) * (size_t)csplit * k * r;
+    split_param = csplit;
+  } else {
+    // Enough CTAs to cover the GPU twice: other batches split the output columns (each split
+    // recomputes the token's shrink).
+    const int64_t want = 2 * (int64_t)num_sms();
+    int64_t splits = N >= want ? 1 : (want + N - 1) / N;
+    const int64_t max_splits = d_out >= 512 ? d_out / 512 : 1;
+    if (splits > max_splits) splits = max_splits;
+    int32_t cols = (int32_t)((d_out + splits - 1) / splits);
+    cols = (cols + 3) & ~3;
+    splits = (d_out + cols - 1) / cols;
+    grid = dim3((unsigned)N, (unsigned)splits);
+    split_param = cols;
+  }
   const T* xp = static_cast<const T*>(x);
   const T* Ap = static_cast<const T*>(A);
   const T* Bp = static_cast<const T*>(B);
@@ -212,19 +290,20 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
   memset(&tab, 0, sizeof(tab));
   if (table) tab = *table;
   const int32_t ind = table ? 1 : 0;
+  const bool split = csplit > 1;
   switch (r) {
     case 8:
-      return launch_kernel(lora_scalar_kernel<T, YT, 8>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
+      return launch_scalar_r<T, YT, 8>(grid, smem, csplit, split, stream, xp, d_in, d_out, Ap, Bp, K, ids, w, k, scale,
+                                       yp, split_param, mask_adapter, err_word, ind, tab);
     case 16:
-      return launch_kernel(lora_scalar_kernel<T, YT, 16>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
+      return launch_scalar_r<T, YT, 16>(grid, smem, csplit, split, stream, xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                        scale, yp, split_param, mask_adapter, err_word, ind, tab);
     case 32:
-      return launch_kernel(lora_scalar_kernel<T, YT, 32>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
+      return launch_scalar_r<T, YT, 32>(grid, smem, csplit, split, stream, xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                        scale, yp, split_param, mask_adapter, err_word, ind, tab);
     case 64:
-      return launch_kernel(lora_scalar_kernel<T, YT, 64>, grid, dim3(kScalarThreads), smem, stream, 0, xp, d_in,
-                           d_out, Ap, Bp, K, ids, w, k, scale, yp, cols, mask_adapter, err_word, ind, tab);
+      return launch_scalar_r<T, YT, 64>(grid, smem, csplit, split, stream, xp, d_in, d_out, Ap, Bp, K, ids, w, k,
+                                        scale, yp, split_param, mask_adapter, err_word, ind, tab);
     default:
       return cudaErrorInvalidValue;
   }
