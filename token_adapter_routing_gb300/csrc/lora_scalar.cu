@@ -52,11 +52,12 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 }
 
 constexpr int kScalarThreads = 256;
-// Batches up to this many tokens split each token over a cluster (see lora_scalar_kernel).
-// Measured on GB300, routing + scalar apply at d = 4096, r = 16, K = 16, clusters of 8: 6.3 →
-// 3.8 µs at 1 token, 7.1 → 4.6 at 32, 8.0 → 6.9 at 96; from 128 tokens the clusters no longer
-// fit one wave and it loses (9.0 → 10.8).
-constexpr int64_t kScalarSplitMaxTokens = 96;
+// Small batches split each token over a cluster of C CTAs (see lora_scalar_kernel): the widest
+// C in {8, 4, 2} with N * C <= this many CTAs.  Measured on GB300, routing + scalar apply at
+// d = 4096, r = 16, K = 16: the fastest width at each batch kept the grid near 256-384 CTAs
+// (C = 8 at 1-32 tokens: 6.3 -> 3.8 us at 1; C = 4 at 96: 7.9 -> 5.7; C = 2 at 128 and 160:
+// 9.0 -> 7.1 and 7.9), and from 256 tokens no split was fastest.
+constexpr int64_t kScalarSplitCtas = 384;
 
 // y element access: fp32, or bf16 (the fp32 sum rounded to nearest even once per update).
 __device__ __forceinline__ void y_add4(float* p, const float (&a)[4]) {
@@ -247,21 +248,26 @@ static cudaError_t launch_scalar_t(const void* x, int64_t N, int32_t d_in, int32
                                    cudaStream_t stream, const AdapterTable* table) {
   const size_t base_smem = sizeof(float) * ((size_t)k * r + (kScalarThreads / 32) * r) + sizeof(int32_t) * k;
   // Small batches: a cluster of C CTAs per token splits d_in for the shrink (C times shorter a
-  // chain) and d_out for the expand.  The widest C with row and column splits that keep 4-column
-  // groups aligned, at least 256 rows and columns per CTA, and the shared memory within 48 KB.
-  int64_t split_max = kScalarSplitMaxTokens;
+  // chain) and d_out for the expand.  The widest C within the CTA budget, with row and column
+  // splits that keep 4-column groups aligned, at least 256 rows and columns per CTA, and the
+  // shared memory within 48 KB.
+  int64_t split_ctas = kScalarSplitCtas;
 #ifdef MOLORA_TUNING_ENV
-  if (const char* e = getenv("MOLORA_SCALAR_SPLIT_MAX")) split_max = atoi(e);
+  if (const char* e = getenv("MOLORA_SCALAR_SPLIT_CTAS")) split_ctas = atoi(e);
 #endif
   int csplit = 1;
-  if (N <= split_max)
-    for (int c : {8, 4, 2}) {
-      if (d_in % c == 0 && d_out % (4 * c) == 0 && d_in / c >= 256 && d_out / c >= 256 &&
-          base_smem + sizeof(float) * (size_t)c * k * r <= 48 * 1024) {
-        csplit = c;
-        break;
-      }
+  int only_c = 0;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_SCALAR_SPLIT_C")) only_c = atoi(e);
+#endif
+  for (int c : {8, 4, 2}) {
+    if (only_c && c != only_c) continue;
+    if (N * c <= split_ctas && d_in % c == 0 && d_out % (4 * c) == 0 && d_in / c >= 256 && d_out / c >= 256 &&
+        base_smem + sizeof(float) * (size_t)c * k * r <= 48 * 1024) {
+      csplit = c;
+      break;
     }
+  }
   dim3 grid;
   size_t smem = base_smem;
   int32_t split_param;
