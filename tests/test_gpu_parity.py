@@ -466,6 +466,32 @@ def test_scalar_decode_sizes_small_integers_bitexact(m, N, d_in, d_out, K, r, k)
     assert torch.equal(ys[0], y_ref) and torch.equal(ys[1], y_ref)
 
 
+@pytest.mark.parametrize("N,k", [(1, 1), (40, 2), (96, 1)])
+def test_scalar_split_bf16y_small_integers_bitexact(m, N, k):
+    """bf16 y on the scalar path at batch sizes where each token is split over a cluster (8 CTAs
+    at 1 and 40 tokens, 4 at 96): every value is a small integer, exact in fp32 and in bf16, so
+    y equals the oracle's result rounded once to bf16, bit for bit."""
+    d_in, d_out, K, r = 4096, 4096, 8, 16
+    g = torch.Generator().manual_seed(171 + N + k)
+    x = torch.randint(-3, 4, (N, d_in), generator=g).to(torch.bfloat16)
+    A = torch.zeros(K, d_in, r)
+    for a_ in range(K):
+        for q in range(r):
+            rows = torch.randperm(d_in, generator=g)[:2]
+            A[a_, rows, q] = torch.where(torch.rand(2, generator=g) < 0.5, -1.0, 1.0)
+    A = A.to(torch.bfloat16)
+    B = torch.randint(-1, 2, (K, r, d_out), generator=g).to(torch.bfloat16)
+    y0b = torch.randint(-8, 9, (N, d_out), generator=g).to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(K, generator=g)[:k] for _ in range(N)]).to(torch.int32)
+    w = torch.ones(N, k)
+    y = dev(y0b).clone()
+    m.molora_lora_apply(dev(x), dev(A), dev(B), dev(ids), y, 1.0, w=dev(w), path="scalar")
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.lora_apply(x, A, B, ids, y0b.float(), 1.0, w)
+    assert y_ref.abs().max().item() < 256
+    assert torch.equal(y.cpu(), y_ref.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("N,d,K,r,k,dtype", [(100, 4096, 16, 16, 2, torch.bfloat16), (200, 4096, 16, 16, 1, torch.bfloat16),
                                              (50, 2048, 4, 16, 1, torch.float32), (9, 4096, 4, 64, 3, torch.bfloat16)])
 def test_scalar_decode_sizes_vs_oracle(m, N, d, K, r, k, dtype):
