@@ -331,16 +331,18 @@ cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int
 }
 
 // ---------------------------------------------------------------------------------------
-// CUDA-core router (fp32 x, or shapes the tensor-core router does not take).  A CTA owns 16
-// tokens and all 64 hidden units: d_in is walked in chunks of 64, each chunk of x [16 x 64]
-// and W1 [64 x 64] staged in shared memory (two buffers; the next chunk's global loads are in
-// flight in registers while the current one is multiplied), and thread (q, u) accumulates
-// token q's hidden units 4u..4u+3 in order over d_in.  Then ReLU, the 64 x K second layer, and
-// one thread per token selects the top k (strictly greater wins, so equal logits keep the
-// lower index) and renormalises the softmax over the selected k.
-constexpr int kRouterTok = 16;
-constexpr int kRouterChunk = 64;
+// CUDA-core router (fp32 x, or shapes the tensor-core router does not take).  A CTA owns 32
+// tokens and all 64 hidden units: d_in is walked in chunks of 32, each chunk of x (stored
+// transposed, [32 inputs][32 tokens]) and W1 [32 x 64] staged in shared memory (two buffers; the
+// next chunk's global loads are in flight in registers while the current one is multiplied).
+// Thread (q, u) accumulates tokens 2q and 2q+1, hidden units 4u..4u+3, in order over d_in: one
+// float2 and one float4 shared-memory load per 8 FMAs.  Then ReLU, the 64 x K second layer, and
+// one thread per token selects the top k (strictly greater wins, so equal logits keep the lower
+// index) and renormalises the softmax over the selected k.
+constexpr int kRouterTok = 32;
+constexpr int kRouterChunk = 32;
 constexpr int kRouterThreads = 256;
+constexpr int kRouterXPad = kRouterTok + 2;  // x rows: 8-byte aligned, stores 2-way at most
 
 template <typename T>
 __global__ void __launch_bounds__(kRouterThreads)
@@ -348,15 +350,12 @@ __global__ void __launch_bounds__(kRouterThreads)
                          const float* __restrict__ b1, const T* __restrict__ W2, const float* __restrict__ b2,
                          int32_t K, int32_t k, float* __restrict__ logits, int32_t* __restrict__ ids,
                          float* __restrict__ w) {
-  __shared__ float xs[2][kRouterTok][kRouterChunk + 1];
+  __shared__ __align__(16) float xs[2][kRouterChunk][kRouterXPad];
   __shared__ __align__(16) float ws[2][kRouterChunk][kRouterHidden];
-  // after the main loop the W1 buffers hold the hidden units and the logits
-  float(*hid)[kRouterHidden + 1] = reinterpret_cast<float(*)[kRouterHidden + 1]>(&ws[0][0][0]);
-  float(*lg)[kMaxAdapters] = reinterpret_cast<float(*)[kMaxAdapters]>(&ws[1][0][0]);
-  static_assert(kRouterTok * (kRouterHidden + 1) <= kRouterChunk * kRouterHidden, "hidden units fit a W1 buffer");
-  static_assert(kRouterTok * kMaxAdapters <= kRouterChunk * kRouterHidden, "logits fit a W1 buffer");
+  __shared__ float hid[kRouterTok][kRouterHidden + 1];
+  __shared__ float lg[kRouterTok][kMaxAdapters];
   constexpr int kXPer = kRouterTok * kRouterChunk / kRouterThreads;     // 4 x elements per thread
-  constexpr int kWPer = kRouterChunk * kRouterHidden / kRouterThreads;  // 16 W1 elements per thread
+  constexpr int kWPer = kRouterChunk * kRouterHidden / kRouterThreads;  // 8 W1 elements per thread
   const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
   const int tid = threadIdx.x, tq = tid >> 4, tu = tid & 15;
   pdl_wait();
@@ -379,7 +378,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 #pragma unroll
     for (int e = 0; e < kXPer; ++e) {
       const int idx = tid + e * kRouterThreads;
-      xs[b][idx / kRouterChunk][idx % kRouterChunk] = rx[e];
+      xs[b][idx % kRouterChunk][idx / kRouterChunk] = rx[e];
     }
 #pragma unroll
     for (int e = 0; e < kWPer; ++e) {
@@ -387,7 +386,7 @@ __global__ void __launch_bounds__(kRouterThreads)
       ws[b][idx / kRouterHidden][idx % kRouterHidden] = rw[e];
     }
   };
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   const int nch = (d_in + kRouterChunk - 1) / kRouterChunk;
   gload(0);
   sstore(0);
@@ -397,21 +396,27 @@ __global__ void __launch_bounds__(kRouterThreads)
     if (c + 1 < nch) gload(c + 1);
 #pragma unroll 8
     for (int ii = 0; ii < kRouterChunk; ++ii) {
-      const float a = xs[b][tq][ii];
+      const float2 a = *reinterpret_cast<const float2*>(&xs[b][ii][2 * tq]);
       const float4 wv = *reinterpret_cast<const float4*>(&ws[b][ii][4 * tu]);
-      acc[0] = fmaf(a, wv.x, acc[0]);
-      acc[1] = fmaf(a, wv.y, acc[1]);
-      acc[2] = fmaf(a, wv.z, acc[2]);
-      acc[3] = fmaf(a, wv.w, acc[3]);
+      acc[0][0] = fmaf(a.x, wv.x, acc[0][0]);
+      acc[0][1] = fmaf(a.x, wv.y, acc[0][1]);
+      acc[0][2] = fmaf(a.x, wv.z, acc[0][2]);
+      acc[0][3] = fmaf(a.x, wv.w, acc[0][3]);
+      acc[1][0] = fmaf(a.y, wv.x, acc[1][0]);
+      acc[1][1] = fmaf(a.y, wv.y, acc[1][1]);
+      acc[1][2] = fmaf(a.y, wv.z, acc[1][2]);
+      acc[1][3] = fmaf(a.y, wv.w, acc[1][3]);
     }
     if (c + 1 < nch) sstore(b ^ 1);  // buffer b^1 was last read before the previous barrier
     __syncthreads();
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float h = acc[j] + (b1 ? b1[4 * tu + j] : 0.f);
-    hid[tq][4 * tu + j] = h > 0.f ? h : 0.f;
-  }
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float h = acc[i][j] + (b1 ? b1[4 * tu + j] : 0.f);
+      hid[2 * tq + i][4 * tu + j] = h > 0.f ? h : 0.f;
+    }
   __syncthreads();
   for (int idx = tid; idx < kRouterTok * K; idx += kRouterThreads) {
     const int q = idx / K, a = idx % K;
