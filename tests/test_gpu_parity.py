@@ -1011,8 +1011,13 @@ def test_router_topk_vs_oracle(m, name, kw, k):
     check_router(wl, k, logits, ids, w)
 
 
-def test_router_fp32_and_biases(m):
-    wl = workloads.make("topk_mlp", N=200, d_in=96, dtype=torch.float32, k=2)
+@pytest.mark.parametrize("N,d_in", [(200, 96),     # d_in under 4 chunks: one CTA per tile
+                                     (1000, 1000),  # a cluster of 4 per tile, ragged chunk and tile
+                                     (77, 160),     # 5 chunks over 4 ranks: the last rank has none
+                                     (4099, 2048),  # 129 tiles, each split over 4 CTAs
+                                     (8000, 256)])  # 250 tiles: past the split's CTA budget
+def test_router_fp32_and_biases(m, N, d_in):
+    wl = workloads.make("topk_mlp", N=N, d_in=d_in, d_out=256, dtype=torch.float32, k=2)
     g = torch.Generator().manual_seed(3)
     b1 = torch.randn(64, generator=g) * 0.1
     b2 = torch.randn(wl.K, generator=g) * 0.1

@@ -332,104 +332,188 @@ cudaError_t launch_lora_scalar(const void* x, molora_dtype dtype, int64_t N, int
 
 // ---------------------------------------------------------------------------------------
 // CUDA-core router (fp32 x, or shapes the tensor-core router does not take).  A CTA owns 32
-// tokens and all 64 hidden units: d_in is walked in chunks of 32, each chunk of x (stored
-// transposed, [32 inputs][32 tokens]) and W1 [32 x 64] staged in shared memory (two buffers; the
-// next chunk's global loads are in flight in registers while the current one is multiplied).
-// Thread (q, u) accumulates tokens 2q and 2q+1, hidden units 4u..4u+3, in order over d_in: one
-// float2 and one float4 shared-memory load per 8 FMAs.  Then ReLU, the 64 x K second layer, and
-// one thread per token selects the top k (strictly greater wins, so equal logits keep the lower
-// index) and renormalises the softmax over the selected k.
+// tokens and all 64 hidden units: d_in is walked in chunks of 32, each chunk of x (token-major,
+// [32 tokens][32 inputs], rows padded to 36 floats) and of W1 ([32 inputs][64 units]) staged in
+// shared memory (two buffers; the next chunk's global loads are in flight in registers while the
+// current one is multiplied).  Thread (tq, tu) accumulates tokens tq, tq+8, tq+16, tq+24 and
+// hidden units 4tu..4tu+3, in order over d_in.  A warp spans 4 consecutive tq and 8 consecutive
+// tu, so per 4 inputs it reads 4 float4 of x (rows 36 floats apart: distinct banks) and 4 float4
+// of W1 (128 contiguous bytes): two shared-memory wavefronts per 16 FMAs of each thread.  Then
+// ReLU, the 64 x K second layer, and one thread per token selects the top k (strictly greater
+// wins, so equal logits keep the lower index) and renormalises the softmax over the selected k.
 constexpr int kRouterTok = 32;
 constexpr int kRouterChunk = 32;
-constexpr int kRouterThreads = 256;
-constexpr int kRouterXPad = kRouterTok + 2;  // x rows: 8-byte aligned, stores 2-way at most
+constexpr int kRouterThreads = 128;
+constexpr int kRouterXPad = kRouterChunk + 4;  // x rows: float4-aligned, 4 banks apart
+// kSplit: a cluster of kRouterSplit CTAs per 32-token tile, CTA c taking a contiguous quarter
+// of d_in (in whole chunks).  CTA j owns tokens 8j..8j+7 of the tile -- the tokens tq + 8j of
+// every thread -- and the others push their partial hidden sums for those tokens into its slots
+// in distributed shared memory; after one cluster barrier the owner adds the slots in rank order
+// (so the result does not depend on timing), then runs the second layer and the top k for its
+// tokens.  Four times the CTAs of the unsplit kernel, for the occupancy a 32-token tile alone
+// cannot give.
+constexpr int kRouterSplit = 4;
+constexpr int kRouterOwn = kRouterTok / kRouterSplit;  // tokens each CTA of a cluster finishes
 
-template <typename T>
+// 4 consecutive elements of T as floats: one 16-byte (fp32) or 8-byte (bf16) load when vec (the
+// caller has checked alignment and that all 4 lie inside the row), else element by element up
+// to n (zero past it).
+__device__ __forceinline__ float4 load4(const float* p, bool vec, int n) {
+  if (vec) return __ldg(reinterpret_cast<const float4*>(p));
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n > 0) v.x = p[0];
+  if (n > 1) v.y = p[1];
+  if (n > 2) v.z = p[2];
+  if (n > 3) v.w = p[3];
+  return v;
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p, bool vec, int n) {
+  if (vec) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u), __uint_as_float(q.y << 16),
+                       __uint_as_float(q.y & 0xFFFF0000u));
+  }
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n > 0) v.x = to_f(p[0]);
+  if (n > 1) v.y = to_f(p[1]);
+  if (n > 2) v.z = to_f(p[2]);
+  if (n > 3) v.w = to_f(p[3]);
+  return v;
+}
+
+template <typename T, bool kSplit>
 __global__ void __launch_bounds__(kRouterThreads)
     router_scalar_kernel(const T* __restrict__ x, int64_t N, int32_t d_in, const T* __restrict__ W1,
                          const float* __restrict__ b1, const T* __restrict__ W2, const float* __restrict__ b2,
                          int32_t K, int32_t k, float* __restrict__ logits, int32_t* __restrict__ ids,
-                         float* __restrict__ w) {
-  __shared__ __align__(16) float xs[2][kRouterChunk][kRouterXPad];
+                         float* __restrict__ w, int vec) {
+  __shared__ __align__(16) float xs[2][kRouterTok][kRouterXPad];
   __shared__ __align__(16) float ws[2][kRouterChunk][kRouterHidden];
-  __shared__ float hid[kRouterTok][kRouterHidden + 1];
-  __shared__ float lg[kRouterTok][kMaxAdapters];
-  constexpr int kXPer = kRouterTok * kRouterChunk / kRouterThreads;     // 4 x elements per thread
-  constexpr int kWPer = kRouterChunk * kRouterHidden / kRouterThreads;  // 8 W1 elements per thread
-  const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
-  const int tid = threadIdx.x, tq = tid >> 4, tu = tid & 15;
+  // the hidden units and logits of the tokens this CTA finishes (all 32, or its block of 8)
+  __shared__ float hid[kSplit ? kRouterOwn : kRouterTok][kRouterHidden + 1];
+  __shared__ float lg[kSplit ? kRouterOwn : kRouterTok][kMaxAdapters];
+  // kSplit: slots[rank][token of this CTA's block][hidden unit] (kRouterSplit x 8 x 65 floats).
+  // Not aliased with the staging buffers: a peer may push while this CTA still multiplies.
+  __shared__ float slots[kSplit ? kRouterSplit : 1][kRouterOwn][kRouterHidden + 1];
+  constexpr int kXG = kRouterChunk / 4, kWG = kRouterHidden / 4;      // float4 groups per row
+  constexpr int kXPer = kRouterTok * kXG / kRouterThreads;            // 2 groups of x per thread
+  constexpr int kWPer = kRouterChunk * kWG / kRouterThreads;          // 4 groups of W1 per thread
+  const int crank = kSplit ? (int)(blockIdx.x % (unsigned)kRouterSplit) : 0;  // == %cluster_ctarank
+  const int64_t t0 = (int64_t)(kSplit ? blockIdx.x / (unsigned)kRouterSplit : blockIdx.x) * kRouterTok;
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int tq = (wi & 1) * 4 + (lane >> 3), tu = (wi >> 1) * 8 + (lane & 7);
+  // this CTA's rows of d_in: whole chunks, a contiguous share per rank
+  const int nch_all = (d_in + kRouterChunk - 1) / kRouterChunk;
+  const int per_rank = (nch_all + kRouterSplit - 1) / kRouterSplit;
+  const int c_lo = kSplit ? min(nch_all, crank * per_rank) : 0;
+  const int c_hi = kSplit ? min(nch_all, c_lo + per_rank) : nch_all;
+  const bool v4 = vec != 0;
+  if constexpr (kSplit) cluster_arrive();  // a peer's shared memory is written only once all have started
   pdl_wait();
   pdl_launch_dependents();
-  float rx[kXPer], rw[kWPer];
+  if constexpr (kSplit) cluster_wait();
+  float4 rx[kXPer], rw[kWPer];
   auto gload = [&](int c) {  // chunk c of x and W1 into registers (zero past the ends)
     const int i0 = c * kRouterChunk;
 #pragma unroll
     for (int e = 0; e < kXPer; ++e) {
-      const int idx = tid + e * kRouterThreads, q = idx / kRouterChunk, ii = idx % kRouterChunk;
-      rx[e] = (t0 + q < N && i0 + ii < d_in) ? to_f(x[(t0 + q) * d_in + i0 + ii]) : 0.f;
+      const int idx = tid + e * kRouterThreads, q = idx / kXG, i = i0 + 4 * (idx % kXG);
+      rx[e] = (t0 + q < N && i < d_in) ? load4(x + (t0 + q) * d_in + i, v4, d_in - i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int e = 0; e < kWPer; ++e) {
-      const int idx = tid + e * kRouterThreads, ii = idx / kRouterHidden, u = idx % kRouterHidden;
-      rw[e] = i0 + ii < d_in ? to_f(W1[(int64_t)(i0 + ii) * kRouterHidden + u]) : 0.f;
+      const int idx = tid + e * kRouterThreads, ii = idx / kWG, u = 4 * (idx % kWG);
+      rw[e] = i0 + ii < d_in ? load4(W1 + (int64_t)(i0 + ii) * kRouterHidden + u, v4, 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
   auto sstore = [&](int b) {
 #pragma unroll
     for (int e = 0; e < kXPer; ++e) {
       const int idx = tid + e * kRouterThreads;
-      xs[b][idx % kRouterChunk][idx / kRouterChunk] = rx[e];
+      *reinterpret_cast<float4*>(&xs[b][idx / kXG][4 * (idx % kXG)]) = rx[e];
     }
 #pragma unroll
     for (int e = 0; e < kWPer; ++e) {
       const int idx = tid + e * kRouterThreads;
-      ws[b][idx / kRouterHidden][idx % kRouterHidden] = rw[e];
+      *reinterpret_cast<float4*>(&ws[b][idx / kWG][4 * (idx % kWG)]) = rw[e];
     }
   };
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  const int nch = (d_in + kRouterChunk - 1) / kRouterChunk;
-  gload(0);
-  sstore(0);
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  if (c_lo < c_hi) {
+    gload(c_lo);
+    sstore(0);
+  }
   __syncthreads();
-  for (int c = 0; c < nch; ++c) {
-    const int b = c & 1;
-    if (c + 1 < nch) gload(c + 1);
-#pragma unroll 8
-    for (int ii = 0; ii < kRouterChunk; ++ii) {
-      const float2 a = *reinterpret_cast<const float2*>(&xs[b][ii][2 * tq]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[b][ii][4 * tu]);
-      acc[0][0] = fmaf(a.x, wv.x, acc[0][0]);
-      acc[0][1] = fmaf(a.x, wv.y, acc[0][1]);
-      acc[0][2] = fmaf(a.x, wv.z, acc[0][2]);
-      acc[0][3] = fmaf(a.x, wv.w, acc[0][3]);
-      acc[1][0] = fmaf(a.y, wv.x, acc[1][0]);
-      acc[1][1] = fmaf(a.y, wv.y, acc[1][1]);
-      acc[1][2] = fmaf(a.y, wv.z, acc[1][2]);
-      acc[1][3] = fmaf(a.y, wv.w, acc[1][3]);
+  for (int c = c_lo; c < c_hi; ++c) {
+    const int b = (c - c_lo) & 1;
+    if (c + 1 < c_hi) gload(c + 1);
+#pragma unroll 2
+    for (int ii = 0; ii < kRouterChunk; ii += 4) {
+      float4 xv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xv[j] = *reinterpret_cast<const float4*>(&xs[b][tq + 8 * j][ii]);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const float4 wv = *reinterpret_cast<const float4*>(&ws[b][ii + s][4 * tu]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = s == 0 ? xv[j].x : s == 1 ? xv[j].y : s == 2 ? xv[j].z : xv[j].w;
+          acc[j][0] = fmaf(a, wv.x, acc[j][0]);
+          acc[j][1] = fmaf(a, wv.y, acc[j][1]);
+          acc[j][2] = fmaf(a, wv.z, acc[j][2]);
+          acc[j][3] = fmaf(a, wv.w, acc[j][3]);
+        }
+      }
     }
-    if (c + 1 < nch) sstore(b ^ 1);  // buffer b^1 was last read before the previous barrier
+    if (c + 1 < c_hi) sstore(b ^ 1);  // buffer b^1 was last read before the previous barrier
     __syncthreads();
   }
+  // tokens this CTA finishes: all 32, or its block of kRouterOwn within the cluster's tile
+  const int q_lo = kSplit ? crank * kRouterOwn : 0;
+  const int q_n = kSplit ? kRouterOwn : kRouterTok;
+  if constexpr (kSplit) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+    for (int j = 0; j < 4; ++j)  // token tq + 8j of the tile is row tq of rank j's block
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float h = acc[i][j] + (b1 ? b1[4 * tu + j] : 0.f);
-      hid[2 * tq + i][4 * tu + j] = h > 0.f ? h : 0.f;
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint32_t local = smem_u32(&slots[crank][tq][4 * tu + jj]);
+        st_cluster_f32(dsmem_addr(local, (uint32_t)j), acc[j][jj]);
+      }
+    cluster_sync();  // every rank's partials have landed; nothing remote after this
+    for (int idx = tid; idx < kRouterOwn * kRouterHidden; idx += kRouterThreads) {
+      const int ql = idx / kRouterHidden, u = idx % kRouterHidden;
+      float h = 0.f;
+#pragma unroll
+      for (int p = 0; p < kRouterSplit; ++p) h += slots[p][ql][u];
+      h += b1 ? b1[u] : 0.f;
+      hid[ql][u] = h > 0.f ? h : 0.f;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float h = acc[j][jj] + (b1 ? b1[4 * tu + jj] : 0.f);
+        hid[tq + 8 * j][4 * tu + jj] = h > 0.f ? h : 0.f;
+      }
+  }
   __syncthreads();
-  for (int idx = tid; idx < kRouterTok * K; idx += kRouterThreads) {
+  // hid rows 0..q_n-1 are tokens t0 + q_lo + 0..q_n-1
+  const int64_t tb = t0 + q_lo;
+  for (int idx = tid; idx < q_n * K; idx += kRouterThreads) {
     const int q = idx / K, a = idx % K;
     float s = 0.f;
     for (int jj = 0; jj < kRouterHidden; ++jj) s = fmaf(hid[q][jj], to_f(W2[jj * K + a]), s);
     if (b2) s += b2[a];
     lg[q][a] = s;
-    if (logits && t0 + q < N) logits[(t0 + q) * K + a] = s;
+    if (logits && tb + q < N) logits[(tb + q) * K + a] = s;
   }
   __syncthreads();
-  if (tid < kRouterTok && t0 + tid < N) {
+  if (tid < q_n && tb + tid < N) {
     const int q = tid;
-    const int64_t t = t0 + q;
+    const int64_t t = tb + q;
     uint64_t used = 0;
     float m = 0.f, denom = 0.f;
     for (int js = 0; js < k; ++js) {
@@ -451,14 +535,33 @@ __global__ void __launch_bounds__(kRouterThreads)
 cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, int32_t d_in, const void* W1,
                                  const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,
                                  float* logits, int32_t* ids, float* w, cudaStream_t stream) {
-  const unsigned grid = (unsigned)((N + kRouterTok - 1) / kRouterTok);
-  if (dtype == MOLORA_BF16)
-    return launch_kernel(router_scalar_kernel<__nv_bfloat16>, dim3(grid), dim3(kRouterThreads), 0, stream, 0,
-                         static_cast<const __nv_bfloat16*>(x), N, d_in, static_cast<const __nv_bfloat16*>(W1), b1,
-                         static_cast<const __nv_bfloat16*>(W2), b2, K, k, logits, ids, w);
-  return launch_kernel(router_scalar_kernel<float>, dim3(grid), dim3(kRouterThreads), 0, stream, 0, static_cast<const float*>(x),
-                       N, d_in, static_cast<const float*>(W1), b1, static_cast<const float*>(W2), b2, K, k, logits, ids,
-                       w);
+  const int64_t tiles = (N + kRouterTok - 1) / kRouterTok;
+  // a cluster per tile while the CTAs stay within about six per SM and every rank has a chunk
+  bool split = tiles * kRouterSplit <= 6 * (int64_t)num_sms() && d_in >= kRouterSplit * kRouterChunk;
+#ifdef MOLORA_TUNING_ENV
+  if (const char* e = getenv("MOLORA_ROUTER_SCALAR_SPLIT")) split = split && atoi(e) != 0;
+#endif
+  const unsigned grid = (unsigned)(tiles * (split ? kRouterSplit : 1));
+  // whole 4-element groups of x rows and W1 rows, 16-byte (fp32) or 8-byte (bf16) aligned
+  const uintptr_t align = dtype == MOLORA_BF16 ? 8 : 16;
+  const int vec = d_in % 4 == 0 && (uintptr_t)x % align == 0 && (uintptr_t)W1 % align == 0;
+  const int cluster = split ? kRouterSplit : 0;
+  if (dtype == MOLORA_BF16) {
+    const auto* xp = static_cast<const __nv_bfloat16*>(x);
+    const auto* w1 = static_cast<const __nv_bfloat16*>(W1);
+    const auto* w2 = static_cast<const __nv_bfloat16*>(W2);
+    return split ? launch_kernel(router_scalar_kernel<__nv_bfloat16, true>, dim3(grid), dim3(kRouterThreads), 0, stream,
+                                 cluster, xp, N, d_in, w1, b1, w2, b2, K, k, logits, ids, w, vec)
+                 : launch_kernel(router_scalar_kernel<__nv_bfloat16, false>, dim3(grid), dim3(kRouterThreads), 0, stream,
+                                 0, xp, N, d_in, w1, b1, w2, b2, K, k, logits, ids, w, vec);
+  }
+  const auto* xp = static_cast<const float*>(x);
+  const auto* w1 = static_cast<const float*>(W1);
+  const auto* w2 = static_cast<const float*>(W2);
+  return split ? launch_kernel(router_scalar_kernel<float, true>, dim3(grid), dim3(kRouterThreads), 0, stream, cluster,
+                               xp, N, d_in, w1, b1, w2, b2, K, k, logits, ids, w, vec)
+               : launch_kernel(router_scalar_kernel<float, false>, dim3(grid), dim3(kRouterThreads), 0, stream, 0, xp,
+                               N, d_in, w1, b1, w2, b2, K, k, logits, ids, w, vec);
 }
 
 }  // namespace molora
