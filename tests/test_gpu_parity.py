@@ -1015,7 +1015,8 @@ def test_router_topk_vs_oracle(m, name, kw, k):
                                      (1000, 1000),  # a cluster of 4 per tile, ragged chunk and tile
                                      (77, 160),     # 5 chunks over 4 ranks: the last rank has none
                                      (4099, 2048),  # 129 tiles, each split over 4 CTAs
-                                     (8000, 256)])  # 250 tiles: past the split's CTA budget
+                                     (8000, 256),   # 250 tiles of a short d_in: one CTA per tile
+                                     (300, 1030)])  # d_in % 4 != 0: element-wise loads, split
 def test_router_fp32_and_biases(m, N, d_in):
     wl = workloads.make("topk_mlp", N=N, d_in=d_in, d_out=256, dtype=torch.float32, k=2)
     g = torch.Generator().manual_seed(3)

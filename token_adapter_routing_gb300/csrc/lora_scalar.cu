@@ -536,8 +536,13 @@ cudaError_t launch_router_scalar(const void* x, molora_dtype dtype, int64_t N, i
                                  const float* b1, const void* W2, const float* b2, int32_t K, int32_t k,
                                  float* logits, int32_t* ids, float* w, cudaStream_t stream) {
   const int64_t tiles = (N + kRouterTok - 1) / kRouterTok;
-  // a cluster per tile while the CTAs stay within about six per SM and every rank has a chunk
-  bool split = tiles * kRouterSplit <= 6 * (int64_t)num_sms() && d_in >= kRouterSplit * kRouterChunk;
+  // A cluster per tile where it pays (measured over N = 64..32768, d_in = 256..4096): a long d_in
+  // (16+ chunks per rank), a grid of fewer tiles than SMs with 8+ chunks per rank, or tiles for
+  // at most half the SMs.  Otherwise one CTA per tile: with 4-8 chunks per rank and the SMs
+  // already busy, the cluster's exchange costs more than the CTAs it adds.
+  const int64_t sms = num_sms();
+  bool split = d_in >= kRouterSplit * kRouterChunk &&
+               (d_in >= 2048 || (d_in >= 1024 && tiles < sms) || 2 * tiles <= sms);
 #ifdef MOLORA_TUNING_ENV
   if (const char* e = getenv("MOLORA_ROUTER_SCALAR_SPLIT")) split = split && atoi(e) != 0;
 #endif
