@@ -1030,6 +1030,19 @@ def test_router_fp32_and_biases(m, N, d_in):
     assert torch.equal(ids.cpu()[clear], ref_ids[clear])
 
 
+@pytest.mark.parametrize("N,d_in", [(4099, 2048), (8000, 256)])
+def test_router_fp32_reproducible(m, N, d_in):
+    # the split CUDA-core router adds the cluster's partials in rank order, and the unsplit one
+    # sums over d_in in order: logits, ids and w are bit-identical from call to call
+    wl = workloads.make("topk_mlp", N=N, d_in=d_in, d_out=256, dtype=torch.float32, k=2)
+    x, W1, W2 = dev(wl.x), dev(wl.W1), dev(wl.W2)
+    first = m.molora_router_topk(x, W1, W2, 2)
+    for _ in range(3):
+        again = m.molora_router_topk(x, W1, W2, 2)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
 def test_router_ties_lower_index_first(m):
     wl = workloads.make("topk_mlp", N=256, k=2)
     W2 = wl.W2.clone()
