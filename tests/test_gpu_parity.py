@@ -1023,11 +1023,9 @@ def test_router_fp32_and_biases(m, N, d_in):
     b1 = torch.randn(64, generator=g) * 0.1
     b2 = torch.randn(wl.K, generator=g) * 0.1
     logits, ids, w = m.molora_router_topk(dev(wl.x), dev(wl.W1), dev(wl.W2), 2, b1=dev(b1), b2=dev(b2))
-    ref_logits, ref_ids, ref_w = oracle.router_topk(wl.x, wl.W1, wl.W2, 2, b1, b2)
-    assert torch.allclose(logits.cpu(), ref_logits, rtol=1e-4, atol=1e-4)
-    srt = torch.sort(ref_logits.double(), dim=1, descending=True).values
-    clear = (srt[:, 1] - srt[:, 2]) > 1e-3
-    assert torch.equal(ids.cpu()[clear], ref_ids[clear])
+    torch.cuda.synchronize()
+    # logits, exact ids on clear tokens, weights within 1e-5 relative, a valid top k elsewhere
+    check_router(wl, 2, logits, ids, w, b1=b1, b2=b2)
 
 
 @pytest.mark.parametrize("N,d_in", [(4099, 2048), (8000, 256)])
