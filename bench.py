@@ -71,6 +71,7 @@ def parse_args(argv=None):
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     p.add_argument("--topk-k", default="1,2,3,4", help="--mode topk: comma-separated k values")
+    p.add_argument("--ranks", default="16", help="--mode crossover: comma-separated adapter ranks (8, 16, 32, 64)")
     p.add_argument("--topk-arms", default="fused_stacked,grouped,router",
                    help="--mode topk: which of fused_stacked, grouped, router to time")
     return p.parse_args(argv)
@@ -599,7 +600,8 @@ def _pct(v, q):
 def run_mode(args):
     """Extra measurements, one JSON line per point:
     crossover  decode sweep (Figures 5 and 9): batch 1..2048 x K 4..64 hot-set adapters, d=4096,
-               r=16, top-1, uniform and Zipf(1.1) adapter draws: route_vocab -> scalar apply,
+               rank r in --ranks (16 by default; the figures use 64), top-1, uniform and Zipf(1.1)
+               adapter draws: route_vocab -> scalar apply,
                and route_vocab_dispatch -> grouped apply; each point timed cold (a CUDA graph
                per call, L2 flushed before each replay, p50 -- the GPU's event clock ticks in
                about 2 us here) and warm (50 calls back to back in one graph, the decode
@@ -972,17 +974,17 @@ def run_mode(args):
                     emit(row)
                     del x, A, B, y, ids, w, ws
     elif args.mode == "crossover":
-        for dist in ("uniform", "zipf"):
+        for r, dist in ((r, dist) for r in (int(v) for v in args.ranks.split(",")) for dist in ("uniform", "zipf")):
             for K in (4, 8, 16, 32, 64):
-                for b in (1, 8, 32, 64, 128, 160, 256, 512, 768, 1024, 1536, 2048):
-                    wl = workloads.make("decode_sweep", N=b, K=K, dist=dist)
+                for b in (1, 8, 32, 64, 128, 160, 256, 384, 512, 768, 1024, 1536, 2048):
+                    wl = workloads.make("decode_sweep", N=b, K=K, r=r, dist=dist)
                     tok, starts = wl.tok.to(dev), wl.starts.to(dev)
                     x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
                     adapter = torch.empty(b, dtype=torch.int32, device=dev)
                     counts = torch.empty(K, dtype=torch.int32, device=dev)
                     offsets = torch.empty(K + 1, dtype=torch.int32, device=dev)
                     perm = torch.empty(b, dtype=torch.int32, device=dev)
-                    row = {"mode": "crossover", "dist": dist, "K": K, "batch": b}
+                    row = {"mode": "crossover", "dist": dist, "K": K, "r": r, "batch": b}
                     for path in ("scalar", "grouped"):
                         def fn(path=path):
                             # each path with the routing it needs: the token-major scalar apply

@@ -74,10 +74,11 @@ typedef enum { MOLORA_F32 = 0, MOLORA_BF16 = 1 } molora_dtype;
 /* Which kernel family molora_lora_apply_ex uses.  AUTO, given a workspace, picks the stacked
  * path where it measured faster than dispatch + grouped (a stacked rank K*r of at least 256,
  * few adapters per selected one, enough tokens); else the dense path for k >= 2 when it
- * applies and is measured faster; else the scalar or grouped path by their measured
- * crossover (Figures 5 and 9 put it near batch 160 on the paper's hardware; this library
- * measures its own and stores the result in its dispatch table).  AUTO takes the grouped
- * path only when the dispatch outputs are given. */
+ * applies and is measured faster; else the scalar or grouped path by their crossover, measured
+ * on GB300 by rank and hot-set size: from 160 tokens for 8 adapters of rank 64 (where Figures 5
+ * and 9 put it, near batch 160), 768-2048 at rank 32, 768-2048 at rank 16 (scalar only beyond
+ * 32 adapters of rank 16).  AUTO takes the grouped path only when the dispatch outputs are
+ * given. */
 typedef enum {
   MOLORA_PATH_AUTO = 0,
   MOLORA_PATH_SCALAR = 1,  /* CUDA-core, token-major, one CTA per token (the memory-bound regime) */

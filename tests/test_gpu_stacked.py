@@ -235,6 +235,19 @@ def test_auto_stacked_or_grouped_follows_the_measured_crossover(m, N, K, r, k, w
     assert m.molora_select_path(torch.bfloat16, N, 4096, 4096, K, r, k) == want
 
 
+@pytest.mark.parametrize("N,K,r,want", [(128, 8, 64, "scalar"), (160, 8, 64, "grouped"), (384, 16, 64, "scalar"),
+                                        (512, 16, 64, "grouped"), (512, 32, 64, "scalar"), (768, 32, 64, "grouped"),
+                                        (768, 64, 64, "scalar"), (1024, 64, 64, "grouped"), (512, 16, 32, "scalar"),
+                                        (768, 16, 32, "grouped"), (1024, 32, 32, "scalar"), (1536, 32, 32, "grouped"),
+                                        (512, 8, 16, "scalar"), (768, 8, 16, "grouped"), (768, 16, 16, "scalar"),
+                                        (2048, 64, 16, "scalar")])
+def test_auto_scalar_or_grouped_by_rank(m, N, K, r, want):
+    """Top-1 at d = 4096: the scalar path re-reads a token's adapter from L2 per token, so the
+    measured crossover to the grouped path falls with the rank (near batch 160 for 8 adapters of
+    rank 64, as Figures 5 and 9 find)."""
+    assert m.molora_select_path(torch.bfloat16, N, 4096, 4096, K, r, 1) == want
+
+
 @pytest.mark.parametrize("with_ws", [True, False])
 def test_auto_without_dispatch_outputs_picks_a_path_that_needs_none(m, with_ws):
     """A shape where AUTO prefers the grouped path, called without counts/offsets/perm: AUTO

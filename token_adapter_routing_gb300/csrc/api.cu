@@ -24,13 +24,29 @@ static bool valid_dtype(molora_dtype d) { return d == MOLORA_F32 || d == MOLORA_
 static molora_status launched(cudaError_t e) { return e == cudaSuccess ? MOLORA_OK : MOLORA_ERR_CUDA; }
 
 // Smallest slot count (N*k) at which the grouped tensor-core apply beats the scalar apply,
-// measured on GB300 with the decode sweep (d = 4096, r = 16, top-1, batch 1..2048, uniform
-// and Zipf(1.1) adapter draws; vocabulary routing -> scalar apply against routing with
-// dispatch -> grouped apply; 50 calls back to back in one CUDA graph, the decode steady
-// state with the hot set in L2).  The scalar path wins every batch up to 512; the grouped
-// path wins from 768 tokens with up to 8 hot-set adapters, from 1024 with 16, at 2048 with
-// 32 under uniform draws; with 64 the scalar path wins at every batch measured.
-static int64_t crossover_tokens(int32_t K) {
+// measured on GB300 with the decode sweep (d = 4096, top-1, batch 1..2048, K = 4..64 hot-set
+// adapters drawn uniformly and Zipf(1.1); vocabulary routing -> scalar apply against routing with
+// dispatch -> grouped apply; calls back to back in one CUDA graph, the decode steady state with
+// the hot set in L2).  The scalar path re-reads its token's A_a and B_a (d_in r + r d_out
+// elements) from L2 for every token, so the crossover falls as the rank grows:
+//   r <= 16: 768 tokens up to 8 adapters, 1024 with 16, 2048 with 32; scalar at every batch
+//            measured with 64;
+//   r = 32:  768 up to 16 adapters, 1536 with 32 (768 under uniform draws, 1536 under Zipf),
+//            2048 with 64;
+//   r = 64:  160 up to 8 adapters (Figures 5 and 9 put it near batch 160 for 8 adapters of rank
+//            64), 512 with 16, 768 with 32, 1024 with 64.
+static int64_t crossover_tokens(int32_t K, int32_t r) {
+  if (r >= 64) {
+    if (K <= 8) return 160;
+    if (K <= 16) return 512;
+    if (K <= 32) return 768;
+    return 1024;
+  }
+  if (r >= 32) {
+    if (K <= 16) return 768;
+    if (K <= 32) return 1536;
+    return 2048;
+  }
   if (K <= 8) return 768;
   if (K <= 16) return 1024;
   if (K <= 32) return 2048;
@@ -62,7 +78,7 @@ static molora_path select_without_ws(molora_dtype dtype, int64_t N, int32_t d_in
                                      int32_t r, int32_t k, bool table) {
   if (!table && k >= 2 && dense_preferred(dtype, N, d_in, d_out, K, r)) return MOLORA_PATH_DENSE;
   if (!grouped_supported(dtype, N, d_in, d_out, K, r, k)) return MOLORA_PATH_SCALAR;
-  return N * (int64_t)k >= crossover_tokens(K) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
+  return N * (int64_t)k >= crossover_tokens(K, r) ? MOLORA_PATH_GROUPED : MOLORA_PATH_SCALAR;
 }
 
 // Workspace convention (include/molora.h): ws_bytes == NULL -> none; ws == NULL -> query;
