@@ -71,7 +71,8 @@ def parse_args(argv=None):
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     p.add_argument("--topk-k", default="1,2,3,4", help="--mode topk: comma-separated k values")
-    p.add_argument("--ranks", default="16", help="--mode crossover: comma-separated adapter ranks (8, 16, 32, 64)")
+    p.add_argument("--ranks", default="16",
+                   help="--mode crossover / perseq: comma-separated adapter ranks (8, 16, 32, 64)")
     p.add_argument("--topk-arms", default="fused_stacked,grouped,router",
                    help="--mode topk: which of fused_stacked, grouped, router to time")
     return p.parse_args(argv)
@@ -623,7 +624,8 @@ def run_mode(args):
                dense apply; router and dense apply fused in one kernel
                (molora_router_lora_apply); and each apply alone.
     perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
-               passes over all tokens against one per-token pass.
+               passes over all tokens against one per-token pass, at each rank in --ranks
+               (Table 3 uses 64).
     skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
                80/10/5/5, 95/2/2/1 modality shares per run): the apply alone and the whole step,
                back to back over six batches as in the main line.
@@ -1182,28 +1184,30 @@ def run_mode(args):
               "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 3) if peak else None,
               "timing": "20 calls back to back in one CUDA graph (x is 33.6 MB: L2-resident)"})
     elif args.mode == "perseq":
-        wl = workloads.make(WORKLOAD)
-        tok, starts = wl.tok.to(dev), wl.starts.to(dev)
-        x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
-        adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
-        counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
-        offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
-        perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
+        for r in (int(v) for v in args.ranks.split(",")):
+            wl = workloads.make(WORKLOAD, r=r)
+            tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+            x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+            adapter = torch.empty(wl.N, dtype=torch.int32, device=dev)
+            counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+            offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(wl.N, dtype=torch.int32, device=dev)
 
-        def per_token():
-            m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
-            m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
+            def per_token():
+                m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
+                m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
 
-        def per_sequence():
-            m.molora_route_vocab(tok, starts, adapter=adapter)
-            for a in range(wl.K):
-                m.molora_lora_apply_masked_pass(x, A, B, adapter, a, y, wl.scale)
-        t_ms = _replay_ms(_graph(per_token, stream), stream, 100, flush)
-        s_ms = _replay_ms(_graph(per_sequence, stream), stream, 100, flush)
-        emit({"mode": "perseq", "workload": "N=2048, d=4096, K=4, r=16 (4-modality benchmark)",
-              "per_token_us_p50": round(_pct(t_ms, 0.5) * 1e3, 2), "per_sequence_us_p50": round(_pct(s_ms, 0.5) * 1e3, 2),
-              "passes": {"per_token": 1, "per_sequence": wl.K},
-              "speedup": round(_pct(s_ms, 0.5) / _pct(t_ms, 0.5), 2), "l2": "flushed between replays"})
+            def per_sequence():
+                m.molora_route_vocab(tok, starts, adapter=adapter)
+                for a in range(wl.K):
+                    m.molora_lora_apply_masked_pass(x, A, B, adapter, a, y, wl.scale)
+            t_ms = _replay_ms(_graph(per_token, stream), stream, 100, flush)
+            s_ms = _replay_ms(_graph(per_sequence, stream), stream, 100, flush)
+            emit({"mode": "perseq", "workload": f"N=2048, d=4096, K=4, r={r} (4-modality benchmark shape)",
+                  "per_token_us_p50": round(_pct(t_ms, 0.5) * 1e3, 2),
+                  "per_sequence_us_p50": round(_pct(s_ms, 0.5) * 1e3, 2),
+                  "passes": {"per_token": 1, "per_sequence": wl.K},
+                  "speedup": round(_pct(s_ms, 0.5) / _pct(t_ms, 0.5), 2), "l2": "flushed between replays"})
     return 0
 
 

@@ -911,6 +911,21 @@ def test_masked_passes_equal_per_token(m, path):
     assert_apply_close(y_tok, y_ref)
 
 
+def test_masked_passes_auto_where_the_stacked_pair_is_preferred(m):
+    # Table 3's shape class (4 modalities, rank 64, 2048 tokens): with a workspace AUTO would take
+    # the stacked pair, which a masked pass (no workspace) cannot run; AUTO picks a kernel that
+    # needs none, and the per-sequence passes still equal the oracle
+    wl = workloads.make("modality4", N=2048, d_in=1024, d_out=1024, r=64)
+    assert m.molora_select_path(wl.dtype, wl.N, wl.d_in, wl.d_out, wl.K, wl.r, 1) == "stacked"
+    adapter = m.molora_route_vocab(dev(wl.tok), dev(wl.starts))
+    y_seq = dev(wl.y0).clone()
+    for a in range(wl.K):
+        m.molora_lora_apply_masked_pass(dev(wl.x), dev(wl.A), dev(wl.B), adapter, a, y_seq, wl.scale, path="auto")
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.per_sequence_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
+    assert_apply_close(y_seq, y_ref)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_sequence_split_passes_equal_per_token(m, path):
     # per-sequence routing that splits the batch into its single-modality runs (Table 6): one

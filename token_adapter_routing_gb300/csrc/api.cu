@@ -340,7 +340,8 @@ molora_status molora_lora_apply_masked_pass(const void* x, molora_dtype dtype, i
   if (st != MOLORA_OK) return st;
   if (a < 0 || a >= K) return MOLORA_ERR_INVALID_ARG;
   if (N == 0) return MOLORA_OK;
-  if (path == MOLORA_PATH_AUTO) path = molora_select_path(dtype, N, d_in, d_out, K, r, 1);
+  // a masked pass takes no workspace: AUTO chooses between the scalar and grouped kernels
+  if (path == MOLORA_PATH_AUTO) path = select_without_ws(dtype, N, d_in, d_out, K, r, 1, false);
   if (path == MOLORA_PATH_SCALAR)
     return launched(launch_lora_scalar(x, dtype, N, d_in, d_out, A, B, K, r, adapter_of, nullptr, 1, scale, y, false,
                                        a, err_word, stream));
