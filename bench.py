@@ -72,7 +72,7 @@ def parse_args(argv=None):
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
     p.add_argument("--topk-k", default="1,2,3,4", help="--mode topk: comma-separated k values")
     p.add_argument("--ranks", default="16",
-                   help="--mode crossover / perseq: comma-separated adapter ranks (8, 16, 32, 64)")
+                   help="--mode crossover / perseq / tiling: comma-separated adapter ranks (8, 16, 32, 64)")
     p.add_argument("--topk-arms", default="fused_stacked,grouped,router",
                    help="--mode topk: which of fused_stacked, grouped, router to time")
     return p.parse_args(argv)
@@ -806,9 +806,15 @@ def run_mode(args):
             if TM:
                 os.environ["MOLORA_TILE_ROWS"] = str(TM)
 
-        cases = [(WORKLOAD, {"dist": d}) for d in ("uniform", "80-10-5-5", "95-2-2-1")]
-        cases += [("decode_sweep", {"N": b, "K": K}) for K in (8, 16, 32, 64) for b in (256, 512, 1024, 2048)]
-        cases += [("decode_sweep", {"N": b, "K": K, "dist": "zipf"}) for K in (32, 64) for b in (512, 2048)]
+        ranks = [int(v) for v in args.ranks.split(",")]
+        cases = []
+        if 16 in ranks:
+            cases += [(WORKLOAD, {"dist": d}) for d in ("uniform", "80-10-5-5", "95-2-2-1")]
+            cases += [("decode_sweep", {"N": b, "K": K}) for K in (8, 16, 32, 64) for b in (256, 512, 1024, 2048)]
+            cases += [("decode_sweep", {"N": b, "K": K, "dist": "zipf"}) for K in (32, 64) for b in (512, 2048)]
+        # other ranks: a grid over the batch (at rank 64 and d = 4096 the plans run one CTA per SM)
+        cases += [("decode_sweep", {"N": b, "K": K, "r": r}) for r in ranks if r != 16 for K in (4, 8, 16, 32)
+                  for b in (512, 768, 1024, 1280, 1536, 1792, 2048, 3072, 4096)]
         for name, kw in cases:
             wl = workloads.make(name, **kw)
             tok, starts = wl.tok.to(dev), wl.starts.to(dev)
@@ -827,7 +833,7 @@ def run_mode(args):
                 m.molora_route_vocab(tok, starts, adapter=adapter)
                 m.molora_lora_apply(x, A, B, adapter, y, wl.scale, path="scalar")
 
-            res = {"mode": "tiling", "workload": name, "N": wl.N, "K": wl.K, "dist": kw.get("dist", "uniform"),
+            res = {"mode": "tiling", "workload": name, "N": wl.N, "K": wl.K, "r": wl.r, "dist": kw.get("dist", "uniform"),
                    "unit": "us per step"}
             force()
             res["scalar"] = round(loop_us(scalar_step), 2)

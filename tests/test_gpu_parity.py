@@ -911,6 +911,17 @@ def test_masked_passes_equal_per_token(m, path):
     assert_apply_close(y_tok, y_ref)
 
 
+@pytest.mark.parametrize("K,N", [(8, 1024), (4, 1536), (16, 1280)])
+def test_grouped_rank64_one_cta_per_sm_plans(m, K, N):
+    # rank 64 at d = 4096: the grouped plan runs one CTA per SM and picks its tile rows by the
+    # waves of resident clusters (128 rows for the first two shapes, 64 for the third)
+    wl = workloads.make("decode_sweep", N=N, K=K, r=64)
+    adapter, counts, offsets, perm, y, e = run_vocab_path(m, wl, "grouped")
+    assert e == 0
+    y_ref, _ = oracle.lora_apply(wl.x, wl.A, wl.B, oracle_adapter(wl, adapter), wl.y0, wl.scale)
+    assert_apply_close(y, y_ref)
+
+
 def test_masked_passes_auto_where_the_stacked_pair_is_preferred(m):
     # Table 3's shape class (4 modalities, rank 64, 2048 tokens): with a workspace AUTO would take
     # the stacked pair, which a masked pass (no workspace) cannot run; AUTO picks a kernel that

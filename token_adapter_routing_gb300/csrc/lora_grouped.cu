@@ -169,7 +169,20 @@ bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, Groupe
   const int64_t sms = num_sms();
   const int64_t tiles64 = (S + 63) / 64;
   const int64_t running64 = tiles64 + (K + 1) / 2;  // 64-row tiles that run (empty ones leave)
-  const int pref_tm = (running64 * 8 > 2 * sms && 2 * tiles64 >= K) ? 128 : 64;
+  int pref_tm = (running64 * 8 > 2 * sms && 2 * tiles64 >= K) ? 128 : 64;
+  GroupedPlan probe;
+  if (!plan_one(d_in, d_out, r, 8, 64, true, &probe)) {
+    // One CTA per SM (rank 64 at d = 4096: the B slice, staging and receive slots take an SM's
+    // shared memory).  Then about sms / 9 clusters of 8 are resident at once (two per GPC of
+    // 18-20 SMs), and the time steps with the waves of launched clusters: take the tile rows
+    // with fewer waves, 64 rows on a tie.  Measured, rank 64, K = 4..32, 512..4096 tokens, 64
+    // vs 128 rows forced: this choice loses 31 us summed over 36 points, the two-per-SM rule
+    // above 103 us (e.g. 4 adapters, 1536 tokens: 25.8 us with 128 rows, 36.7 with 64).
+    const int64_t wave = sms / 9 > 0 ? sms / 9 : 1;
+    const int64_t w64 = (tiles64 + K + wave - 1) / wave;
+    const int64_t w128 = ((S + 127) / 128 + K + wave - 1) / wave;
+    pref_tm = w128 < w64 ? 128 : 64;
+  }
   // (clusters of 4 measured with 64-row tiles only; large groups keep clusters of 8)
   const int pref_c = (pref_tm == 64 && (tiles64 + K) * 8 > 3 * sms) ? 4 : 8;
   const Cand preferred[] = {{pref_c, pref_tm, true}, {pref_c, pref_tm, false}};
