@@ -228,7 +228,9 @@ def test_full_size_topk_scaling_stacked(m, k):
 @pytest.mark.parametrize("N,K,r,k,want", [(2048, 16, 16, 1, "grouped"), (2048, 16, 16, 4, "stacked"),
                                           (8192, 8, 64, 1, "stacked"), (1024, 4, 64, 1, "grouped"),
                                           (1024, 4, 64, 2, "stacked"), (4096, 64, 16, 4, "stacked"),
-                                          (2048, 64, 16, 2, "grouped"), (8192, 16, 64, 1, "grouped")])
+                                          (2048, 64, 16, 2, "grouped"), (8192, 16, 64, 1, "grouped"),
+                                          (2048, 8, 64, 1, "grouped"), (4096, 8, 64, 1, "stacked"),
+                                          (2048, 64, 16, 4, "stacked")])
 def test_auto_stacked_or_grouped_follows_the_measured_crossover(m, N, K, r, k, want):
     """At d = 4096 AUTO (with a workspace) takes the stacked pair only where it measured faster
     than dispatch + grouped apply: few adapters per selected one, enough tokens."""

@@ -876,15 +876,17 @@ size_t stacked_workspace_bytes(int64_t N, int32_t K, int32_t r) { return 2 * g_b
 // (the pair does K/k times the grouped path's tensor work) and enough tokens for its tiles to
 // fill the GPU.  Measured on GB300 at d = 4096 (bench.py --mode crossover_stacked: K*r of 256,
 // 512 and 1024 with r = 16 and 64, k = 1, 2, 4, 1024..8192 tokens); this rule picks the faster
-// path at 70 of the 72 points (the misses: a tie, and one point within 7%).  With k = 1 the
-// grouped path gathers and reduces each token once, which is why it keeps small batches even
-// at K/k = 4.
+// path at 71 of the 72 points (the miss: a tie within 1%).  With k = 1 the grouped path gathers
+// and reduces each token once, which is why it keeps small batches even at K/k = 4, and 2048
+// tokens at K/k = 8 (8 adapters of rank 64: 46.3 vs 49.9 us, since the grouped plan counts
+// waves of resident clusters at that rank).
 bool stacked_preferred(molora_dtype dtype, int64_t N, int32_t d_in, int32_t d_out, int32_t K, int32_t r, int32_t k,
                        bool router) {
   if (K * r < 256 || k < 1) return false;
   const int32_t per_pick = (K + k - 1) / k;
-  const bool wins = (per_pick <= 4 && N >= 1024 && !(k == 1 && N < 2048)) || (per_pick <= 8 && N >= 2048) ||
-                    (per_pick <= 16 && k >= 2 && N >= 4096);
+  const bool wins = (per_pick <= 4 && N >= 1024 && !(k == 1 && N < 2048)) ||
+                    (per_pick <= 8 && N >= (k == 1 ? 4096 : 2048)) ||
+                    (per_pick <= 16 && k >= 2 && N >= (k >= 4 ? 2048 : 4096));
   return wins && stacked_supported(dtype, N, d_in, d_out, K, r, router);
 }
 
