@@ -66,7 +66,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--mode", choices=["step", "crossover", "crossover_topk", "crossover_stacked", "decode_step", "topk",
                                       "router", "perseq", "skew",
-                                      "bf16y", "indirect", "split", "kernels", "tiling"],
+                                      "bf16y", "indirect", "split", "kernels", "tiling", "cv"],
                    default="step",
                    help="step: the contract line; the others print extra measurement lines (see run_mode)")
     p.add_argument("--replays", type=int, default=1000, help="graph replays per point in --mode topk")
@@ -626,6 +626,11 @@ def run_mode(args):
     perseq     the per-sequence baseline on the 4-modality workload (Tables 3 and 4): K masked
                passes over all tokens against one per-token pass, at each rank in --ranks
                (Table 3 uses 64).
+    cv         step latency spread (Table 11): the decode step (route_vocab -> apply on the AUTO
+               path, d = 4096, r = 16, K = 16 hot-set adapters) at batch 32..256, issued eagerly
+               (two library calls) or as one CUDA graph replay, 1000 steps each, every step timed
+               on the host clock around launch + synchronize (the GPU event clock ticks in about
+               2 us here): mean, p50, p99 and the coefficient of variation.
     skew       the 4-modality workload with the group-size distributions of Table 9 (uniform,
                80/10/5/5, 95/2/2/1 modality shares per run): the apply alone and the whole step,
                back to back over six batches as in the main line.
@@ -1189,6 +1194,38 @@ def run_mode(args):
               "algorithmic_bytes": nbytes, "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
               "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 3) if peak else None,
               "timing": "20 calls back to back in one CUDA graph (x is 33.6 MB: L2-resident)"})
+    elif args.mode == "cv":
+        for b in (32, 64, 128, 256):
+            wl = workloads.make("decode_sweep", N=b, K=16)
+            tok, starts = wl.tok.to(dev), wl.starts.to(dev)
+            x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
+            adapter = torch.empty(b, dtype=torch.int32, device=dev)
+            counts = torch.empty(wl.K, dtype=torch.int32, device=dev)
+            offsets = torch.empty(wl.K + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(b, dtype=torch.int32, device=dev)
+
+            def step():
+                m.molora_route_vocab_dispatch(tok, starts, adapter=adapter, counts=counts, offsets=offsets, perm=perm)
+                m.molora_lora_apply(x, A, B, adapter, y, wl.scale, counts=counts, offsets=offsets, perm=perm)
+            g = _graph(step, stream)
+
+            def spread(fn, n=1000):
+                with torch.cuda.stream(stream):
+                    for _ in range(50):
+                        fn()
+                    stream.synchronize()
+                    ts = []
+                    for _ in range(n):
+                        t0 = time.perf_counter()
+                        fn()
+                        stream.synchronize()
+                        ts.append((time.perf_counter() - t0) * 1e6)
+                ts.sort()
+                mean = statistics.fmean(ts)
+                return {"mean_us": round(mean, 2), "p50_us": round(_pct(ts, 0.5), 2), "p99_us": round(_pct(ts, 0.99), 2),
+                        "cv": round(statistics.pstdev(ts) / mean, 3)}
+            emit({"mode": "cv", "batch": b, "K": wl.K, "r": wl.r, "eager": spread(step), "graph": spread(g.replay),
+                  "timing": "host clock around launch + synchronize, 1000 steps after 50 warm-up"})
     elif args.mode == "perseq":
         for r in (int(v) for v in args.ranks.split(",")):
             wl = workloads.make(WORKLOAD, r=r)
