@@ -627,7 +627,8 @@ def run_mode(args):
                passes over all tokens against one per-token pass, at each rank in --ranks
                (Table 3 uses 64).
     cv         step latency spread (Table 11): the decode step (route_vocab -> apply on the AUTO
-               path, d = 4096, r = 16, K = 16 hot-set adapters) at batch 32..256, issued eagerly
+               path, d = 4096, r = 16, K = 16 hot-set adapters drawn uniformly or Zipf(1.1) -- the
+               access patterns of Figure 8) at batch 32..256, issued eagerly
                (two library calls) or as one CUDA graph replay, 1000 steps each, every step timed
                on the host clock around launch + synchronize (the GPU event clock ticks in about
                2 us here): mean, p50, p99 and the coefficient of variation.
@@ -1195,8 +1196,8 @@ def run_mode(args):
               "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 3) if peak else None,
               "timing": "20 calls back to back in one CUDA graph (x is 33.6 MB: L2-resident)"})
     elif args.mode == "cv":
-        for b in (32, 64, 128, 256):
-            wl = workloads.make("decode_sweep", N=b, K=16)
+        for dist, b in ((dist, b) for dist in ("uniform", "zipf") for b in (32, 64, 128, 256)):
+            wl = workloads.make("decode_sweep", N=b, K=16, dist=dist)
             tok, starts = wl.tok.to(dev), wl.starts.to(dev)
             x, A, B, y = wl.x.to(dev), wl.A.to(dev), wl.B.to(dev), wl.y0.to(dev)
             adapter = torch.empty(b, dtype=torch.int32, device=dev)
@@ -1224,7 +1225,7 @@ def run_mode(args):
                 mean = statistics.fmean(ts)
                 return {"mean_us": round(mean, 2), "p50_us": round(_pct(ts, 0.5), 2), "p99_us": round(_pct(ts, 0.99), 2),
                         "cv": round(statistics.pstdev(ts) / mean, 3)}
-            emit({"mode": "cv", "batch": b, "K": wl.K, "r": wl.r, "eager": spread(step), "graph": spread(g.replay),
+            emit({"mode": "cv", "batch": b, "K": wl.K, "r": wl.r, "dist": dist, "eager": spread(step), "graph": spread(g.replay),
                   "timing": "host clock around launch + synchronize, 1000 steps after 50 warm-up"})
     elif args.mode == "perseq":
         for r in (int(v) for v in args.ranks.split(",")):
