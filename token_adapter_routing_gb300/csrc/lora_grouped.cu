@@ -171,7 +171,7 @@ bool choose(int32_t d_in, int32_t d_out, int32_t r, int64_t S, int32_t K, Groupe
   const int64_t running64 = tiles64 + (K + 1) / 2;  // 64-row tiles that run (empty ones leave)
   int pref_tm = (running64 * 8 > 2 * sms && 2 * tiles64 >= K) ? 128 : 64;
   GroupedPlan probe;
-  if (!plan_one(d_in, d_out, r, 8, 64, true, &probe)) {
+  if (!plan_one(d_in, d_out, r, 8, 64, true, &probe) && plan_one(d_in, d_out, r, 8, 64, false, &probe)) {
     // One CTA per SM (rank 64 at d = 4096: the B slice, staging and receive slots take an SM's
     // shared memory).  Then about sms / 9 clusters of 8 are resident at once (two per GPC of
     // 18-20 SMs), and the time steps with the waves of launched clusters: take the tile rows
